@@ -1,0 +1,140 @@
+"""The CPU oracle for C = A x B^T -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+legs of ``bench.py`` may import this package. The product path (the CUDA
+library and its Python binding) never imports it and shares no code with it.
+
+Contents:
+  * ``gemm_tn_reference``  -- the fp64 triple loop (C, ``gemm_oracle.c``): the
+    plain product ref = A x B^T and the magnitude sum bound = sum |a*b|.
+  * ``parity_report``      -- the element-wise pass criterion
+        |c - ref| <= 1e-2 * bound + 1e-3
+    with NaN/Inf anywhere in c counted as a failure.
+  * ``tiling_model``       -- the traffic / shared-memory model and the counted
+    tiled loop of "Tiling a matmul" (pure Python).
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py`` and
+``tests/test_tiling_model.py`` to values fixed by the pages or by mathematics
+(exact rational brute force, identity/permutation/integer closed forms, the
+pages' printed tables); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import build as _build
+
+__all__ = ["gemm_tn_reference", "parity_report", "ParityReport", "ALLOW_REL", "ALLOW_ABS",
+           "host_threads", "load_library"]
+
+#: The pass criterion's two constants: |c - ref| <= ALLOW_REL * bound + ALLOW_ABS.
+ALLOW_REL = 1e-2
+ALLOW_ABS = 1e-3
+
+_LIBS: dict[tuple, ctypes.CDLL] = {}
+
+
+def host_threads() -> int:
+    """Threads the oracle uses: every core this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover - non-Linux
+        return max(1, os.cpu_count() or 1)
+
+
+def load_library(plant: int = 0, out_dir=None) -> ctypes.CDLL:
+    """Load (building first if needed) the oracle's C library."""
+    key = (plant, str(out_dir))
+    lib = _LIBS.get(key)
+    if lib is not None:
+        return lib
+    path = _build.build(plant=plant, out_dir=out_dir)
+    lib = ctypes.CDLL(str(path))
+    fn = lib.oracle_gemm_tn_f64
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    _LIBS[key] = lib
+    return lib
+
+
+def _as_f64(x) -> np.ndarray:
+    """Widen an fp16/bf16 (torch or numpy) matrix exactly to a C-contiguous fp64
+    numpy array. Widening fp16 or bf16 to fp64 is exact."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().to("cpu", torch.float64).contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def gemm_tn_reference(a, b, nthreads: int | None = None, lib: ctypes.CDLL | None = None):
+    """ref, bound for C = A x B^T.
+
+    a: [M, K], b: [N, K] (torch or numpy; fp16/bf16/fp32/fp64 values, read
+    exactly as fp64). Returns two fp64 numpy arrays of shape [M, N]:
+    ref[i, j] = sum_k a[i, k] * b[j, k] summed in increasing k, and
+    bound[i, j] = sum_k |a[i, k] * b[j, k]|.
+    "0. A Minimal Hopper Matmul", section "Block Tiling" (C = A x B^T, A (M, K),
+    B (N, K)). ``lib`` selects another build of the C loop (the pinning tests
+    pass deliberately wrong builds); by default the real one is used.
+    """
+    A = _as_f64(a)
+    B = _as_f64(b)
+    if A.ndim != 2 or B.ndim != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError(f"expected A [M,K] and B [N,K], got {A.shape} and {B.shape}")
+    M, K = A.shape
+    N = B.shape[0]
+    ref = np.zeros((M, N), dtype=np.float64)
+    bound = np.zeros((M, N), dtype=np.float64)
+    if M and N:
+        lib = lib or load_library()
+        rc = lib.oracle_gemm_tn_f64(A.ctypes.data, B.ctypes.data, M, N, K,
+                                    ref.ctypes.data, bound.ctypes.data,
+                                    int(nthreads or host_threads()))
+        if rc != 0:
+            raise RuntimeError(f"oracle_gemm_tn_f64 failed with {rc}")
+    return ref, bound
+
+
+@dataclass
+class ParityReport:
+    ok: bool
+    max_ratio: float          # max over elements of |c - ref| / allowance
+    argmax: tuple             # (i, j) of that element
+    n_bad: int                # elements over the allowance or not finite
+    n_nonfinite: int
+    max_abs_err: float
+
+    def __str__(self) -> str:
+        return (f"ok={self.ok} max_ratio={self.max_ratio:.3e} at {self.argmax} "
+                f"bad={self.n_bad} nonfinite={self.n_nonfinite} max_abs_err={self.max_abs_err:.3e}")
+
+
+def parity_report(c, ref: np.ndarray, bound: np.ndarray) -> ParityReport:
+    """Apply the pass criterion |c - ref| <= 1e-2 * bound + 1e-3 element-wise.
+
+    c is the result under test (any dtype, widened to fp64); NaN or Inf in c
+    fails (the inputs of every workload are finite and in range).
+    """
+    C = _as_f64(c)
+    if C.shape != ref.shape:
+        raise ValueError(f"shape mismatch {C.shape} vs {ref.shape}")
+    if C.size == 0:
+        return ParityReport(True, 0.0, (), 0, 0, 0.0)
+    finite = np.isfinite(C)
+    err = np.abs(C - ref)
+    allow = ALLOW_REL * bound + ALLOW_ABS
+    ratio = np.where(finite, err / allow, np.inf)
+    flat = int(np.argmax(ratio))
+    idx = tuple(int(v) for v in np.unravel_index(flat, ratio.shape))
+    bad = ~(ratio <= 1.0)
+    max_abs = float(np.max(np.where(finite, err, 0.0)))
+    return ParityReport(bool(not bad.any()), float(ratio.flat[flat]), idx, int(bad.sum()),
+                        int((~finite).sum()), max_abs)

@@ -1,0 +1,198 @@
+"""Pins for the fp64 oracle of C = A x B^T, against things other than itself.
+
+* exact rational arithmetic (brute force) on tiny and odd shapes: every fp16 or
+  bf16 value is a dyadic rational, so the true sum is known exactly;
+* closed forms: identity and permutation matrices reproduce A exactly; all-ones
+  operands give K everywhere; small-integer operands give the exact integer
+  product (checked with integer matrix multiplication, a library routine);
+* the pass criterion itself: the oracle rounded to the output dtype passes with
+  a wide margin, a single element moved by twice its allowance fails, NaN fails;
+* planted mistakes: deliberately wrong builds of the C loop (a dropped term, an
+  un-transposed B, a flipped sign, swapped output indices) each fail at least
+  one of the pins above.
+
+"0. A Minimal Hopper Matmul", section "Block Tiling": C = A x B^T with A (M, K)
+and B (N, K). "Tiling a matmul", section "Where it breaks" (numerical order):
+tiling changes only the order of additions, so any correct order lands within
+the summation error bound of the exact value.
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import build as oracle_build
+
+U = 2.0 ** -53  # unit roundoff of fp64
+
+
+def _rand(shape, dtype, seed, kind="uniform"):
+    g = np.random.Generator(np.random.PCG64(seed))
+    x = g.uniform(-1.0, 1.0, size=shape).astype(np.float32) if kind == "uniform" else \
+        g.integers(-2, 3, size=shape).astype(np.float32)
+    return torch.from_numpy(x).to(dtype)
+
+
+def _exact(a: torch.Tensor, b: torch.Tensor):
+    """Exact C = A x B^T and sum |a*b| with Fractions."""
+    A = [[Fraction(float(v)) for v in row] for row in a.to(torch.float64).tolist()]
+    B = [[Fraction(float(v)) for v in row] for row in b.to(torch.float64).tolist()]
+    M, N, K = len(A), len(B), a.shape[1]
+    ref = [[sum((A[i][k] * B[j][k] for k in range(K)), Fraction(0)) for j in range(N)] for i in range(M)]
+    mag = [[sum((abs(A[i][k] * B[j][k]) for k in range(K)), Fraction(0)) for j in range(N)] for i in range(M)]
+    return ref, mag
+
+
+def _gamma(k: int) -> float:
+    """gamma_k = k u / (1 - k u): the recursive-summation error factor."""
+    return k * U / (1.0 - k * U)
+
+
+TINY = [(1, 1, 1), (2, 3, 1), (3, 2, 7), (7, 16, 17), (16, 7, 33), (17, 33, 16),
+        (33, 17, 65), (1, 65, 127), (65, 1, 129), (2, 2, 129)]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("mnk", TINY)
+def test_bruteforce_exact_rational(mnk, dtype):
+    m, n, k = mnk
+    a = _rand((m, k), dtype, 11 + m + 3 * n + 7 * k)
+    b = _rand((n, k), dtype, 13 + m + 5 * n + 11 * k)
+    ref, bound = oracle.gemm_tn_reference(a, b)
+    exact, mag = _exact(a, b)
+    g = _gamma(k)
+    for i in range(m):
+        for j in range(n):
+            # products are exact in fp64; only the K-term summation rounds
+            assert abs(Fraction(ref[i, j]) - exact[i][j]) <= Fraction(g) * mag[i][j]
+            assert abs(Fraction(bound[i, j]) - mag[i][j]) <= Fraction(g) * mag[i][j]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_identity_reproduces_a_exactly(dtype):
+    m, k = 37, 53
+    a = _rand((m, k), dtype, 5)
+    eye = torch.eye(k, dtype=dtype)
+    ref, bound = oracle.gemm_tn_reference(a, eye)
+    np.testing.assert_array_equal(ref, a.double().numpy())
+    np.testing.assert_array_equal(bound, a.double().abs().numpy())
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_permutation_reproduces_columns_exactly(dtype):
+    m, k = 29, 41
+    a = _rand((m, k), dtype, 6)
+    perm = np.random.Generator(np.random.PCG64(7)).permutation(k)
+    p = torch.zeros((k, k), dtype=dtype)
+    p[torch.arange(k), torch.from_numpy(perm)] = 1  # row j of B selects column perm[j] of A
+    ref, _ = oracle.gemm_tn_reference(a, p)
+    np.testing.assert_array_equal(ref, a.double().numpy()[:, perm])
+
+
+@pytest.mark.parametrize("mnk", [(1, 1, 1), (5, 3, 256), (3, 5, 4097), (16, 16, 8192)])
+def test_all_ones_gives_k(mnk):
+    m, n, k = mnk
+    ref, bound = oracle.gemm_tn_reference(torch.ones((m, k), dtype=torch.float16),
+                                          torch.ones((n, k), dtype=torch.float16))
+    assert (ref == k).all() and (bound == k).all()
+
+
+@pytest.mark.parametrize("mnk", [(24, 24, 24), (31, 17, 45), (17, 31, 64), (40, 40, 300)])
+def test_small_integers_give_exact_integer_product(mnk):
+    m, n, k = mnk
+    a = _rand((m, k), torch.float16, 100 + m, kind="int")
+    b = _rand((n, k), torch.float16, 200 + n, kind="int")
+    ref, bound = oracle.gemm_tn_reference(a, b)
+    ai = a.to(torch.int64).numpy()
+    bi = b.to(torch.int64).numpy()
+    np.testing.assert_array_equal(ref, (ai @ bi.T).astype(np.float64))
+    np.testing.assert_array_equal(bound, (np.abs(ai) @ np.abs(bi).T).astype(np.float64))
+    if m == n == k:  # the product of a non-symmetric pair differs from A x B
+        assert not np.array_equal(ref, (ai @ bi).astype(np.float64))
+
+
+def test_thread_count_does_not_change_results():
+    a = _rand((67, 129), torch.bfloat16, 1)
+    b = _rand((45, 129), torch.bfloat16, 2)
+    r1, b1 = oracle.gemm_tn_reference(a, b, nthreads=1)
+    r8, b8 = oracle.gemm_tn_reference(a, b, nthreads=8)
+    np.testing.assert_array_equal(r1, r8)
+    np.testing.assert_array_equal(b1, b8)
+
+
+def test_empty_shapes():
+    ref, bound = oracle.gemm_tn_reference(torch.zeros((0, 5)), torch.zeros((3, 5)))
+    assert ref.shape == (0, 3)
+    ref, bound = oracle.gemm_tn_reference(torch.zeros((4, 0)), torch.zeros((3, 0)))
+    assert ref.shape == (4, 3) and (ref == 0).all() and (bound == 0).all()
+
+
+# ---------------------------------------------------------------- pass criterion
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_criterion_accepts_rounded_oracle(dtype):
+    a = _rand((64, 300), dtype, 3)
+    b = _rand((48, 300), dtype, 4)
+    ref, bound = oracle.gemm_tn_reference(a, b)
+    rounded = torch.from_numpy(ref).to(dtype)
+    rep = oracle.parity_report(rounded, ref, bound)
+    assert rep.ok and rep.max_ratio < 0.25, rep
+
+
+def test_criterion_rejects_perturbation_and_nan():
+    a = _rand((16, 64), torch.float32, 8)
+    b = _rand((16, 64), torch.float32, 9)
+    ref, bound = oracle.gemm_tn_reference(a, b)
+    c = ref.copy()
+    c[3, 5] += 2.0 * (oracle.ALLOW_REL * bound[3, 5] + oracle.ALLOW_ABS)
+    rep = oracle.parity_report(c, ref, bound)
+    assert not rep.ok and rep.argmax == (3, 5) and rep.n_bad == 1
+    c = ref.copy()
+    c[0, 0] = np.nan
+    assert not oracle.parity_report(c, ref, bound).ok
+    c = ref.copy()
+    c[1, 1] = np.inf
+    assert not oracle.parity_report(c, ref, bound).ok
+    assert oracle.parity_report(ref, ref, bound).ok
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+def _pins_failed(lib) -> list[str]:
+    """Run a compact version of the pins above against a given build; return
+    the names of those that fail."""
+    failed = []
+    # all-ones closed form
+    ref, _ = oracle.gemm_tn_reference(torch.ones((6, 33)), torch.ones((6, 33)), lib=lib)
+    if not (ref == 33).all():
+        failed.append("all_ones")
+    # integer product, square and non-symmetric
+    a = _rand((24, 24), torch.float16, 41, kind="int")
+    b = _rand((24, 24), torch.float16, 42, kind="int")
+    ref, _ = oracle.gemm_tn_reference(a, b, lib=lib)
+    if not np.array_equal(ref, (a.long().numpy() @ b.long().numpy().T).astype(np.float64)):
+        failed.append("integer_square")
+    # brute force, one odd square shape
+    a = _rand((7, 7), torch.float16, 43)
+    b = _rand((7, 7), torch.float16, 44)
+    ref, _ = oracle.gemm_tn_reference(a, b, lib=lib)
+    exact, mag = _exact(a, b)
+    if any(abs(Fraction(ref[i, j]) - exact[i][j]) > Fraction(_gamma(7)) * mag[i][j]
+           for i in range(7) for j in range(7)):
+        failed.append("bruteforce")
+    return failed
+
+
+def test_real_build_passes_compact_pins():
+    assert _pins_failed(oracle.load_library()) == []
+
+
+@pytest.mark.parametrize("plant", [1, 2, 3, 4])
+def test_each_planted_mistake_is_caught(plant, tmp_path):
+    lib = oracle.load_library(plant=plant, out_dir=tmp_path)
+    assert _pins_failed(lib), f"planted mistake {plant} went unnoticed"
+    assert oracle_build.library_path(plant, tmp_path).exists()
