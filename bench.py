@@ -1,0 +1,381 @@
+"""Throughput of C = A x B^T (bf16 8192^3 by default) on GB300 through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one gemm_tn call over the workload's operands, already resident in
+HBM. Prints ONE JSON line (rank 0): TFLOP/s = 2*M*N*K / device time, its
+roofline fraction (live CUDA-event launch durations against the measured peak),
+an end-to-end figure through gemm_tn_host (host buffers, copies inside the
+timed region), the fp64 CPU oracle timed on this host's cores as a reported
+baseline, and SM clocks sampled during the timed region.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the product needs no exchange between GPUs); `value` is the sum over ranks of
+the work divided by the slowest rank's time.
+
+--impl reference times the CPU oracle (the only reference implementation of
+this path) on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+METRIC = "TFLOP/s (2MNK/t) for C=A·Bᵀ bf16 8192³ on 1 GB300; % of dense tensor peak"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Algorithmic DRAM traffic per launch measured by ncu for the default workload
+# (dram__bytes_read.sum + dram__bytes_write.sum); see profiles/. None until a
+# capture of the current kernel exists.
+NCU_TRAFFIC_BYTES = {}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="bf16_8192x8192x8192")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ distributed
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks
+
+def gpu_smi_id(dev) -> str:
+    """nvidia-smi --id for a torch device: its UUID (robust to CUDA_VISIBLE_DEVICES)."""
+    import torch
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    if uuid is not None:
+        text = str(uuid)
+        return text if text.startswith("GPU-") else f"GPU-{text}"
+    return str(dev.index)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)  # let the first sample land before the timed region
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], None, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------ oracle baseline
+
+def cpu_oracle_rate(a, b, seconds: float):
+    """Time the fp64 oracle on a bounded row sample of the workload; returns
+    (TFLOP/s, cores, description)."""
+    import oracle
+    m, k = a.shape
+    n = b.shape[0]
+    cores = oracle.host_threads()
+    rows = max(1, min(m, cores))
+    t0 = time.perf_counter()
+    oracle.gemm_tn_reference(a[:rows], b)
+    dt = time.perf_counter() - t0
+    target_rows = int(min(m, max(rows, rows * seconds / max(dt, 1e-6))))
+    if target_rows > rows:
+        t0 = time.perf_counter()
+        oracle.gemm_tn_reference(a[:target_rows], b)
+        dt = time.perf_counter() - t0
+        rows = target_rows
+    flops = 2.0 * rows * n * k
+    return flops / dt / 1e12, cores, f"first {rows} of {m} rows of C (all {n} columns, K={k}), {dt:.1f} s"
+
+
+# ------------------------------------------------------------------ native arm
+
+def run_native(args, dist: Dist, peaks, peak_src):
+    import torch
+    import dense_tiled_gemm_03_gb300 as gt
+    from dense_tiled_gemm_03_gb300 import build as native_build
+    from dense_tiled_gemm_03_gb300.workloads import WORKLOADS, workload_operands
+
+    if dist.rank == 0 or not native_build.LIBRARY.exists():
+        native_build.build()
+    dist.barrier()
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    a_cpu, b_cpu = workload_operands(w)
+    a, b = a_cpu.to(dev), b_cpu.to(dev)
+    c = torch.empty((w.m, w.n), dtype=a.dtype, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    cfg_name = gt.gemm_tn_config_name(gt.gemm_tn_select_config(int(w.dtype == "bf16"), w.m, w.n, w.k))
+    op_bytes = (w.m * w.k + w.n * w.k) * 2
+    flush = op_bytes < 2 * L2_BYTES
+    scratch = torch.empty(L2_BYTES * 2 // 4, dtype=torch.int32, device=dev) if flush else None
+
+    def step():
+        gt.mm_tn(a, b, out=c, status=status)
+
+    for _ in range(args.warmup):
+        if flush:
+            scratch.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_smi_id(dev))
+    if dist.rank == 0:
+        sampler.start()
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    region0.record(stream)
+    for i in range(args.steps):
+        if flush:
+            scratch.fill_(1)   # write a buffer larger than L2 between timed launches
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    region1.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clocks = sampler.stop() if dist.rank == 0 else None
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device watchdog fired: {gt.gemm_tn_status_string(int(status.item()))}")
+
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    avg_launch_ms = sum(launch_ms) / len(launch_ms)
+    region_ms = region0.elapsed_time(region1)
+    # with an L2 flush between launches the region includes the flushes: take
+    # the step time from the launches themselves
+    step_ms = avg_launch_ms if flush else region_ms / args.steps
+    step_ms = dist.max(step_ms)
+    avg_launch_ms = dist.max(avg_launch_ms)
+    value = dist.world * w.flops / (step_ms * 1e-3) / 1e12
+
+    # roofline of the dominant (only) kernel of the step
+    tensor_peak = float(peaks["bf16_tflops"])
+    hbm_peak = float(peaks["hbm_gbs"])
+    # algorithmic bytes: each operand read once, C written once (2 B per element)
+    compulsory = (w.m * w.k + w.n * w.k + w.m * w.n) * 2
+    hbm_bound = hbm_peak * 1e9 * (w.flops / compulsory) < tensor_peak * 1e12
+    if hbm_bound:
+        achieved = compulsory / (avg_launch_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(achieved / hbm_peak, 4)}
+    else:
+        achieved = w.flops / (avg_launch_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / tensor_peak, 4),
+                    "frac_of_sustained": round(achieved / float(peaks.get("bf16_tflops_sustained", tensor_peak)), 4)}
+    roofline["traffic"] = NCU_TRAFFIC_BYTES.get((w.name, cfg_name))
+    roofline["algorithmic_bytes"] = compulsory
+    roofline["peak_source"] = f"{peak_src} ({'hbm_gbs' if hbm_bound else 'bf16_tflops'} burst; kernel timed alone)"
+    roofline["kernel"] = f"gemm_tn_sm103_kernel<{cfg_name}>"
+
+    # end to end through the host-buffer entry point
+    pin_a, pin_b = a_cpu.pin_memory(), b_cpu.pin_memory()
+    pin_c = torch.empty((w.m, w.n), dtype=a_cpu.dtype).pin_memory()
+    gt.mm_tn_host(pin_a, pin_b, out=pin_c, device=dev)   # warm
+    dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        gt.mm_tn_host(pin_a, pin_b, out=pin_c, device=dev)
+    e2e_s = dist.max((time.perf_counter() - t0) / args.e2e_steps)
+    e2e = {"value": round(dist.world * w.flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": op_bytes, "d2h_bytes_per_step": w.m * w.n * 2 + 4,
+           "steps": args.e2e_steps, "entry_point": "gemm_tn_host (pinned host buffers)"}
+
+    launches_per_step = 1  # the default workloads' operands are TMA-aligned: no repack kernels
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": dist.world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "m": w.m, "n": w.n, "k": w.k, "dist": w.dist, "seed": w.seed,
+                   "kernel_config": cfg_name, "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU",
+                   "l2": "L2 flushed between launches" if flush else
+                   f"inputs larger than L2 ({op_bytes / 1e6:.0f} MB of operands vs {L2_BYTES / 1e6:.0f} MB)",
+                   "accumulate": "fp32"},
+        "pct_of_peak": round(100 * w.flops / (avg_launch_ms * 1e-3) / 1e12 / tensor_peak, 2),
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clocks,
+    }
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = cpu_oracle_rate(a_cpu, b_cpu, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    return line
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, dist: Dist):
+    """The CPU oracle, timed as it stands on this host's cores: each step is a
+    bounded row sample of the workload, sized so the whole run takes about two
+    minutes."""
+    from dense_tiled_gemm_03_gb300.workloads import WORKLOADS, workload_operands
+    import oracle
+
+    w = WORKLOADS[args.workload]
+    a_cpu, b_cpu = workload_operands(w)
+    cores = oracle.host_threads()
+    total = args.steps + args.warmup
+    # calibrate rows per step against a ~120 s budget for the whole run
+    probe = max(1, min(w.m, cores))
+    t0 = time.perf_counter()
+    oracle.gemm_tn_reference(a_cpu[:probe], b_cpu)
+    per_row = (time.perf_counter() - t0) / probe
+    rows = int(max(1, min(w.m, 120.0 / total / max(per_row, 1e-9))))
+    for i in range(args.warmup):
+        r0 = (i * rows) % w.m
+        oracle.gemm_tn_reference(a_cpu[r0:r0 + rows], b_cpu)
+    t0 = time.perf_counter()
+    done = 0
+    for i in range(args.steps):
+        r0 = (i * rows) % w.m
+        oracle.gemm_tn_reference(a_cpu[r0:r0 + rows], b_cpu)
+        done += min(rows, w.m - r0)
+    dt = time.perf_counter() - t0
+    value = 2.0 * done * w.n * w.k / dt / 1e12
+    sample = f"{rows} rows of C per step (all {w.n} columns, K={w.k}) of {w.name}"
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": dist.world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "m": w.m, "n": w.n, "k": w.k, "seed": w.seed},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be >= 1")
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            if dist.rank == 0:
+                print(json.dumps(run_reference(args, dist)), flush=True)
+            return
+        peaks, src = load_peaks()
+        line = run_native(args, dist, peaks, src)
+        if dist.rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+"""ctypes binding of ``libgemm_tn.so`` (the C ABI in ``include/gemm_tn.h``).
+
+Argument marshalling only: every step of the product runs in the library's
+CUDA kernels. The functions keep the C names and signatures; ``mm_tn`` and
+``mm_tn_host`` are conveniences that take torch tensors, pass their pointers,
+strides and the current CUDA stream, and raise ``GemmTnError`` on a non-zero
+status. There is no fallback: if the library is missing or cannot be loaded,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from pathlib import Path
+
+PKG = Path(__file__).resolve().parent
+LIBRARY_PATH = PKG / "libgemm_tn.so"
+
+GEMM_TN_F16 = 0
+GEMM_TN_BF16 = 1
+
+GEMM_TN_OK = 0
+GEMM_TN_ERR_INVALID_VALUE = 1
+GEMM_TN_ERR_UNSUPPORTED_DTYPE = 2
+GEMM_TN_ERR_MISALIGNED = 3
+GEMM_TN_ERR_UNSUPPORTED_DEVICE = 4
+GEMM_TN_ERR_CUDA = 5
+GEMM_TN_ERR_TIMEOUT = 6
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_ptr = ctypes.c_void_p
+
+_SIGNATURES = {
+    "gemm_tn": (_int, [_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr]),
+    "gemm_tn_ex": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]),
+    "gemm_tn_host": (_int, [_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr]),
+    "gemm_tn_select_config": (_int, [_int, _i64, _i64, _i64]),
+    "gemm_tn_num_configs": (_int, []),
+    "gemm_tn_config_name": (ctypes.c_char_p, [_int]),
+    "gemm_tn_status_string": (ctypes.c_char_p, [_int]),
+    "gemm_tn_last_cuda_error": (_int, []),
+    "gemm_tn_last_error_message": (ctypes.c_char_p, []),
+    "gemm_tn_version": (_int, []),
+}
+
+
+class GemmTnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        lib = library()
+        msg = lib.gemm_tn_last_error_message().decode()
+        super().__init__(f"{where}: {lib.gemm_tn_status_string(status).decode()} ({msg})")
+
+
+def library() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not LIBRARY_PATH.exists():
+                raise RuntimeError(
+                    f"{LIBRARY_PATH} is missing: build it with `python -m dense_tiled_gemm_03_gb300.build` "
+                    "(there is no CPU fallback)")
+            lib = ctypes.CDLL(str(LIBRARY_PATH))
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+# ---------------------------------------------------------------- C-named calls
+
+def gemm_tn(dtype, m, n, k, a, b, c, stream=None) -> int:
+    return library().gemm_tn(dtype, m, n, k, a, b, c, stream)
+
+
+def gemm_tn_ex(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status=None, stream=None) -> int:
+    return library().gemm_tn_ex(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, stream)
+
+
+def gemm_tn_host(dtype, m, n, k, a_host, b_host, c_host, stream=None) -> int:
+    return library().gemm_tn_host(dtype, m, n, k, a_host, b_host, c_host, stream)
+
+
+def gemm_tn_select_config(dtype, m, n, k) -> int:
+    return library().gemm_tn_select_config(dtype, m, n, k)
+
+
+def gemm_tn_num_configs() -> int:
+    return library().gemm_tn_num_configs()
+
+
+def gemm_tn_config_name(config: int) -> str:
+    return library().gemm_tn_config_name(config).decode()
+
+
+def gemm_tn_status_string(status: int) -> str:
+    return library().gemm_tn_status_string(status).decode()
+
+
+def gemm_tn_last_cuda_error() -> int:
+    return library().gemm_tn_last_cuda_error()
+
+
+def gemm_tn_last_error_message() -> str:
+    return library().gemm_tn_last_error_message().decode()
+
+
+def gemm_tn_version() -> int:
+    return library().gemm_tn_version()
+
+
+# ---------------------------------------------------------------- torch helpers
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return GEMM_TN_F16
+    if t.dtype == torch.bfloat16:
+        return GEMM_TN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: expected float16 or bfloat16")
+
+
+def _row_pitch(t, cols: int) -> int:
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError("operands must be 2-D with unit stride along the last dimension")
+    return t.stride(0) if t.shape[0] > 1 else max(cols, 1)
+
+
+def mm_tn(a, b, out=None, status=None):
+    """C = A x B^T on the GPU through gemm_tn_ex. a: [M, K], b: [N, K] CUDA
+    tensors of the same fp16/bf16 dtype with unit stride along K; out: optional
+    [M, N] tensor of that dtype with unit stride along N; status: optional
+    one-element int32 CUDA tensor for the device watchdog. Runs on the
+    current CUDA stream of a's device."""
+    import torch
+    if a.device.type != "cuda" or b.device != a.device:
+        raise ValueError("a and b must be CUDA tensors on one device")
+    if a.dtype != b.dtype:
+        raise TypeError("a and b must have the same dtype")
+    m, k = a.shape
+    n, kb = b.shape
+    if kb != k:
+        raise ValueError(f"inner dimensions differ: {tuple(a.shape)} x {tuple(b.shape)}^T")
+    if out is None:
+        out = torch.empty((m, n), dtype=a.dtype, device=a.device)
+    elif out.shape != (m, n) or out.dtype != a.dtype or out.device != a.device:
+        raise ValueError("out must be [M, N] with the dtype and device of a")
+    lda, ldb, ldc = _row_pitch(a, k), _row_pitch(b, k), _row_pitch(out, n)
+    stream = torch.cuda.current_stream(a.device).cuda_stream
+    d_status = status.data_ptr() if status is not None else None
+    with torch.cuda.device(a.device):
+        rc = gemm_tn_ex(_dtype_code(a), m, n, k, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(), ldc,
+                        d_status, stream)
+    if rc != GEMM_TN_OK:
+        raise GemmTnError(rc, "gemm_tn_ex")
+    return out
+
+
+def mm_tn_host(a, b, out=None, device=None):
+    """C = A x B^T through gemm_tn_host: a, b, out are contiguous CPU tensors
+    (pinned or pageable); the call copies to the GPU, computes, copies back and
+    waits."""
+    import torch
+    if a.device.type != "cpu" or b.device.type != "cpu":
+        raise ValueError("mm_tn_host takes CPU tensors")
+    a = a.contiguous()
+    b = b.contiguous()
+    m, k = a.shape
+    n = b.shape[0]
+    if out is None:
+        out = torch.empty((m, n), dtype=a.dtype)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        rc = gemm_tn_host(_dtype_code(a), m, n, k, a.data_ptr(), b.data_ptr(), out.data_ptr(), stream)
+    if rc != GEMM_TN_OK:
+        raise GemmTnError(rc, "gemm_tn_host")
+    return out

@@ -1,0 +1,408 @@
+// gemm_tn_api.cu -- the C ABI declared in include/gemm_tn.h: argument
+// validation, alignment classification, the frozen configuration table,
+// tensor-map encoding and the launch of the sm_103a kernels.
+//
+// Host flow of one call ("0. A Minimal Hopper Matmul", sections "Kernel Setup"
+// and "Running the Kernel": the caller owns A, B, C; the grid covers
+// ceil(M / block_m) x ceil(N / block_n) tiles; "TMA: Tensor Memory Access":
+// the tensor-map descriptor is built on the host):
+//   validate -> (K == 0: zero C) -> classify operand alignment -> repack a
+//   misaligned operand into a workspace -> pick a configuration -> encode the
+//   tensor maps -> launch the persistent kernel on `stream`.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm_tn.h"
+#include "gemm_tn_internal.h"
+#include "sm103_gemm_kernel.cuh"
+
+namespace gemm_tn_impl {
+
+cudaError_t launch_gemm_1cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
+int max_resident_1cta(int id, bool bf16);
+int smem_bytes_1cta(int id);
+cudaError_t launch_gemm_2cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
+int max_resident_2cta(int id, bool bf16);
+int smem_bytes_2cta(int id);
+
+namespace {
+
+constexpr int kAbiVersion = 100;
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+constexpr int kBlockK = 64;
+
+const ConfigInfo kConfigs[kNumConfigs] = {
+    {"1cta_n256", 1, 128, 256, 256, 4, 0},
+    {"1cta_n128", 1, 128, 128, 128, 6, 0},
+    {"2cta_n256", 2, 256, 256, 128, 6, 0},
+};
+
+thread_local int t_last_cuda_error = 0;
+thread_local char t_last_message[256] = "";
+
+int fail(int status, const char* what) {
+  std::snprintf(t_last_message, sizeof(t_last_message), "%s", what);
+  return status;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  t_last_cuda_error = static_cast<int>(e);
+  std::snprintf(t_last_message, sizeof(t_last_message), "%s: %s", what, cudaGetErrorString(e));
+  return GEMM_TN_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- device facts
+
+struct DeviceFacts {
+  bool valid = false;
+  int cc_major = 0, cc_minor = 0, num_sms = 0;
+  int max_clusters[kNumConfigs][2] = {};   // [config][bf16], 0 = not queried yet
+};
+
+std::mutex g_device_mutex;
+DeviceFacts g_devices[64];
+
+int current_device(DeviceFacts** facts) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return fail(GEMM_TN_ERR_UNSUPPORTED_DEVICE, "no current CUDA device");
+  }
+  std::lock_guard<std::mutex> lock(g_device_mutex);
+  DeviceFacts& f = g_devices[dev];
+  if (!f.valid) {
+    if (cudaDeviceGetAttribute(&f.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&f.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&f.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(GEMM_TN_ERR_UNSUPPORTED_DEVICE, "cannot query the current device");
+    }
+    f.valid = true;
+  }
+  if (f.cc_major != 10 || f.cc_minor != 3) {
+    return fail(GEMM_TN_ERR_UNSUPPORTED_DEVICE, "device is not compute capability 10.3 (sm_103a)");
+  }
+  *facts = &f;
+  return GEMM_TN_OK;
+}
+
+int resident_clusters(DeviceFacts* f, int cfg, bool bf16) {
+  {
+    std::lock_guard<std::mutex> lock(g_device_mutex);
+    if (f->max_clusters[cfg][bf16] > 0) return f->max_clusters[cfg][bf16];
+  }
+  const int n = kConfigs[cfg].cta_group == 2 ? max_resident_2cta(cfg, bf16) : max_resident_1cta(cfg, bf16);
+  std::lock_guard<std::mutex> lock(g_device_mutex);
+  f->max_clusters[cfg][bf16] = n;
+  return n;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    } else {
+      cudaGetLastError();
+    }
+  });
+  return g_encode;
+}
+
+// Row-major [rows, cols] 16-bit matrix with pitch `ld` elements, loaded in
+// boxes of 64 columns (128 bytes) x box_rows rows with the 128-byte swizzle
+// the MMA descriptors expect. Out-of-range box elements read as zero.
+int encode_operand_map(CUtensorMap* map, bool bf16, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                       int box_rows) {
+  auto encode = encode_fn();
+  if (encode == nullptr) return fail(GEMM_TN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                            const_cast<void*>(ptr), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return fail(GEMM_TN_ERR_CUDA, buf);
+  }
+  return GEMM_TN_OK;
+}
+
+// ---------------------------------------------------------------- validation
+
+bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+// Bytes spanned by a [rows, cols] matrix with pitch ld (16-bit elements).
+uintptr_t span_bytes(int64_t rows, int64_t cols, int64_t ld) {
+  return static_cast<uintptr_t>(((rows - 1) * ld + cols) * 2);
+}
+
+int validate(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
+             const void* c, int64_t ldc) {
+  if (dtype != GEMM_TN_F16 && dtype != GEMM_TN_BF16) return fail(GEMM_TN_ERR_UNSUPPORTED_DTYPE, "dtype");
+  if (m < 0 || n < 0 || k < 0 || m > kMaxDim || n > kMaxDim || k > kMaxDim)
+    return fail(GEMM_TN_ERR_INVALID_VALUE, "sizes must be in [0, 2^31)");
+  if (m == 0 || n == 0) return GEMM_TN_OK;
+  if (c == nullptr) return fail(GEMM_TN_ERR_INVALID_VALUE, "C is NULL");
+  if (ldc < n || ldc > kMaxDim * 2) return fail(GEMM_TN_ERR_INVALID_VALUE, "ldc < n");
+  if (reinterpret_cast<uintptr_t>(c) % 2) return fail(GEMM_TN_ERR_MISALIGNED, "C is not 2-byte aligned");
+  if (k == 0) return GEMM_TN_OK;
+  if (a == nullptr || b == nullptr) return fail(GEMM_TN_ERR_INVALID_VALUE, "A or B is NULL");
+  if (lda < k || ldb < k || lda > kMaxDim * 2 || ldb > kMaxDim * 2)
+    return fail(GEMM_TN_ERR_INVALID_VALUE, "lda or ldb < k");
+  if (reinterpret_cast<uintptr_t>(a) % 2 || reinterpret_cast<uintptr_t>(b) % 2)
+    return fail(GEMM_TN_ERR_MISALIGNED, "A or B is not 2-byte aligned");
+  const uintptr_t c0 = reinterpret_cast<uintptr_t>(c), c1 = c0 + span_bytes(m, n, ldc);
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), a1 = a0 + span_bytes(m, k, lda);
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(b), b1 = b0 + span_bytes(n, k, ldb);
+  if (ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1))
+    return fail(GEMM_TN_ERR_INVALID_VALUE, "C overlaps A or B");
+  return GEMM_TN_OK;
+}
+
+// TMA wants a 16-byte-aligned base and a row pitch that is a multiple of 16 bytes.
+bool tma_compatible(const void* p, int64_t ld) {
+  return reinterpret_cast<uintptr_t>(p) % 16 == 0 && ld % 8 == 0;
+}
+
+int64_t round_up(int64_t x, int64_t q) { return (x + q - 1) / q * q; }
+
+// ---------------------------------------------------------------- configuration
+
+int parse_forced_config() {
+  const char* s = std::getenv("GEMM_TN_FORCE_CONFIG");
+  if (s == nullptr || *s == '\0') return -1;
+  for (int i = 0; i < kNumConfigs; ++i)
+    if (std::strcmp(s, kConfigs[i].name) == 0) return i;
+  char* end = nullptr;
+  const long v = std::strtol(s, &end, 10);
+  if (end != s && *end == '\0' && v >= 0 && v < kNumConfigs) return static_cast<int>(v);
+  return -1;
+}
+
+// The frozen table. Pair tiles (256 x 256) for every shape with more than one
+// 128-row block of output rows; a single-CTA 128 x 128 tile when M fits one
+// block, so the N dimension alone supplies enough tiles for the SMs.
+int choose_config(int64_t m, int64_t /*n*/, int64_t /*k*/) {
+  const int forced = parse_forced_config();
+  if (forced >= 0) return forced;
+  if (m <= 128) return kCfg1CtaN128;
+  return kCfg1CtaN256;
+}
+
+uint64_t watchdog_ns() {
+  const char* s = std::getenv("GEMM_TN_WATCHDOG_MS");
+  long ms = 4000;
+  if (s != nullptr && *s != '\0') {
+    char* end = nullptr;
+    const long v = std::strtol(s, &end, 10);
+    if (end != s && v > 0) ms = v;
+  }
+  return static_cast<uint64_t>(ms) * 1000000ull;
+}
+
+int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
+             void* c, int64_t ldc, int* d_status, cudaStream_t stream, int drop_load_kb) {
+  t_last_cuda_error = 0;
+  t_last_message[0] = '\0';
+  int st = validate(dtype, m, n, k, a, lda, b, ldb, c, ldc);
+  if (st != GEMM_TN_OK) return st;
+  if (m == 0 || n == 0) return GEMM_TN_OK;
+  DeviceFacts* dev = nullptr;
+  st = current_device(&dev);
+  if (st != GEMM_TN_OK) return st;
+
+  if (k == 0) {  // the empty sum
+    cudaError_t e = cudaMemset2DAsync(c, static_cast<size_t>(ldc) * 2, 0, static_cast<size_t>(n) * 2,
+                                      static_cast<size_t>(m), stream);
+    return e == cudaSuccess ? GEMM_TN_OK : fail_cuda(e, "cudaMemset2DAsync");
+  }
+  const bool bf16 = dtype == GEMM_TN_BF16;
+
+  // Operands the TMA cannot address directly go through a padded workspace.
+  const bool repack_a = !tma_compatible(a, lda);
+  const bool repack_b = !tma_compatible(b, ldb);
+  const int64_t ld_pad = round_up(k, 8);
+  void* workspace = nullptr;
+  const void* a_use = a;
+  const void* b_use = b;
+  int64_t lda_use = lda, ldb_use = ldb;
+  if (repack_a || repack_b) {
+    const size_t a_bytes = repack_a ? static_cast<size_t>(round_up(m * ld_pad * 2, 256)) : 0;
+    const size_t b_bytes = repack_b ? static_cast<size_t>(n * ld_pad * 2) : 0;
+    cudaError_t e = cudaMallocAsync(&workspace, a_bytes + b_bytes, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMallocAsync (repack workspace)");
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (repack_a) {
+      e = launch_repack(a, lda, ws, ld_pad, m, k, dev->num_sms, stream);
+      a_use = ws;
+      lda_use = ld_pad;
+    }
+    if (e == cudaSuccess && repack_b) {
+      e = launch_repack(b, ldb, ws + a_bytes, ld_pad, n, k, dev->num_sms, stream);
+      b_use = ws + a_bytes;
+      ldb_use = ld_pad;
+    }
+    if (e != cudaSuccess) {
+      cudaFreeAsync(workspace, stream);
+      return fail_cuda(e, "repack launch");
+    }
+  }
+
+  const int cfg_id = choose_config(m, n, k);
+  const ConfigInfo& cfg = kConfigs[cfg_id];
+  alignas(64) gemm_tn_dev::GemmArgs args;
+  std::memset(&args, 0, sizeof(args));
+  st = encode_operand_map(&args.tmap_a, bf16, a_use, m, k, lda_use, 128);
+  if (st == GEMM_TN_OK) st = encode_operand_map(&args.tmap_b, bf16, b_use, n, k, ldb_use, cfg.b_rows);
+  if (st != GEMM_TN_OK) {
+    if (workspace) cudaFreeAsync(workspace, stream);
+    return st;
+  }
+  args.c = c;
+  args.ldc = ldc;
+  args.m = static_cast<int32_t>(m);
+  args.n = static_cast<int32_t>(n);
+  args.k = static_cast<int32_t>(k);
+  args.num_m_tiles = static_cast<int32_t>((m + cfg.tile_m - 1) / cfg.tile_m);
+  args.num_n_tiles = static_cast<int32_t>((n + cfg.block_n - 1) / cfg.block_n);
+  args.num_k_blocks = static_cast<int32_t>((k + kBlockK - 1) / kBlockK);
+  const int64_t tiles = static_cast<int64_t>(args.num_m_tiles) * args.num_n_tiles;
+  if (tiles > INT32_MAX) {
+    if (workspace) cudaFreeAsync(workspace, stream);
+    return fail(GEMM_TN_ERR_INVALID_VALUE, "too many output tiles");
+  }
+  args.num_tiles = static_cast<int32_t>(tiles);
+  args.group_m = std::min<int32_t>(cfg.cta_group == 2 ? 8 : 16, args.num_m_tiles);
+  args.status = d_status;
+  args.timeout_ns = watchdog_ns();
+  args.drop_load_kb = drop_load_kb;
+
+  const int clusters = resident_clusters(dev, cfg_id, bf16);
+  if (clusters <= 0) {
+    if (workspace) cudaFreeAsync(workspace, stream);
+    return fail(GEMM_TN_ERR_CUDA, "kernel cannot be resident on this device (occupancy query)");
+  }
+  const int grid = static_cast<int>(std::min<int64_t>(tiles, clusters)) * cfg.cta_group;
+  cudaError_t e = cfg.cta_group == 2 ? launch_gemm_2cta(cfg_id, bf16, args, grid, stream)
+                                     : launch_gemm_1cta(cfg_id, bf16, args, grid, stream);
+  if (workspace) {
+    cudaError_t e2 = cudaFreeAsync(workspace, stream);
+    if (e == cudaSuccess) e = e2;
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+  return GEMM_TN_OK;
+}
+
+}  // namespace
+
+const ConfigInfo& config_info(int id) { return kConfigs[id]; }
+
+}  // namespace gemm_tn_impl
+
+using namespace gemm_tn_impl;
+
+extern "C" {
+
+int gemm_tn(int dtype, int64_t m, int64_t n, int64_t k, const void* a, const void* b, void* c,
+            gemm_tn_stream_t stream) {
+  return run_gemm(dtype, m, n, k, a, k, b, k, c, n, nullptr, reinterpret_cast<cudaStream_t>(stream), -1);
+}
+
+int gemm_tn_ex(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
+               void* c, int64_t ldc, int* d_status, gemm_tn_stream_t stream) {
+  return run_gemm(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, reinterpret_cast<cudaStream_t>(stream), -1);
+}
+
+int gemm_tn_host(int dtype, int64_t m, int64_t n, int64_t k, const void* a_host, const void* b_host, void* c_host,
+                 gemm_tn_stream_t stream_handle) {
+  t_last_cuda_error = 0;
+  t_last_message[0] = '\0';
+  int st = validate(dtype, m, n, k, a_host, k, b_host, k, c_host, n);
+  if (st != GEMM_TN_OK || m == 0 || n == 0) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+  const size_t a_bytes = static_cast<size_t>(m * k * 2), b_bytes = static_cast<size_t>(n * k * 2);
+  const size_t c_bytes = static_cast<size_t>(m * n * 2);
+  const size_t a_off = 0, b_off = static_cast<size_t>(round_up(static_cast<int64_t>(a_bytes), 256));
+  const size_t c_off = b_off + static_cast<size_t>(round_up(static_cast<int64_t>(b_bytes), 256));
+  uint8_t* dev_buf = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&dev_buf), c_off + c_bytes + sizeof(int), stream);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaMallocAsync");
+  int* d_status = reinterpret_cast<int*>(dev_buf + c_off + c_bytes);
+  int rc = GEMM_TN_OK;
+  e = cudaMemsetAsync(d_status, 0, sizeof(int), stream);
+  if (e == cudaSuccess && a_bytes) e = cudaMemcpyAsync(dev_buf + a_off, a_host, a_bytes, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess && b_bytes) e = cudaMemcpyAsync(dev_buf + b_off, b_host, b_bytes, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) {
+    rc = fail_cuda(e, "host-to-device copy");
+  } else {
+    rc = run_gemm(dtype, m, n, k, dev_buf + a_off, k, dev_buf + b_off, k, dev_buf + c_off, n, d_status, stream, -1);
+  }
+  int h_status = 0;
+  if (rc == GEMM_TN_OK) {
+    e = cudaMemcpyAsync(c_host, dev_buf + c_off, c_bytes, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h_status, d_status, sizeof(int), cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) rc = fail_cuda(e, "device-to-host copy");
+  }
+  cudaError_t ef = cudaFreeAsync(dev_buf, stream);
+  cudaError_t es = cudaStreamSynchronize(stream);
+  if (rc == GEMM_TN_OK && ef != cudaSuccess) rc = fail_cuda(ef, "cudaFreeAsync");
+  if (rc == GEMM_TN_OK && es != cudaSuccess) rc = fail_cuda(es, "cudaStreamSynchronize");
+  if (rc == GEMM_TN_OK && h_status != 0) rc = fail(h_status, "device watchdog expired");
+  return rc;
+}
+
+int gemm_tn_select_config(int dtype, int64_t m, int64_t n, int64_t k) {
+  if (dtype != GEMM_TN_F16 && dtype != GEMM_TN_BF16) return -1;
+  if (m <= 0 || n <= 0 || k <= 0 || m > kMaxDim || n > kMaxDim || k > kMaxDim) return -1;
+  return choose_config(m, n, k);
+}
+
+int gemm_tn_num_configs(void) { return kNumConfigs; }
+
+const char* gemm_tn_config_name(int config) {
+  if (config < 0 || config >= kNumConfigs) return "invalid";
+  return kConfigs[config].name;
+}
+
+const char* gemm_tn_status_string(int status) {
+  switch (status) {
+    case GEMM_TN_OK: return "GEMM_TN_OK";
+    case GEMM_TN_ERR_INVALID_VALUE: return "GEMM_TN_ERR_INVALID_VALUE";
+    case GEMM_TN_ERR_UNSUPPORTED_DTYPE: return "GEMM_TN_ERR_UNSUPPORTED_DTYPE";
+    case GEMM_TN_ERR_MISALIGNED: return "GEMM_TN_ERR_MISALIGNED";
+    case GEMM_TN_ERR_UNSUPPORTED_DEVICE: return "GEMM_TN_ERR_UNSUPPORTED_DEVICE";
+    case GEMM_TN_ERR_CUDA: return "GEMM_TN_ERR_CUDA";
+    case GEMM_TN_ERR_TIMEOUT: return "GEMM_TN_ERR_TIMEOUT";
+    default: return "GEMM_TN_ERR_UNKNOWN";
+  }
+}
+
+int gemm_tn_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* gemm_tn_last_error_message(void) { return t_last_message; }
+
+int gemm_tn_version(void) { return kAbiVersion; }
+
+}  // extern "C"

@@ -1,0 +1,49 @@
+// gemm_tn_internal.h -- host-side interface between the C-ABI translation unit
+// and the translation units that hold the kernel instantiations.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace gemm_tn_dev {
+struct GemmArgs;
+}
+
+namespace gemm_tn_impl {
+
+// Frozen configuration table ("TileLang: a tile language one level below
+// Triton", section "A few engineering points": freeze tuning results into a
+// table). Index order is part of the ABI (gemm_tn_config_name).
+enum ConfigId : int {
+  kCfg1CtaN256 = 0,   // one CTA per 128 x 256 tile, 4-stage ring
+  kCfg1CtaN128 = 1,   // one CTA per 128 x 128 tile, 6-stage ring (skinny / few tiles)
+  kCfg2CtaN256 = 2,   // CTA pair per 256 x 256 tile (cta_group::2), 6-stage ring
+  kNumConfigs = 3
+};
+
+struct ConfigInfo {
+  const char* name;
+  int cta_group;
+  int tile_m;      // rows per tile (128 * cta_group)
+  int block_n;     // columns per tile
+  int b_rows;      // rows of B one CTA loads (block_n / cta_group)
+  int stages;
+  int smem_bytes;
+};
+
+const ConfigInfo& config_info(int id);
+
+// Launch one configuration. grid = CTAs (a multiple of cta_group).
+cudaError_t launch_gemm(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
+
+// Co-resident clusters (CTA pairs, or single CTAs) of a configuration on the
+// current device; 0 on error.
+int max_resident_clusters(int id, bool bf16);
+
+// Row repack: dst[r][0:ld_dst] = src[r][0:cols] padded with zeros, for r < rows.
+cudaError_t launch_repack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,
+                          int num_sms, cudaStream_t stream);
+
+}  // namespace gemm_tn_impl

@@ -1,0 +1,39 @@
+// sm103_gemm_1cta.cu -- instantiations of the tcgen05 GEMM kernel with one CTA
+// per output tile (cta_group::1): 128 x 256 and 128 x 128 tiles.
+#include "gemm_tn_internal.h"
+#include "sm103_launch.cuh"
+
+namespace gemm_tn_impl {
+
+using Cfg256F16 = gemm_tn_dev::GemmConfig<1, 256, 4, false>;
+using Cfg256Bf16 = gemm_tn_dev::GemmConfig<1, 256, 4, true>;
+using Cfg128F16 = gemm_tn_dev::GemmConfig<1, 128, 6, false>;
+using Cfg128Bf16 = gemm_tn_dev::GemmConfig<1, 128, 6, true>;
+
+cudaError_t launch_gemm_1cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream) {
+  switch (id) {
+    case kCfg1CtaN256:
+      return bf16 ? Launcher<Cfg256Bf16>::launch(args, grid, stream) : Launcher<Cfg256F16>::launch(args, grid, stream);
+    case kCfg1CtaN128:
+      return bf16 ? Launcher<Cfg128Bf16>::launch(args, grid, stream) : Launcher<Cfg128F16>::launch(args, grid, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+int max_resident_1cta(int id, bool bf16) {
+  switch (id) {
+    case kCfg1CtaN256:
+      return bf16 ? Launcher<Cfg256Bf16>::max_clusters() : Launcher<Cfg256F16>::max_clusters();
+    case kCfg1CtaN128:
+      return bf16 ? Launcher<Cfg128Bf16>::max_clusters() : Launcher<Cfg128F16>::max_clusters();
+    default:
+      return 0;
+  }
+}
+
+int smem_bytes_1cta(int id) {
+  return id == kCfg1CtaN256 ? static_cast<int>(Cfg256F16::kSmemBytes) : static_cast<int>(Cfg128F16::kSmemBytes);
+}
+
+}  // namespace gemm_tn_impl

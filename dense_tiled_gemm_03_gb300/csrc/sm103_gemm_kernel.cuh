@@ -1,0 +1,407 @@
+// sm103_gemm_kernel.cuh -- the persistent, warp-specialized tcgen05 GEMM kernel
+// for C[M,N] = A[M,K] x B[N,K]^T on sm_103a (GB300).
+//
+// Structure (prior art on the pages, redesigned for tcgen05 / TMEM):
+//  * Block tiling: each CTA (or CTA pair) owns output tiles and walks K in
+//    64-element blocks ("0. A Minimal Hopper Matmul", section "Block Tiling";
+//    "Tiling a matmul", section "Counting traffic").
+//  * A multi-stage shared-memory ring filled by TMA and handed off through
+//    full/empty mbarriers ("Tiling a matmul", section "Pipelining";
+//    "TileLang: a tile language one level below Triton", section "What it
+//    generated": 3 full + 3 empty barriers around a TMA producer).
+//  * Warp specialization: warp 0 is the TMA producer, one thread of warp 1
+//    issues every tcgen05.mma, warps 2..5 are the epilogue.
+//  * Accumulators live in tensor memory (TMEM), double-buffered so the
+//    epilogue of one tile overlaps the main loop of the next. The operand
+//    round trip through registers that the Hopper V0 kernel pays ("0. A
+//    Minimal Hopper Matmul", sections "Data Flow" and "What's Next") does not
+//    exist here: tcgen05.mma reads both operands from shared memory.
+//  * Persistent scheduler with grouped rasterization so tiles running at the
+//    same time share rows of A and of B in L2 ("Tiling a matmul", section "The
+//    levels of tiling", and "Check yourself" on launch order).
+//  * kCtaGroup == 2: a cluster of two CTAs on two SMs computes a 256-row tile
+//    with cta_group::2 MMAs; each CTA loads its own 128 rows of A and half of
+//    the B tile, and the pair's leader issues the MMAs.
+//  * Ragged M/N/K: TMA zero-fills out-of-range boxes; the epilogue stores
+//    only in-range elements, which also handles any row stride of C.
+//  * Barriers sit after every TMA/MMA buffer in a fixed layout ("0. A Minimal
+//    Hopper Matmul", section "Epilogue": a barrier placed inside a live TMA
+//    destination corrupts results).
+//  * Every wait is bounded: past the deadline the kernel records
+//    GEMM_TN_ERR_TIMEOUT, tells the other roles to stop, drains its own async
+//    work, frees TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace gemm_tn_dev {
+
+constexpr int kNumThreads = 192;       // 6 warps
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kFirstEpilogueWarp = 2;
+constexpr int kNumEpilogueWarps = 4;
+constexpr int kStatusTimeout = 6;      // == GEMM_TN_ERR_TIMEOUT
+
+// Kernel arguments. Tensor maps first: they must be 64-byte aligned.
+struct GemmArgs {
+  CUtensorMap tmap_a;     // A: dims {K, M}, box {64, 128}, 128B swizzle
+  CUtensorMap tmap_b;     // B: dims {K, N}, box {64, BN / cta_group}, 128B swizzle
+  void* c;                // C [M, N], row stride ldc elements
+  int64_t ldc;
+  int32_t m, n, k;
+  int32_t num_m_tiles, num_n_tiles, num_k_blocks, num_tiles;
+  int32_t group_m;        // tile rows per rasterization group
+  int* status;            // nullable device int: first error code wins
+  uint64_t timeout_ns;    // per-wait watchdog budget
+  int32_t drop_load_kb;   // test hook: producer of tile 0 skips this k-block's loads (-1: never)
+};
+
+template <int kCtaGroup_, int kBlockN_, int kStages_, bool kBf16_>
+struct GemmConfig {
+  static constexpr int kCtaGroup = kCtaGroup_;
+  static constexpr int kBlockM = 128;                    // rows per CTA
+  static constexpr int kTileM = kBlockM * kCtaGroup;     // rows per tile (MMA M)
+  static constexpr int kBlockN = kBlockN_;               // columns per tile (MMA N)
+  static constexpr int kBRows = kBlockN / kCtaGroup;     // rows of B each CTA loads
+  static constexpr int kBlockK = 64;                     // one 128-byte swizzle row of 16-bit data
+  static constexpr int kMmaK = 16;
+  static constexpr int kStages = kStages_;
+  static constexpr bool kBf16 = kBf16_;
+  static constexpr uint32_t kATileBytes = kBlockM * kBlockK * 2;
+  static constexpr uint32_t kBTileBytes = kBRows * kBlockK * 2;
+  static constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kAccCols = kBlockN;               // fp32 columns per accumulator
+  static constexpr int kNumAcc = 2;
+  static constexpr uint32_t kTmemCols = kAccCols * kNumAcc;
+  // epilogue staging: per warp 32 rows x (16 packed words + 1 pad word)
+  static constexpr int kStageRowWords = 17;
+  static constexpr uint32_t kEpiBytes = kNumEpilogueWarps * 32 * kStageRowWords * 4;
+  // layout (offsets from the 1024-aligned base)
+  static constexpr uint32_t kOffA = 0;
+  static constexpr uint32_t kOffB = kOffA + kStages * kATileBytes;
+  static constexpr uint32_t kOffEpi = kOffB + kStages * kBTileBytes;
+  static constexpr uint32_t kOffBar = (kOffEpi + kEpiBytes + 7u) & ~7u;
+  static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1;   // full, empty, acc_full, acc_empty, drain
+  static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+  static constexpr uint32_t kSmemUsed = kOffAbort + 4;
+  static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;      // slack for aligning the base
+  static constexpr uint32_t kIdesc = mma_idesc_f16(kBf16, kTileM, kBlockN);
+
+  static_assert(kBlockN % 32 == 0 && kBlockN >= 32 && kBlockN <= 256, "MMA N");
+  static_assert(kCtaGroup == 1 || kCtaGroup == 2, "cta group");
+  static_assert(kBRows % 8 == 0 && kBRows <= 256, "TMA box rows");
+  static_assert(kATileBytes % 1024 == 0 && kBTileBytes % 1024 == 0, "swizzle atoms stay 1024-aligned");
+  static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
+  static_assert(kOffBar >= kOffEpi + kEpiBytes, "barriers after every buffer");
+  static_assert(kSmemBytes <= 232448, "fits the opt-in shared memory of one CTA");
+};
+
+// Tile index -> (tile row, tile column), grouped so that consecutive indices
+// sweep `group_m` tile rows before moving to the next column.
+__device__ __forceinline__ void tile_coords(int tile, int num_m_tiles, int num_n_tiles, int group_m, int& tm,
+                                            int& tn) {
+  const int per_group = group_m * num_n_tiles;
+  const int g = tile / per_group;
+  const int first_m = g * group_m;
+  const int rows = min(num_m_tiles - first_m, group_m);
+  const int in_group = tile - g * per_group;
+  tm = first_m + in_group % rows;
+  tn = in_group / rows;
+}
+
+template <class Cfg>
+__device__ __forceinline__ void store_pair_bits(uint32_t& out, uint32_t lo, uint32_t hi) {
+  const float flo = __uint_as_float(lo), fhi = __uint_as_float(hi);
+  if constexpr (Cfg::kBf16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(flo, fhi);
+    out = *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(flo, fhi);
+    out = *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <class Cfg>
+struct Watchdog {
+  const GemmArgs* args;
+  volatile uint32_t* abort_flag;
+  uint32_t abort_addr;   // shared address of the abort flag (for the peer CTA)
+
+  // Wait for the phase of `bar` with parity `parity`; false on timeout or
+  // when another role has already given up.
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
+    constexpr bool kCluster = Cfg::kCtaGroup == 2;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
+    const uint64_t deadline = globaltimer_ns() + args->timeout_ns;
+    while (true) {
+      if (mbar_try_wait<kCluster>(bar, parity)) return true;
+      if (*abort_flag) return false;
+      if (globaltimer_ns() > deadline) {
+        fail();
+        return false;
+      }
+    }
+  }
+
+  // Bounded wait used while draining after a failure: never sets the flag.
+  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
+    constexpr bool kCluster = Cfg::kCtaGroup == 2;
+    const uint64_t deadline = globaltimer_ns() + args->timeout_ns;
+    while (!mbar_try_wait<kCluster>(bar, parity)) {
+      if (globaltimer_ns() > deadline) return false;
+    }
+    return true;
+  }
+
+  __device__ __forceinline__ void fail() const {
+    if (args->status != nullptr) atomicCAS(args->status, 0, kStatusTimeout);
+    *abort_flag = 1u;
+    if constexpr (Cfg::kCtaGroup == 2) {
+      st_cluster_u32(map_to_cta(abort_addr, cluster_ctarank() ^ 1u), 1u);
+    }
+  }
+};
+
+template <class Cfg>
+__global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __grid_constant__ GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t base = smem_addr(smem);
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const uint32_t cta_rank = (Cfg::kCtaGroup == 2) ? cluster_ctarank() : 0u;
+  const bool leader = cta_rank == 0;
+
+  auto a_tile = [&](int s) { return base + Cfg::kOffA + s * Cfg::kATileBytes; };
+  auto b_tile = [&](int s) { return base + Cfg::kOffB + s * Cfg::kBTileBytes; };
+  auto full_bar = [&](int s) { return base + Cfg::kOffBar + 8u * s; };
+  auto empty_bar = [&](int s) { return base + Cfg::kOffBar + 8u * (Cfg::kStages + s); };
+  auto acc_full_bar = [&](int a) { return base + Cfg::kOffBar + 8u * (2 * Cfg::kStages + a); };
+  auto acc_empty_bar = [&](int a) { return base + Cfg::kOffBar + 8u * (2 * Cfg::kStages + Cfg::kNumAcc + a); };
+  const uint32_t drain_bar = base + Cfg::kOffBar + 8u * (2 * Cfg::kStages + 2 * Cfg::kNumAcc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffTmemSlot);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffAbort);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < Cfg::kNumAcc; ++a) {
+      mbar_init(acc_full_bar(a), 1);
+      mbar_init(acc_empty_bar(a), Cfg::kCtaGroup * kNumEpilogueWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_descriptor(&args.tmap_a);
+    tma_prefetch_descriptor(&args.tmap_b);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc<Cfg::kCtaGroup>(smem_addr(tmem_slot), Cfg::kTmemCols);
+    tmem_relinquish<Cfg::kCtaGroup>();
+  }
+  tc_fence_before_sync();
+  if constexpr (Cfg::kCtaGroup == 2) {
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const Watchdog<Cfg> wd{&args, abort_flag, smem_addr(const_cast<uint32_t*>(abort_flag))};
+  const int num_clusters = gridDim.x / Cfg::kCtaGroup;
+  const int cluster_id = blockIdx.x / Cfg::kCtaGroup;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_phase_of[Cfg::kStages];
+      for (int s = 0; s < Cfg::kStages; ++s) issued_phase_of[s] = -1;
+      bool ok = true;
+      int local_tile = 0;
+      for (int tile = cluster_id; tile < args.num_tiles && ok; tile += num_clusters, ++local_tile) {
+        int tm, tn;
+        tile_coords(tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tn);
+        const int a_row = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM;
+        const int b_row = tn * Cfg::kBlockN + static_cast<int>(cta_rank) * Cfg::kBRows;
+        for (int kb = 0; kb < args.num_k_blocks; ++kb) {
+          if (!wd.wait(empty_bar(stage), phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          if (leader) mbar_arrive_expect_tx(fb, Cfg::kCtaGroup * Cfg::kStageBytes);
+          const bool drop = local_tile == 0 && kb == args.drop_load_kb;
+          if (!drop) {
+            const int x = kb * Cfg::kBlockK;
+            if constexpr (Cfg::kCtaGroup == 2) {
+              const uint32_t fb_leader = map_to_cta(fb, 0);
+              tma_load_2d_pair(&args.tmap_a, a_tile(stage), fb_leader, x, a_row);
+              tma_load_2d_pair(&args.tmap_b, b_tile(stage), fb_leader, x, b_row);
+            } else {
+              tma_load_2d(&args.tmap_a, a_tile(stage), fb, x, a_row);
+              tma_load_2d(&args.tmap_b, b_tile(stage), fb, x, b_row);
+            }
+          }
+          issued_phase_of[stage] = static_cast<int>(phase);
+          if (++stage == Cfg::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      (void)ok;
+      if (leader) {
+        // Loads may still be landing if another role gave up: wait (bounded)
+        // for the last phase issued into every stage before the CTA may exit.
+        // On the normal path these phases have completed already. The
+        // leader's full barriers count the peer's bytes too.
+        for (int s = 0; s < Cfg::kStages; ++s) {
+          if (issued_phase_of[s] >= 0) wd.drain(full_bar(s), static_cast<uint32_t>(issued_phase_of[s]));
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (leader && lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = cluster_id; tile < args.num_tiles && ok; tile += num_clusters) {
+        if (!wd.wait(acc_empty_bar(acc), acc_phase ^ 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
+        for (int kb = 0; kb < args.num_k_blocks; ++kb) {
+          if (!wd.wait(full_bar(stage), phase)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage));
+          const uint64_t b_desc = sw128_kmajor_desc(b_tile(stage));
+#pragma unroll
+          for (int kk = 0; kk < Cfg::kBlockK / Cfg::kMmaK; ++kk) {
+            // advancing 16 elements along K = 32 bytes = 2 descriptor units
+            mma_f16<Cfg::kCtaGroup>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, Cfg::kIdesc,
+                                    (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          if constexpr (Cfg::kCtaGroup == 2) {
+            mma_commit_pair(empty_bar(stage), 0x3);
+          } else {
+            mma_commit(empty_bar(stage));
+          }
+          if (++stage == Cfg::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if constexpr (Cfg::kCtaGroup == 2) {
+          mma_commit_pair(acc_full_bar(acc), 0x3);
+        } else {
+          mma_commit(acc_full_bar(acc));
+        }
+        if (++acc == Cfg::kNumAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // All MMAs issued by this thread must finish before TMEM is freed.
+      if constexpr (Cfg::kCtaGroup == 2) {
+        mma_commit_pair(drain_bar, 0x1);
+      } else {
+        mma_commit(drain_bar);
+      }
+      wd.drain(drain_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const uint32_t quarter = warp & 3u;           // TMEM lanes this warp may read
+    uint32_t* stg = reinterpret_cast<uint32_t*>(smem + Cfg::kOffEpi) +
+                    (warp - kFirstEpilogueWarp) * 32 * Cfg::kStageRowWords;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const uint32_t acc_empty_leader0 =
+        (Cfg::kCtaGroup == 2) ? map_to_cta(acc_empty_bar(0), 0) : acc_empty_bar(0);
+    for (int tile = cluster_id; tile < args.num_tiles; tile += num_clusters) {
+      int tm, tn;
+      tile_coords(tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tn);
+      if (!wd.wait(acc_full_bar(acc), acc_phase)) break;
+      tc_fence_after_sync();
+      const int row0 = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM + static_cast<int>(quarter) * 32;
+      const int col_tile = tn * Cfg::kBlockN;
+      const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + static_cast<uint32_t>(acc * Cfg::kAccCols);
+      uint16_t* cptr = static_cast<uint16_t*>(args.c);
+      for (int chunk = 0; chunk < Cfg::kBlockN / 32; ++chunk) {
+        const int col0 = col_tile + chunk * 32;
+        if (col0 >= args.n) break;   // the rest of this tile lies past N (warp-uniform)
+        uint32_t r[32];
+        tmem_load_32x32(t_row + static_cast<uint32_t>(chunk * 32), r);
+        tmem_load_wait();
+        // this thread holds row (row0 + lane), columns [col0, col0 + 32)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) store_pair_bits<Cfg>(stg[lane * Cfg::kStageRowWords + j], r[2 * j], r[2 * j + 1]);
+        __syncwarp();
+        // transpose through shared memory: each store instruction writes 32
+        // consecutive columns of one row
+        const int col = col0 + static_cast<int>(lane);
+        const bool col_ok = col < args.n;
+#pragma unroll 4
+        for (int rr = 0; rr < 32; ++rr) {
+          const int row = row0 + rr;
+          const uint16_t v = reinterpret_cast<const uint16_t*>(stg + rr * Cfg::kStageRowWords)[lane];
+          if (col_ok && row < args.m) cptr[static_cast<int64_t>(row) * args.ldc + col] = v;
+        }
+        __syncwarp();
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (Cfg::kCtaGroup == 2) {
+          mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
+        } else {
+          mbar_arrive(acc_empty_bar(acc));
+        }
+      }
+      if (++acc == Cfg::kNumAcc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  if constexpr (Cfg::kCtaGroup == 2) {
+    cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc<Cfg::kCtaGroup>(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace gemm_tn_dev

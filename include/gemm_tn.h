@@ -1,0 +1,126 @@
+/*
+ * gemm_tn.h -- C ABI of a GB300-native (sm_103a) tiled dense GEMM.
+ *
+ * Operation ("0. A Minimal Hopper Matmul", section "Block Tiling", and its note
+ * on K-major data layout):
+ *
+ *     C[i][j] = sum_{k} A[i][k] * B[j][k]          i < M, j < N, k < K
+ *
+ * i.e. C = A x B^T with A of shape [M, K] and B of shape [N, K], both K-major
+ * (each row contiguous, K elements long, rows `lda` / `ldb` elements apart),
+ * and C of shape [M, N] row-major with rows `ldc` elements apart. A and B are
+ * fp16 or bf16; products are accumulated in fp32 ("0. A Minimal Hopper
+ * Matmul", section "Kernel Setup": fp32 accumulator) and the result is rounded
+ * to nearest-even into the input dtype ("Epilogue": cast back to 16 bits).
+ * Tiling changes only the order of the additions ("Tiling a matmul", section
+ * "Where it breaks"), so results match the exact product within
+ * |c - ref| <= 1e-2 * sum_k |a_ik * b_jk| + 1e-3 but are not bit-identical to
+ * any particular summation order.
+ *
+ * Conventions shared by every entry point:
+ *   - Sizes are element counts. M, N and K must each be below 2^31.
+ *   - Device pointers are caller-owned; nothing is retained after a call.
+ *     A, B and C must each be 2-byte aligned. C must not overlap A or B.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Device
+ *     work is enqueued on it and the call returns without waiting, except
+ *     gemm_tn_host, which waits for its stream.
+ *   - M == 0 or N == 0 does nothing and returns GEMM_TN_OK. K == 0 writes
+ *     zeros to C (the empty sum).
+ *   - Host-side errors are the return value; nothing is enqueued on error.
+ *   - Device-side watchdog: every wait inside the kernel is bounded (default
+ *     4 s, environment variable GEMM_TN_WATCHDOG_MS). When one expires the
+ *     kernel stops, leaves C unspecified and, if the caller passed `d_status`,
+ *     stores GEMM_TN_ERR_TIMEOUT there (first error wins; the caller zeroes
+ *     it and reads it after synchronising).
+ *   - Thread-safe: the only shared state is a per-device cache of attributes.
+ *   - Only compute capability 10.3 (GB300) devices are supported.
+ */
+#ifndef GEMM_TN_H_
+#define GEMM_TN_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMM_TN_API __attribute__((visibility("default")))
+#else
+#define GEMM_TN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* gemm_tn_stream_t;
+
+/* Element type of A, B and C. */
+enum gemm_tn_dtype { GEMM_TN_F16 = 0, GEMM_TN_BF16 = 1 };
+
+/* Return / device status codes. */
+enum gemm_tn_status {
+  GEMM_TN_OK = 0,
+  GEMM_TN_ERR_INVALID_VALUE = 1,      /* negative or too-large size, NULL pointer with non-zero size,
+                                         leading dimension too small, C overlapping A or B */
+  GEMM_TN_ERR_UNSUPPORTED_DTYPE = 2,  /* dtype is neither GEMM_TN_F16 nor GEMM_TN_BF16 */
+  GEMM_TN_ERR_MISALIGNED = 3,         /* a pointer is not 2-byte aligned */
+  GEMM_TN_ERR_UNSUPPORTED_DEVICE = 4, /* no current device, or it is not compute capability 10.3 */
+  GEMM_TN_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed: see gemm_tn_last_cuda_error() */
+  GEMM_TN_ERR_TIMEOUT = 6             /* device watchdog expired (written to *d_status only) */
+};
+
+/*
+ * gemm_tn -- C = A x B^T for contiguous operands: lda = ldb = k, ldc = n.
+ * a: device [m, k]; b: device [n, k]; c: device [m, n] (written).
+ */
+GEMM_TN_API int gemm_tn(int dtype, int64_t m, int64_t n, int64_t k, const void* a, const void* b, void* c,
+            gemm_tn_stream_t stream);
+
+/*
+ * gemm_tn_ex -- C = A x B^T with explicit row strides (in elements):
+ * lda >= k, ldb >= k, ldc >= n. Any stride and any 2-byte-aligned pointer is
+ * accepted. When A or B is not laid out the way the tensor-memory-access
+ * engine needs (16-byte-aligned base, row pitch a multiple of 16 bytes) the
+ * call first copies that operand into a stream-ordered workspace
+ * (cudaMallocAsync / cudaFreeAsync on `stream`) with a padded row pitch.
+ * d_status: nullable device int that receives GEMM_TN_ERR_TIMEOUT if the
+ * device watchdog fires; never cleared by the library.
+ */
+GEMM_TN_API int gemm_tn_ex(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b,
+               int64_t ldb, void* c, int64_t ldc, int* d_status, gemm_tn_stream_t stream);
+
+/*
+ * gemm_tn_host -- C = A x B^T with contiguous operands in HOST memory
+ * (pageable or pinned): copies A and B to the device, runs gemm_tn_ex, copies
+ * C back and waits for `stream`. Device buffers come from cudaMallocAsync on
+ * `stream` and are released before return. Returns GEMM_TN_ERR_TIMEOUT if the
+ * watchdog fired.
+ */
+GEMM_TN_API int gemm_tn_host(int dtype, int64_t m, int64_t n, int64_t k, const void* a_host, const void* b_host,
+                 void* c_host, gemm_tn_stream_t stream);
+
+/* Kernel configuration gemm_tn_ex would run for this problem on the current
+ * device (an index into the table below), or -1 for a no-op / invalid size.
+ * The environment variable GEMM_TN_FORCE_CONFIG (a name or an index)
+ * overrides the table. */
+GEMM_TN_API int gemm_tn_select_config(int dtype, int64_t m, int64_t n, int64_t k);
+
+/* Number of kernel configurations, and the name of one ("1cta_n256", ...). */
+GEMM_TN_API int gemm_tn_num_configs(void);
+GEMM_TN_API const char* gemm_tn_config_name(int config);
+
+/* Human-readable text of a status code. */
+GEMM_TN_API const char* gemm_tn_status_string(int status);
+
+/* cudaError_t of the last failing CUDA call made by this thread (0 if none),
+ * and a one-line description of the last error this thread returned. */
+GEMM_TN_API int gemm_tn_last_cuda_error(void);
+GEMM_TN_API const char* gemm_tn_last_error_message(void);
+
+/* ABI version: major * 100 + minor. */
+GEMM_TN_API int gemm_tn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_TN_H_ */

@@ -1,0 +1,109 @@
+"""Host-only checks of the C ABI: the library loads, exports every function the
+public headers declare, and rejects bad arguments before touching a device.
+No compute call is made (this runs on machines without a GPU)."""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+import dense_tiled_gemm_03_gb300 as gt
+from dense_tiled_gemm_03_gb300 import build as native_build
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    native_build.build()
+    return gt.library()
+
+
+def declared_functions() -> list[str]:
+    names = []
+    for header in sorted((ROOT / "include").glob("*.h")):
+        text = header.read_text()
+        names += re.findall(r"^GEMM_TN_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("gemm_tn", "gemm_tn_ex", "gemm_tn_host", "gemm_tn_status_string", "gemm_tn_last_cuda_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_version_status_strings_and_configs(lib):
+    assert gt.gemm_tn_version() == 100
+    assert gt.gemm_tn_status_string(gt.GEMM_TN_OK) == "GEMM_TN_OK"
+    assert gt.gemm_tn_status_string(gt.GEMM_TN_ERR_TIMEOUT) == "GEMM_TN_ERR_TIMEOUT"
+    assert gt.gemm_tn_status_string(99) == "GEMM_TN_ERR_UNKNOWN"
+    names = [gt.gemm_tn_config_name(i) for i in range(gt.gemm_tn_num_configs())]
+    assert names == ["1cta_n256", "1cta_n128", "2cta_n256"]
+    assert gt.gemm_tn_config_name(-1) == "invalid"
+
+
+def test_config_table(lib, monkeypatch):
+    monkeypatch.delenv("GEMM_TN_FORCE_CONFIG", raising=False)
+    sel = lambda m, n, k: gt.gemm_tn_config_name(gt.gemm_tn_select_config(gt.GEMM_TN_BF16, m, n, k))
+    assert sel(128, 16384, 16384) == "1cta_n128"   # skinny: one 128-row block of outputs
+    assert sel(8192, 8192, 8192) in ("1cta_n256", "2cta_n256")
+    assert gt.gemm_tn_select_config(gt.GEMM_TN_BF16, 0, 5, 5) == -1
+    assert gt.gemm_tn_select_config(7, 5, 5, 5) == -1
+    monkeypatch.setenv("GEMM_TN_FORCE_CONFIG", "1cta_n128")
+    assert sel(8192, 8192, 8192) == "1cta_n128"
+    monkeypatch.setenv("GEMM_TN_FORCE_CONFIG", "2")
+    assert sel(8192, 8192, 8192) == "2cta_n256"
+
+
+# Fake, well-separated addresses: validation never dereferences them.
+A, B, C = 0x10000000, 0x20000000, 0x30000000
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((5, 4, 4, 4, A, 4, B, 4, C, 4), gt.GEMM_TN_ERR_UNSUPPORTED_DTYPE),
+    ((0, -1, 4, 4, A, 4, B, 4, C, 4), gt.GEMM_TN_ERR_INVALID_VALUE),
+    ((0, 4, 4, 1 << 31, A, 1 << 31, B, 1 << 31, C, 4), gt.GEMM_TN_ERR_INVALID_VALUE),
+    ((0, 4, 4, 4, A, 4, B, 4, None, 4), gt.GEMM_TN_ERR_INVALID_VALUE),      # NULL C
+    ((0, 4, 4, 4, None, 4, B, 4, C, 4), gt.GEMM_TN_ERR_INVALID_VALUE),      # NULL A
+    ((0, 4, 4, 4, A, 3, B, 4, C, 4), gt.GEMM_TN_ERR_INVALID_VALUE),         # lda < k
+    ((0, 4, 4, 4, A, 4, B, 4, C, 3), gt.GEMM_TN_ERR_INVALID_VALUE),         # ldc < n
+    ((0, 4, 4, 4, A + 1, 4, B, 4, C, 4), gt.GEMM_TN_ERR_MISALIGNED),
+    ((1, 4, 4, 4, A, 4, B, 4, C + 1, 4), gt.GEMM_TN_ERR_MISALIGNED),
+    ((0, 4, 4, 4, A, 4, B, 4, A + 8, 4), gt.GEMM_TN_ERR_INVALID_VALUE),     # C overlaps A
+    ((0, 4, 4, 4, A, 4, B, 4, B + 30, 4), gt.GEMM_TN_ERR_INVALID_VALUE),    # C overlaps B's last byte
+])
+def test_validation_rejects_before_any_device_call(lib, args, expected):
+    assert gt.gemm_tn_ex(*args, None, None) == expected
+    assert gt.gemm_tn_last_error_message() != ""
+
+
+def test_empty_output_is_a_noop(lib):
+    assert gt.gemm_tn_ex(0, 0, 4, 4, None, 4, None, 4, None, 4, None, None) == gt.GEMM_TN_OK
+    assert gt.gemm_tn_ex(1, 4, 0, 4, None, 4, None, 4, None, 1, None, None) == gt.GEMM_TN_OK
+    assert gt.gemm_tn(1, 0, 0, 0, None, None, None, None) == gt.GEMM_TN_OK
+
+
+def test_c_adjacent_to_b_is_not_overlap(lib):
+    # B spans [B, B + 32) for 4 x 4 fp16; C starting right after it is legal,
+    # so validation passes and the call proceeds to the device check.
+    rc = gt.gemm_tn_ex(0, 4, 4, 4, A, 4, B, 4, B + 32, 4, None, None)
+    assert rc in (gt.GEMM_TN_OK, gt.GEMM_TN_ERR_UNSUPPORTED_DEVICE, gt.GEMM_TN_ERR_CUDA)
+    if rc != gt.GEMM_TN_OK:
+        assert "C overlaps" not in gt.gemm_tn_last_error_message()
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    from dense_tiled_gemm_03_gb300 import _native
+    monkeypatch.setattr(_native, "_lib", None)
+    monkeypatch.setattr(_native, "LIBRARY_PATH", tmp_path / "libgemm_tn.so")
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        _native.library()

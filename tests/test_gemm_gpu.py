@@ -1,0 +1,229 @@
+"""GPU parity of the sm_103a GEMM against the fp64 oracle, through the C ABI.
+
+Pass criterion for every element: |c - ref| <= 1e-2 * sum_k |a_ik * b_jk| + 1e-3,
+no NaN/Inf (C is pre-filled with NaN, so every element must be written).
+Exactness where the arithmetic is exact: small-integer operands, identity and
+permutation matrices. Edge cases: empty and ragged shapes, K = 0, padded and
+misaligned strides, misaligned base pointers, repeated launches.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import dense_tiled_gemm_03_gb300 as gt
+from dense_tiled_gemm_03_gb300.workloads import WORKLOADS, make_operands, workload_operands
+
+from _parity import (assert_parity, assert_sampled_parity, edge_indices, forced_config, gpu_gemm,
+                     require_gpu)
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = ["1cta_n256", "1cta_n128", "2cta_n256"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+    from dense_tiled_gemm_03_gb300 import build as native_build
+    native_build.build()
+    torch.cuda.init()
+
+
+# ------------------------------------------------------------ small and odd shapes
+
+ODD_SHAPES = [(1, 1, 1), (1, 1, 64), (7, 13, 17), (128, 256, 64), (129, 257, 65), (255, 511, 130),
+              (300, 200, 1000), (64, 1024, 8), (513, 129, 200), (1000, 1000, 64)]
+
+
+@pytest.mark.parametrize("config", CONFIGS)
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("mnk", ODD_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_odd_shapes(mnk, dtype, config):
+    m, n, k = mnk
+    a, b = make_operands(m, n, k, dtype, "uniform", seed=m * 131 + n * 7 + k)
+    c, status = gpu_gemm(a, b, config)
+    assert status == 0
+    assert_parity(c, a, b, f"{mnk} {dtype} {config}")
+
+
+# ------------------------------------------------------------ the five workloads
+
+@pytest.mark.parametrize("name", ["fp16_256x256x256", "fp16_4096x4096x4096", "fp16_3001x5003x4097",
+                                  "bf16_128x16384x16384"])
+def test_workload_full_parity(name):
+    """Element-by-element parity over the whole output, default configuration."""
+    a, b = workload_operands(name)
+    c, status = gpu_gemm(a, b)
+    assert status == 0
+    assert_parity(c, a, b, name)
+
+
+@pytest.mark.parametrize("config", CONFIGS)
+@pytest.mark.parametrize("name", ["fp16_256x256x256", "fp16_3001x5003x4097"])
+def test_workload_parity_every_config(name, config):
+    a, b = workload_operands(name)
+    c, status = gpu_gemm(a, b, config)
+    assert status == 0
+    assert_parity(c, a, b, f"{name} {config}")
+
+
+def test_headline_workload_sampled_parity():
+    """bf16 8192^3 in the configuration the benchmark runs: every column of
+    sampled rows and every row of sampled columns (tile edges included)."""
+    w = WORKLOADS["bf16_8192x8192x8192"]
+    a, b = workload_operands(w)
+    c, status = gpu_gemm(a, b)
+    assert status == 0
+    assert torch.isfinite(c.float()).all()
+    rng = np.random.Generator(np.random.PCG64(7))
+    rows = edge_indices(w.m, 256, rng, 16)
+    cols = edge_indices(w.n, 256, rng, 16)
+    assert_sampled_parity(c, a, b, rows, cols, w.name)
+
+
+# ------------------------------------------------------------ exact cases
+
+@pytest.mark.parametrize("config", CONFIGS)
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_small_integers_are_exact(dtype, config):
+    # entries in {-2..2}, K = 64: |C| <= 256, exact in fp32 and in both 16-bit types
+    m, n, k = 300, 400, 64
+    a, b = make_operands(m, n, k, dtype, "int_small", seed=77)
+    c, status = gpu_gemm(a, b, config)
+    assert status == 0
+    exact = (a.long() @ b.long().T)
+    assert torch.equal(c.double(), exact.double()), "integer product not reproduced exactly"
+
+
+@pytest.mark.parametrize("config", CONFIGS)
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_identity_and_permutation_reproduce_a(dtype, config):
+    m, k = 333, 256
+    a, _ = make_operands(m, 1, k, dtype, "uniform", seed=5)
+    eye = torch.eye(k, dtype=a.dtype)
+    c, _ = gpu_gemm(a, eye, config)
+    assert torch.equal(c, a)
+    perm = torch.from_numpy(np.random.Generator(np.random.PCG64(3)).permutation(k))
+    p = torch.zeros((k, k), dtype=a.dtype)
+    p[torch.arange(k), perm] = 1
+    c, _ = gpu_gemm(a, p, config)
+    assert torch.equal(c, a[:, perm])
+
+
+def test_all_ones_gives_k():
+    for k in (256, 4096):
+        a = torch.ones((200, k), dtype=torch.float16)
+        b = torch.ones((300, k), dtype=torch.float16)
+        c, _ = gpu_gemm(a, b)
+        assert (c.double() == k).all()
+
+
+# ------------------------------------------------------------ edge cases
+
+def test_k_zero_writes_zeros():
+    a = torch.empty((10, 0), dtype=torch.bfloat16)
+    b = torch.empty((20, 0), dtype=torch.bfloat16)
+    c, status = gpu_gemm(a, b)
+    assert status == 0 and (c == 0).all()
+
+
+def test_empty_m_or_n_is_noop():
+    dev = torch.device("cuda", 0)
+    a = torch.ones((0, 8), dtype=torch.float16, device=dev)
+    b = torch.ones((5, 8), dtype=torch.float16, device=dev)
+    out = gt.mm_tn(a, b)
+    assert out.shape == (0, 5)
+    out = gt.mm_tn(b, a)
+    assert out.shape == (5, 0)
+
+
+@pytest.mark.parametrize("pad", [(8, 8, 8), (3, 5, 7), (0, 0, 5), (1, 0, 0)])
+def test_padded_and_misaligned_strides(pad):
+    """Row pitches larger than the logical width: multiples of 8 use the TMA
+    directly, others go through the repack workspace; any ldc is stored with
+    predicated element stores."""
+    pa, pb, pc = pad
+    m, n, k = 300, 333, 200
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "fp16", "uniform", seed=sum(pad))
+    a_big = torch.zeros((m, k + pa), dtype=torch.float16)
+    a_big[:, :k] = a_cpu
+    b_big = torch.zeros((n, k + pb), dtype=torch.float16)
+    b_big[:, :k] = b_cpu
+    a = a_big.to(dev)[:, :k]
+    b = b_big.to(dev)[:, :k]
+    c_big = torch.full((m, n + pc), float("nan"), dtype=torch.float16, device=dev)
+    c = c_big[:, :n]
+    gt.mm_tn(a, b, out=c)
+    torch.cuda.synchronize()
+    assert_parity(c.cpu(), a_cpu, b_cpu, f"pad {pad}")
+    if pc:
+        assert torch.isnan(c_big[:, n:].float()).all(), "wrote outside C"
+
+
+def test_misaligned_base_pointers():
+    """Operands starting 2 bytes past a 16-byte boundary (repack path) and an
+    output starting 2 bytes past one (predicated stores)."""
+    m, n, k = 257, 129, 4097
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "bf16", "uniform", seed=9)
+    a_buf = torch.zeros(m * k + 1, dtype=torch.bfloat16, device=dev)
+    a_buf[1:] = a_cpu.flatten().to(dev)
+    b_buf = torch.zeros(n * k + 1, dtype=torch.bfloat16, device=dev)
+    b_buf[1:] = b_cpu.flatten().to(dev)
+    c_buf = torch.full((m * n + 1,), float("nan"), dtype=torch.bfloat16, device=dev)
+    a = a_buf[1:].view(m, k)
+    b = b_buf[1:].view(n, k)
+    c = c_buf[1:].view(m, n)
+    assert a.data_ptr() % 16 == 2
+    gt.mm_tn(a, b, out=c)
+    torch.cuda.synchronize()
+    assert_parity(c.cpu(), a_cpu, b_cpu, "misaligned base")
+    assert torch.isnan(c_buf[:1].float()).all()
+
+
+@pytest.mark.parametrize("config", CONFIGS)
+def test_repeated_launches_are_bit_identical(config):
+    """NaN canary + determinism: C is re-filled with NaN before each launch,
+    every launch must overwrite all of it, and all launches agree bit for bit
+    (a corrupted barrier shows up as sporadic NaNs or differences)."""
+    m, n, k = 1000, 1200, 1024
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "bf16", "uniform", seed=31)
+    a, b = a_cpu.to(dev), b_cpu.to(dev)
+    out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    first = None
+    with forced_config(config):
+        for _ in range(20):
+            out.fill_(float("nan"))
+            gt.mm_tn(a, b, out=out)
+            got = out.clone()
+            if first is None:
+                first = got
+            else:
+                assert torch.equal(got.view(torch.int16), first.view(torch.int16))
+    torch.cuda.synchronize()
+    assert not torch.isnan(first.float()).any()
+    assert_parity(first.cpu(), a_cpu, b_cpu, config)
+
+
+def test_plain_entry_point_and_host_entry_point_agree():
+    """gemm_tn (device pointers, contiguous) and gemm_tn_host (host buffers,
+    copies inside the call) give the same bits as gemm_tn_ex."""
+    m, n, k = 640, 768, 512
+    a_cpu, b_cpu = make_operands(m, n, k, "fp16", "normal_over_sqrt_k", seed=12)
+    c_ex, _ = gpu_gemm(a_cpu, b_cpu)
+    dev = torch.device("cuda", 0)
+    a, b = a_cpu.to(dev), b_cpu.to(dev)
+    c = torch.empty((m, n), dtype=torch.float16, device=dev)
+    rc = gt.gemm_tn(gt.GEMM_TN_F16, m, n, k, a.data_ptr(), b.data_ptr(), c.data_ptr(),
+                    torch.cuda.current_stream().cuda_stream)
+    assert rc == gt.GEMM_TN_OK
+    torch.cuda.synchronize()
+    assert torch.equal(c.cpu(), c_ex)
+    c_host = gt.mm_tn_host(a_cpu.pin_memory(), b_cpu.pin_memory())
+    assert torch.equal(c_host, c_ex)
+    c_host = gt.mm_tn_host(a_cpu, b_cpu)   # pageable
+    assert torch.equal(c_host, c_ex)
