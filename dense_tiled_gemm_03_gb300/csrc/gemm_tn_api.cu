@@ -43,6 +43,7 @@ const ConfigInfo kConfigs[kNumConfigs] = {
     {"1cta_n256", 1, 128, 256, 256, 4, 0},
     {"1cta_n128", 1, 128, 128, 128, 6, 0},
     {"2cta_n256", 2, 256, 256, 128, 6, 0},
+    {"2cta_n128", 2, 256, 128, 64, 8, 0},
 };
 
 thread_local int t_last_cuda_error = 0;

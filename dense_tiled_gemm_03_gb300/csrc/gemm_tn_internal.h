@@ -20,7 +20,8 @@ enum ConfigId : int {
   kCfg1CtaN256 = 0,   // one CTA per 128 x 256 tile, 4-stage ring
   kCfg1CtaN128 = 1,   // one CTA per 128 x 128 tile, 6-stage ring (skinny / few tiles)
   kCfg2CtaN256 = 2,   // CTA pair per 256 x 256 tile (cta_group::2), 6-stage ring
-  kNumConfigs = 3
+  kCfg2CtaN128 = 3,   // CTA pair per 256 x 128 tile (cta_group::2), 8-stage ring
+  kNumConfigs = 4
 };
 
 struct ConfigInfo {

@@ -1,5 +1,6 @@
 // sm103_gemm_2cta.cu -- instantiations of the tcgen05 GEMM kernel with a CTA
-// pair (a 2-CTA cluster on two SMs, cta_group::2) per 256 x 256 output tile.
+// pair (a 2-CTA cluster on two SMs, cta_group::2) per 256 x 256 or 256 x 128
+// output tile.
 #include "gemm_tn_internal.h"
 #include "sm103_launch.cuh"
 
@@ -7,17 +8,34 @@ namespace gemm_tn_impl {
 
 using CfgPairF16 = gemm_tn_dev::GemmConfig<2, 256, 6, false>;
 using CfgPairBf16 = gemm_tn_dev::GemmConfig<2, 256, 6, true>;
+using CfgPair128F16 = gemm_tn_dev::GemmConfig<2, 128, 8, false>;
+using CfgPair128Bf16 = gemm_tn_dev::GemmConfig<2, 128, 8, true>;
 
 cudaError_t launch_gemm_2cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream) {
-  if (id != kCfg2CtaN256) return cudaErrorInvalidValue;
-  return bf16 ? Launcher<CfgPairBf16>::launch(args, grid, stream) : Launcher<CfgPairF16>::launch(args, grid, stream);
+  switch (id) {
+    case kCfg2CtaN256:
+      return bf16 ? Launcher<CfgPairBf16>::launch(args, grid, stream) : Launcher<CfgPairF16>::launch(args, grid, stream);
+    case kCfg2CtaN128:
+      return bf16 ? Launcher<CfgPair128Bf16>::launch(args, grid, stream)
+                  : Launcher<CfgPair128F16>::launch(args, grid, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 int max_resident_2cta(int id, bool bf16) {
-  if (id != kCfg2CtaN256) return 0;
-  return bf16 ? Launcher<CfgPairBf16>::max_clusters() : Launcher<CfgPairF16>::max_clusters();
+  switch (id) {
+    case kCfg2CtaN256:
+      return bf16 ? Launcher<CfgPairBf16>::max_clusters() : Launcher<CfgPairF16>::max_clusters();
+    case kCfg2CtaN128:
+      return bf16 ? Launcher<CfgPair128Bf16>::max_clusters() : Launcher<CfgPair128F16>::max_clusters();
+    default:
+      return 0;
+  }
 }
 
-int smem_bytes_2cta(int /*id*/) { return static_cast<int>(CfgPairF16::kSmemBytes); }
+int smem_bytes_2cta(int id) {
+  return id == kCfg2CtaN256 ? static_cast<int>(CfgPairF16::kSmemBytes) : static_cast<int>(CfgPair128F16::kSmemBytes);
+}
 
 }  // namespace gemm_tn_impl

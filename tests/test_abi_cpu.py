@@ -47,7 +47,7 @@ def test_version_status_strings_and_configs(lib):
     assert gt.gemm_tn_status_string(gt.GEMM_TN_ERR_TIMEOUT) == "GEMM_TN_ERR_TIMEOUT"
     assert gt.gemm_tn_status_string(99) == "GEMM_TN_ERR_UNKNOWN"
     names = [gt.gemm_tn_config_name(i) for i in range(gt.gemm_tn_num_configs())]
-    assert names == ["1cta_n256", "1cta_n128", "2cta_n256"]
+    assert names == ["1cta_n256", "1cta_n128", "2cta_n256", "2cta_n128"]
     assert gt.gemm_tn_config_name(-1) == "invalid"
 
 
