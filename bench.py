@@ -37,7 +37,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Algorithmic DRAM traffic per launch measured by ncu for the default workload
 # (dram__bytes_read.sum + dram__bytes_write.sum); see profiles/. None until a
 # capture of the current kernel exists.
-NCU_TRAFFIC_BYTES = {}
+NCU_TRAFFIC_BYTES = {
+    ("bf16_8192x8192x8192", "1cta_n256"): 951_858_432 + 123_698_432,   # gemm_tn_1cta_n256_bf16_8192.md
+}
 
 
 def parse_args():
