@@ -52,6 +52,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--config", default=None, help="force a kernel configuration (GEMM_TN_FORCE_CONFIG)")
     return ap.parse_args()
 
 
@@ -363,6 +364,8 @@ def run_reference(args, dist: Dist):
 
 def main():
     args = parse_args()
+    if args.config:
+        os.environ["GEMM_TN_FORCE_CONFIG"] = args.config
     if args.gpus < 1:
         raise SystemExit("--gpus must be >= 1")
     dist = Dist()

@@ -202,14 +202,17 @@ int parse_forced_config() {
   return -1;
 }
 
-// The frozen table. Pair tiles (256 x 256) for every shape with more than one
-// 128-row block of output rows; a single-CTA 128 x 128 tile when M fits one
-// block, so the N dimension alone supplies enough tiles for the SMs.
+// The frozen table, from measurements on GB300 (bf16 8192^3: pair tile 1698
+// TFLOP/s vs 1565 for the single-CTA 128 x 256 tile; fp16 4096^3: 1346 vs
+// 1202; fp16 3001 x 5003 x 4097: 751 vs 623). Pair tiles (256 x 256) for every
+// shape with more than one 128-row block of output rows; a single-CTA 128 x 128
+// tile when M fits one block, so the N dimension alone supplies the tiles
+// (bf16 128 x 16384 x 16384: 5.2 TB/s vs 4.9 for the pair tile).
 int choose_config(int64_t m, int64_t /*n*/, int64_t /*k*/) {
   const int forced = parse_forced_config();
   if (forced >= 0) return forced;
   if (m <= 128) return kCfg1CtaN128;
-  return kCfg1CtaN256;
+  return kCfg2CtaN256;
 }
 
 uint64_t watchdog_ns() {
