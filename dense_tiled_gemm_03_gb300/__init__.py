@@ -21,6 +21,8 @@ from ._native import (  # noqa: F401
     gemm_tn,
     gemm_tn_config_name,
     gemm_tn_ex,
+    gemm_tn_ex_noalloc,
+    GEMM_TN_NOALLOC_SCRATCH_BYTES,
     gemm_tn_host,
     gemm_tn_last_cuda_error,
     gemm_tn_last_error_message,

@@ -37,6 +37,7 @@ _ptr = ctypes.c_void_p
 _SIGNATURES = {
     "gemm_tn": (_int, [_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr]),
     "gemm_tn_ex": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]),
+    "gemm_tn_ex_noalloc": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]),
     "gemm_tn_host": (_int, [_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr]),
     "gemm_tn_select_config": (_int, [_int, _i64, _i64, _i64]),
     "gemm_tn_num_configs": (_int, []),
@@ -84,6 +85,15 @@ def gemm_tn(dtype, m, n, k, a, b, c, stream=None) -> int:
 
 def gemm_tn_ex(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status=None, stream=None) -> int:
     return library().gemm_tn_ex(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, stream)
+
+
+def gemm_tn_ex_noalloc(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status=None, stream=None) -> int:
+    """gemm_tn_ex that allocates no device memory (see include/gemm_tn.h)."""
+    return library().gemm_tn_ex_noalloc(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, stream)
+
+
+#: bytes of the static scratch gemm_tn_ex_noalloc may use (GEMM_TN_NOALLOC_SCRATCH_BYTES)
+GEMM_TN_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 def gemm_tn_host(dtype, m, n, k, a_host, b_host, c_host, stream=None) -> int:

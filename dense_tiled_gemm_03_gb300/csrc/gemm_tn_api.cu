@@ -226,8 +226,12 @@ uint64_t watchdog_ns() {
   return static_cast<uint64_t>(ms) * 1000000ull;
 }
 
+// fixed_scratch: nullptr = repack workspace from cudaMallocAsync (the normal
+// path); otherwise a caller-designated device buffer of fixed_scratch_bytes
+// that is used instead and never freed (gemm_tn_ex_noalloc).
 int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
-             void* c, int64_t ldc, int* d_status, cudaStream_t stream, int drop_load_kb) {
+             void* c, int64_t ldc, int* d_status, cudaStream_t stream, int drop_load_kb,
+             void* fixed_scratch = nullptr, size_t fixed_scratch_bytes = 0) {
   t_last_cuda_error = 0;
   t_last_message[0] = '\0';
   int st = validate(dtype, m, n, k, a, lda, b, ldb, c, ldc);
@@ -249,14 +253,28 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   const bool repack_b = !tma_compatible(b, ldb);
   const int64_t ld_pad = round_up(k, 8);
   void* workspace = nullptr;
+  void* owned_workspace = nullptr;   // what this call allocated and must free
   const void* a_use = a;
   const void* b_use = b;
   int64_t lda_use = lda, ldb_use = ldb;
   if (repack_a || repack_b) {
     const size_t a_bytes = repack_a ? static_cast<size_t>(round_up(m * ld_pad * 2, 256)) : 0;
     const size_t b_bytes = repack_b ? static_cast<size_t>(n * ld_pad * 2) : 0;
-    cudaError_t e = cudaMallocAsync(&workspace, a_bytes + b_bytes, stream);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaMallocAsync (repack workspace)");
+    cudaError_t e = cudaSuccess;
+    if (fixed_scratch != nullptr) {
+      if (a_bytes + b_bytes > fixed_scratch_bytes) {
+        char buf[160];
+        std::snprintf(buf, sizeof(buf),
+                      "repack needs %zu bytes of scratch, more than the %zu-byte static scratch of the no-alloc path",
+                      a_bytes + b_bytes, fixed_scratch_bytes);
+        return fail(GEMM_TN_ERR_INVALID_VALUE, buf);
+      }
+      workspace = fixed_scratch;
+    } else {
+      e = cudaMallocAsync(&workspace, a_bytes + b_bytes, stream);
+      if (e != cudaSuccess) return fail_cuda(e, "cudaMallocAsync (repack workspace)");
+      owned_workspace = workspace;
+    }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     if (repack_a) {
       e = launch_repack(a, lda, ws, ld_pad, m, k, dev->num_sms, stream);
@@ -269,7 +287,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
       ldb_use = ld_pad;
     }
     if (e != cudaSuccess) {
-      cudaFreeAsync(workspace, stream);
+      if (owned_workspace) cudaFreeAsync(owned_workspace, stream);
       return fail_cuda(e, "repack launch");
     }
   }
@@ -281,7 +299,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   st = encode_operand_map(&args.tmap_a, bf16, a_use, m, k, lda_use, 128);
   if (st == GEMM_TN_OK) st = encode_operand_map(&args.tmap_b, bf16, b_use, n, k, ldb_use, cfg.b_rows);
   if (st != GEMM_TN_OK) {
-    if (workspace) cudaFreeAsync(workspace, stream);
+    if (owned_workspace) cudaFreeAsync(owned_workspace, stream);
     return st;
   }
   args.c = c;
@@ -294,7 +312,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   args.num_k_blocks = static_cast<int32_t>((k + kBlockK - 1) / kBlockK);
   const int64_t tiles = static_cast<int64_t>(args.num_m_tiles) * args.num_n_tiles;
   if (tiles > INT32_MAX) {
-    if (workspace) cudaFreeAsync(workspace, stream);
+    if (owned_workspace) cudaFreeAsync(owned_workspace, stream);
     return fail(GEMM_TN_ERR_INVALID_VALUE, "too many output tiles");
   }
   args.num_tiles = static_cast<int32_t>(tiles);
@@ -305,17 +323,47 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
 
   const int clusters = resident_clusters(dev, cfg_id, bf16);
   if (clusters <= 0) {
-    if (workspace) cudaFreeAsync(workspace, stream);
+    if (owned_workspace) cudaFreeAsync(owned_workspace, stream);
     return fail(GEMM_TN_ERR_CUDA, "kernel cannot be resident on this device (occupancy query)");
   }
   const int grid = static_cast<int>(std::min<int64_t>(tiles, clusters)) * cfg.cta_group;
   cudaError_t e = cfg.cta_group == 2 ? launch_gemm_2cta(cfg_id, bf16, args, grid, stream)
                                      : launch_gemm_1cta(cfg_id, bf16, args, grid, stream);
-  if (workspace) {
-    cudaError_t e2 = cudaFreeAsync(workspace, stream);
+  if (owned_workspace) {
+    cudaError_t e2 = cudaFreeAsync(owned_workspace, stream);
     if (e == cudaSuccess) e = e2;
   }
   if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+  return GEMM_TN_OK;
+}
+
+// ---------------------------------------------------------------- no-alloc scratch
+//
+// Scratch for gemm_tn_ex_noalloc: file-scope device memory that every GPU
+// loading this library holds until the process exits. Only the repack of a
+// misaligned operand uses it. In host code `g_noalloc_scratch` names a host-side
+// stand-in, not device memory, so its device address is looked up once per
+// device (with that device current) and cached.
+__device__ __align__(256) uint8_t g_noalloc_scratch[GEMM_TN_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[64] = {};
+
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return fail(GEMM_TN_ERR_UNSUPPORTED_DEVICE, "no current CUDA device");
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return fail_cuda(e, "cudaGetSymbolAddress (no-alloc scratch)");
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
   return GEMM_TN_OK;
 }
 
@@ -337,6 +385,22 @@ int gemm_tn(int dtype, int64_t m, int64_t n, int64_t k, const void* a, const voi
 int gemm_tn_ex(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
                void* c, int64_t ldc, int* d_status, gemm_tn_stream_t stream) {
   return run_gemm(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, reinterpret_cast<cudaStream_t>(stream), -1);
+}
+
+int gemm_tn_ex_noalloc(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b,
+                       int64_t ldb, void* c, int64_t ldc, int* d_status, gemm_tn_stream_t stream) {
+  t_last_cuda_error = 0;
+  t_last_message[0] = '\0';
+  int st = validate(dtype, m, n, k, a, lda, b, ldb, c, ldc);
+  if (st != GEMM_TN_OK || m == 0 || n == 0) return st;
+  DeviceFacts* facts = nullptr;
+  st = current_device(&facts);
+  if (st != GEMM_TN_OK) return st;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != GEMM_TN_OK) return st;
+  return run_gemm(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, reinterpret_cast<cudaStream_t>(stream), -1,
+                  scratch, GEMM_TN_NOALLOC_SCRATCH_BYTES);
 }
 
 int gemm_tn_host(int dtype, int64_t m, int64_t n, int64_t k, const void* a_host, const void* b_host, void* c_host,

@@ -89,6 +89,37 @@ GEMM_TN_API int gemm_tn_ex(int dtype, int64_t m, int64_t n, int64_t k, const voi
                int64_t ldb, void* c, int64_t ldc, int* d_status, gemm_tn_stream_t stream);
 
 /*
+ * gemm_tn_ex_noalloc -- gemm_tn_ex for callers that cannot allocate device
+ * memory: the pages this library follows have no counterpart of it.
+ *
+ * Some callers must not call cudaMalloc or cudaMallocAsync: a framework that
+ * has reserved (nearly) all device memory for its own pool at start-up, where
+ * an extra allocation fails or fragments the pool, or a code path with a hard
+ * latency or memory budget, where an allocation can block or fail at the
+ * worst moment. This entry point computes exactly what gemm_tn_ex computes,
+ * with the same arguments and checks, and allocates nothing: the only
+ * temporary memory gemm_tn_ex may need, the padded copy of an operand whose
+ * base or row pitch the tensor-memory-access engine cannot address, comes
+ * from a static device array of GEMM_TN_NOALLOC_SCRATCH_BYTES (64 MiB) that
+ * every GPU loading this library holds until the process exits.
+ *
+ * - The first call on a device looks up that array's device address (with
+ *   the device current) and caches it; make that first call before any
+ *   stream capture on the device.
+ * - A problem whose repacked operands need more than
+ *   GEMM_TN_NOALLOC_SCRATCH_BYTES is rejected with GEMM_TN_ERR_INVALID_VALUE
+ *   and nothing is enqueued. Operands that need no repack use no scratch.
+ * - All calls share the one array and it keeps the last call's contents
+ *   (every byte a call reads is written by that call first). Calls whose GPU
+ *   work overlaps in time (different streams, or threads) race on it:
+ *   serialise them, e.g. on one stream.
+ */
+#define GEMM_TN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+GEMM_TN_API int gemm_tn_ex_noalloc(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda,
+                                   const void* b, int64_t ldb, void* c, int64_t ldc, int* d_status,
+                                   gemm_tn_stream_t stream);
+
+/*
  * gemm_tn_host -- C = A x B^T with contiguous operands in HOST memory
  * (pageable or pinned): copies A and B to the device, runs gemm_tn_ex, copies
  * C back and waits for `stream`. Device buffers come from cudaMallocAsync on

@@ -1,0 +1,94 @@
+"""gemm_tn_ex_noalloc: the entry point for callers that cannot allocate device
+memory (a framework that has reserved the GPU's memory for its own pool, or a
+code path that must not block or fail on an allocation). It must give the
+results gemm_tn_ex gives, taking the repack scratch from the library's static
+device array instead of cudaMallocAsync, and reject problems that would need
+more scratch than that array holds.
+
+This file is collected last on purpose: if it fails, a run that stops at the
+first failure has already run every other test.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import dense_tiled_gemm_03_gb300 as gt
+import oracle
+from dense_tiled_gemm_03_gb300.workloads import make_operands
+
+from _parity import require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+    from dense_tiled_gemm_03_gb300 import build as native_build
+    native_build.build()
+
+
+def _padded(t: torch.Tensor, pad: int, dev) -> torch.Tensor:
+    """A device view of t whose row pitch is t's width + pad elements."""
+    rows, cols = t.shape
+    big = torch.zeros((rows, cols + pad), dtype=t.dtype)
+    big[:, :cols] = t
+    return big.to(dev)[:, :cols]
+
+
+def _call(fn, a, b, c, status):
+    dtype = gt.GEMM_TN_BF16 if a.dtype == torch.bfloat16 else gt.GEMM_TN_F16
+    m, k = a.shape
+    n = b.shape[0]
+    return fn(dtype, m, n, k, a.data_ptr(), a.stride(0), b.data_ptr(), b.stride(0), c.data_ptr(), c.stride(0),
+              status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.parametrize("dtype,mnk,pads", [
+    ("fp16", (301, 503, 409), (0, 0, 0)),     # K = 409: both row pitches misaligned -> both repacked
+    ("bf16", (257, 640, 1000), (3, 0, 5)),    # A padded to an odd pitch, B aligned, C odd pitch
+    ("fp16", (512, 384, 256), (0, 0, 0)),     # aligned: no scratch used at all
+])
+def test_noalloc_matches_gemm_tn_ex_on_two_calls_in_a_row(dtype, mnk, pads):
+    m, n, k = mnk
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, dtype, "uniform", seed=m + n + k)
+    a = _padded(a_cpu, pads[0], dev)
+    b = _padded(b_cpu, pads[1], dev)
+    c_ref = _padded(torch.full((m, n), float("nan"), dtype=a.dtype), pads[2], dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    assert _call(gt.gemm_tn_ex, a, b, c_ref, status) == gt.GEMM_TN_OK
+    torch.cuda.synchronize()
+    ref, bound = oracle.gemm_tn_reference(a_cpu, b_cpu)
+    allowance = oracle.ALLOW_REL * bound + oracle.ALLOW_ABS
+    expected = c_ref.cpu().double().numpy()
+    for call in range(2):
+        c = _padded(torch.full((m, n), float("nan"), dtype=a.dtype), pads[2], dev)
+        rc = _call(gt.gemm_tn_ex_noalloc, a, b, c, status)
+        assert rc == gt.GEMM_TN_OK, gt.gemm_tn_last_error_message()
+        torch.cuda.synchronize()
+        got = c.cpu().double().numpy()
+        assert np.isfinite(got).all(), f"call {call}: unwritten output"
+        assert (np.abs(got - expected) <= allowance).all(), f"call {call}: differs from gemm_tn_ex"
+        assert oracle.parity_report(got, ref, bound).ok, f"call {call}: fails the oracle criterion"
+    assert int(status.item()) == 0
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    """Repacking A and B of 8192 x 4097 fp16 needs 2 * 8192 * 4104 * 2 bytes,
+    more than the 64 MiB static scratch: rejected, nothing written."""
+    m = n = 8192
+    k = 4097
+    dev = torch.device("cuda", 0)
+    a = torch.zeros((m, k), dtype=torch.float16, device=dev)
+    b = torch.zeros((n, k), dtype=torch.float16, device=dev)
+    c = torch.full((m, n), 7.0, dtype=torch.float16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    rc = _call(gt.gemm_tn_ex_noalloc, a, b, c, status)
+    assert rc == gt.GEMM_TN_ERR_INVALID_VALUE
+    assert "static scratch" in gt.gemm_tn_last_error_message()
+    torch.cuda.synchronize()
+    assert (c == 7.0).all()
+    assert gt.GEMM_TN_NOALLOC_SCRATCH_BYTES == 64 * 1024 * 1024
