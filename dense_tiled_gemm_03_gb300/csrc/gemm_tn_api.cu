@@ -127,21 +127,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return g_encode;
 }
 
-// Row-major [rows, cols] 16-bit matrix with pitch `ld` elements, loaded in
-// boxes of 64 columns (128 bytes) x box_rows rows with the 128-byte swizzle
-// the MMA descriptors expect. Out-of-range box elements read as zero.
-int encode_operand_map(CUtensorMap* map, bool bf16, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
-                       int box_rows) {
+// Row-major [rows, cols] 16-bit matrix with pitch `ld` elements, moved in
+// boxes of box_cols x box_rows with the given swizzle. Operands use 64-column
+// (128-byte) boxes with the 128-byte swizzle the MMA descriptors expect; C
+// uses 32 x 32 boxes with the 64-byte swizzle of the epilogue staging.
+// Out-of-range elements read as zero and are not written.
+int encode_matrix_map(CUtensorMap* map, bool bf16, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                      int box_cols, int box_rows, CUtensorMapSwizzle swizzle) {
   auto encode = encode_fn();
   if (encode == nullptr) return fail(GEMM_TN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t elem_strides[2] = {1, 1};
   const CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                             const_cast<void*>(ptr), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[96];
     std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
@@ -213,6 +214,24 @@ int choose_config(int64_t m, int64_t /*n*/, int64_t /*k*/) {
   if (forced >= 0) return forced;
   if (m <= 128) return kCfg1CtaN128;
   return kCfg2CtaN256;
+}
+
+// GEMM_TN_EPILOGUE=direct forces the predicated element-store epilogue even
+// when C could be written through the TMA (used to test both paths).
+bool force_direct_epilogue() {
+  const char* s = std::getenv("GEMM_TN_EPILOGUE");
+  return s != nullptr && std::strcmp(s, "direct") == 0;
+}
+
+// Test hook: GEMM_TN_TEST_DROP_LOAD=<k-block> makes each CTA's producer skip
+// the loads of that k-block of its first tile, so the MMA issuer's bounded
+// wait on it expires and the watchdog path runs (no fault is involved).
+int test_drop_load_kb() {
+  const char* s = std::getenv("GEMM_TN_TEST_DROP_LOAD");
+  if (s == nullptr || *s == '\0') return -1;
+  char* end = nullptr;
+  const long v = std::strtol(s, &end, 10);
+  return (end != s && v >= 0 && v < INT32_MAX) ? static_cast<int>(v) : -1;
 }
 
 uint64_t watchdog_ns() {
@@ -296,14 +315,21 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   const ConfigInfo& cfg = kConfigs[cfg_id];
   alignas(64) gemm_tn_dev::GemmArgs args;
   std::memset(&args, 0, sizeof(args));
-  st = encode_operand_map(&args.tmap_a, bf16, a_use, m, k, lda_use, 128);
-  if (st == GEMM_TN_OK) st = encode_operand_map(&args.tmap_b, bf16, b_use, n, k, ldb_use, cfg.b_rows);
+  st = encode_matrix_map(&args.tmap_a, bf16, a_use, m, k, lda_use, kBlockK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st == GEMM_TN_OK)
+    st = encode_matrix_map(&args.tmap_b, bf16, b_use, n, k, ldb_use, kBlockK, cfg.b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+  // C goes out through the TMA when its base and pitch allow; otherwise the
+  // epilogue's predicated element stores handle any 2-byte-aligned layout.
+  const bool c_tma = tma_compatible(c, ldc) && !force_direct_epilogue();
+  if (st == GEMM_TN_OK && c_tma)
+    st = encode_matrix_map(&args.tmap_c, bf16, c, m, n, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (st != GEMM_TN_OK) {
     if (owned_workspace) cudaFreeAsync(owned_workspace, stream);
     return st;
   }
   args.c = c;
   args.ldc = ldc;
+  args.c_tma_store = c_tma ? 1 : 0;
   args.m = static_cast<int32_t>(m);
   args.n = static_cast<int32_t>(n);
   args.k = static_cast<int32_t>(k);
@@ -384,7 +410,8 @@ int gemm_tn(int dtype, int64_t m, int64_t n, int64_t k, const void* a, const voi
 
 int gemm_tn_ex(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
                void* c, int64_t ldc, int* d_status, gemm_tn_stream_t stream) {
-  return run_gemm(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, reinterpret_cast<cudaStream_t>(stream), -1);
+  return run_gemm(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, reinterpret_cast<cudaStream_t>(stream),
+                  test_drop_load_kb());
 }
 
 int gemm_tn_ex_noalloc(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b,

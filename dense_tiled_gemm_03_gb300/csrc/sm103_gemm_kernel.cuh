@@ -53,8 +53,10 @@ constexpr int kStatusTimeout = 6;      // == GEMM_TN_ERR_TIMEOUT
 struct GemmArgs {
   CUtensorMap tmap_a;     // A: dims {K, M}, box {64, 128}, 128B swizzle
   CUtensorMap tmap_b;     // B: dims {K, N}, box {64, BN / cta_group}, 128B swizzle
+  CUtensorMap tmap_c;     // C: dims {N, M}, box {32, 32}, 64B swizzle (valid when c_tma_store)
   void* c;                // C [M, N], row stride ldc elements
   int64_t ldc;
+  int32_t c_tma_store;    // 1: epilogue stores through the TMA; 0: predicated element stores
   int32_t m, n, k;
   int32_t num_m_tiles, num_n_tiles, num_k_blocks, num_tiles;
   int32_t group_m;        // tile rows per rasterization group
@@ -80,9 +82,13 @@ struct GemmConfig {
   static constexpr int kAccCols = kBlockN;               // fp32 columns per accumulator
   static constexpr int kNumAcc = 2;
   static constexpr uint32_t kTmemCols = kAccCols * kNumAcc;
-  // epilogue staging: per warp 32 rows x (16 packed words + 1 pad word)
+  // epilogue staging, per warp: either 32 rows x (16 packed words + 1 pad
+  // word) for the transposed element stores, or two 32 x 32 16-bit boxes
+  // (2 KiB each, 64-byte swizzle) for the TMA store
   static constexpr int kStageRowWords = 17;
-  static constexpr uint32_t kEpiBytes = kNumEpilogueWarps * 32 * kStageRowWords * 4;
+  static constexpr uint32_t kEpiWarpBytes = 4096;
+  static constexpr uint32_t kEpiBytes = kNumEpilogueWarps * kEpiWarpBytes;
+  static_assert(32 * kStageRowWords * 4 <= kEpiWarpBytes, "transpose staging fits the warp's slot");
   // layout (offsets from the 1024-aligned base)
   static constexpr uint32_t kOffA = 0;
   static constexpr uint32_t kOffB = kOffA + kStages * kATileBytes;
@@ -101,6 +107,7 @@ struct GemmConfig {
   static_assert(kATileBytes % 1024 == 0 && kBTileBytes % 1024 == 0, "swizzle atoms stay 1024-aligned");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
   static_assert(kOffBar >= kOffEpi + kEpiBytes, "barriers after every buffer");
+  static_assert(kOffEpi % 1024 == 0, "TMA-store staging boxes stay swizzle-aligned");
   static_assert(kSmemBytes <= 232448, "fits the opt-in shared memory of one CTA");
 };
 
@@ -338,12 +345,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
   } else {
     // ------------------------------------------------------------------ epilogue
     const uint32_t quarter = warp & 3u;           // TMEM lanes this warp may read
-    uint32_t* stg = reinterpret_cast<uint32_t*>(smem + Cfg::kOffEpi) +
-                    (warp - kFirstEpilogueWarp) * 32 * Cfg::kStageRowWords;
+    uint8_t* warp_stage = smem + Cfg::kOffEpi + (warp - kFirstEpilogueWarp) * Cfg::kEpiWarpBytes;
+    uint32_t* stg = reinterpret_cast<uint32_t*>(warp_stage);
+    const uint32_t stage_addr = smem_addr(warp_stage);
+    const bool tma_store = args.c_tma_store != 0;
+    int store_buf = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     const uint32_t acc_empty_leader0 =
         (Cfg::kCtaGroup == 2) ? map_to_cta(acc_empty_bar(0), 0) : acc_empty_bar(0);
+    uint16_t* cptr = static_cast<uint16_t*>(args.c);
     for (int tile = cluster_id; tile < args.num_tiles; tile += num_clusters) {
       int tm, tn;
       tile_coords(tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tn);
@@ -352,36 +363,73 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       const int row0 = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM + static_cast<int>(quarter) * 32;
       const int col_tile = tn * Cfg::kBlockN;
       const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + static_cast<uint32_t>(acc * Cfg::kAccCols);
-      uint16_t* cptr = static_cast<uint16_t*>(args.c);
-      for (int chunk = 0; chunk < Cfg::kBlockN / 32; ++chunk) {
+      // 32-column chunks of this tile that lie inside N (warp-uniform, >= 1)
+      const int chunks = min(Cfg::kBlockN / 32, (args.n - col_tile + 31) / 32);
+      for (int chunk = 0; chunk < chunks; ++chunk) {
         const int col0 = col_tile + chunk * 32;
-        if (col0 >= args.n) break;   // the rest of this tile lies past N (warp-uniform)
         uint32_t r[32];
         tmem_load_32x32(t_row + static_cast<uint32_t>(chunk * 32), r);
         tmem_load_wait();
-        // this thread holds row (row0 + lane), columns [col0, col0 + 32)
-#pragma unroll
-        for (int j = 0; j < 16; ++j) store_pair_bits<Cfg>(stg[lane * Cfg::kStageRowWords + j], r[2 * j], r[2 * j + 1]);
-        __syncwarp();
-        // transpose through shared memory: each store instruction writes 32
-        // consecutive columns of one row
-        const int col = col0 + static_cast<int>(lane);
-        const bool col_ok = col < args.n;
-#pragma unroll 4
-        for (int rr = 0; rr < 32; ++rr) {
-          const int row = row0 + rr;
-          const uint16_t v = reinterpret_cast<const uint16_t*>(stg + rr * Cfg::kStageRowWords)[lane];
-          if (col_ok && row < args.m) cptr[static_cast<int64_t>(row) * args.ldc + col] = v;
+        if (chunk == chunks - 1) {
+          // the accumulator is in registers now: hand it back to the MMA warp
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (Cfg::kCtaGroup == 2) {
+              mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
+            } else {
+              mbar_arrive(acc_empty_bar(acc));
+            }
+          }
         }
-        __syncwarp();
-      }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (Cfg::kCtaGroup == 2) {
-          mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
+        // this thread holds row (row0 + lane), columns [col0, col0 + 32)
+        uint32_t packed[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) store_pair_bits<Cfg>(packed[j], r[2 * j], r[2 * j + 1]);
+        // The TMA store writes whole 32 x 32 boxes: only boxes that lie inside
+        // M and N go that way (a box crossing N is not clipped element by
+        // element); edge chunks use the predicated element stores.
+        const bool box_inside = col0 + 32 <= args.n && row0 + 32 <= args.m;
+        if (tma_store && box_inside) {
+          // the TMA store that last read this buffer must be done with it
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+          const uint32_t buf = stage_addr + static_cast<uint32_t>(store_buf) * 2048u;
+          // 64-byte-swizzled 32 x 32 box: 16-byte chunk j of row r sits at
+          // chunk position j ^ ((r >> 1) & 3) of the row's 64 bytes
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t pos = static_cast<uint32_t>(j) ^ ((lane >> 1) & 3u);
+            st_shared_v4(buf + lane * 64u + pos * 16u, packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                         packed[4 * j + 3]);
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&args.tmap_c, buf, col0, row0);
+            bulk_commit_group();
+          }
+          store_buf ^= 1;
         } else {
-          mbar_arrive(acc_empty_bar(acc));
+          if (tma_store) {
+            // the staging block doubles as the TMA boxes: let pending stores finish reading it
+            if (lane == 0) bulk_wait_group_read<0>();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) stg[lane * Cfg::kStageRowWords + j] = packed[j];
+          __syncwarp();
+          // transpose through shared memory: each store instruction writes 32
+          // consecutive columns of one row
+          const int col = col0 + static_cast<int>(lane);
+          const bool col_ok = col < args.n;
+#pragma unroll 4
+          for (int rr = 0; rr < 32; ++rr) {
+            const int row = row0 + rr;
+            const uint16_t v = reinterpret_cast<const uint16_t*>(stg + rr * Cfg::kStageRowWords)[lane];
+            if (col_ok && row < args.m) cptr[static_cast<int64_t>(row) * args.ldc + col] = v;
+          }
+          __syncwarp();
         }
       }
       if (++acc == Cfg::kNumAcc) {
@@ -389,6 +437,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         acc_phase ^= 1u;
       }
     }
+    if (tma_store && lane == 0) bulk_wait_group_all();   // stores complete before the CTA exits
+    __syncwarp();
   }
 
   // ------------------------------------------------------------------ teardown

@@ -32,6 +32,9 @@
  *     kernel stops, leaves C unspecified and, if the caller passed `d_status`,
  *     stores GEMM_TN_ERR_TIMEOUT there (first error wins; the caller zeroes
  *     it and reads it after synchronising).
+ *     The environment variable GEMM_TN_TEST_DROP_LOAD=<k-block> is a test
+ *     hook of gemm_tn_ex: the kernel skips that k-block's loads of its first
+ *     tiles so that a wait expires and the watchdog path runs.
  *   - Thread-safe: the only shared state is a per-device cache of attributes.
  *   - Only compute capability 10.3 (GB300) devices are supported.
  */

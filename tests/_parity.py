@@ -20,29 +20,40 @@ def require_gpu():
     assert (major, minor) == (10, 3), f"expected a GB300 (sm_103), got sm_{major}{minor}"
 
 
-class forced_config:
-    """Context manager: run the library with GEMM_TN_FORCE_CONFIG set."""
+class env_var:
+    """Context manager: set (or, with None, unset) one environment variable."""
 
-    def __init__(self, name: str | None):
-        self.name = name
-        self.old = None
+    def __init__(self, key: str, value: str | None):
+        self.key, self.value, self.old = key, value, None
 
     def __enter__(self):
-        self.old = os.environ.get("GEMM_TN_FORCE_CONFIG")
-        if self.name is None:
-            os.environ.pop("GEMM_TN_FORCE_CONFIG", None)
+        self.old = os.environ.get(self.key)
+        if self.value is None:
+            os.environ.pop(self.key, None)
         else:
-            os.environ["GEMM_TN_FORCE_CONFIG"] = self.name
+            os.environ[self.key] = self.value
         return self
 
     def __exit__(self, *exc):
         if self.old is None:
-            os.environ.pop("GEMM_TN_FORCE_CONFIG", None)
+            os.environ.pop(self.key, None)
         else:
-            os.environ["GEMM_TN_FORCE_CONFIG"] = self.old
+            os.environ[self.key] = self.old
 
 
-def gpu_gemm(a_cpu: torch.Tensor, b_cpu: torch.Tensor, config: str | None = None, out_fill=float("nan")):
+def forced_config(name: str | None):
+    """Run the library with GEMM_TN_FORCE_CONFIG set to a configuration name."""
+    return env_var("GEMM_TN_FORCE_CONFIG", name)
+
+
+def epilogue_mode(mode: str):
+    """"auto": TMA-store epilogue whenever C allows it; "direct": force the
+    predicated element-store epilogue."""
+    return env_var("GEMM_TN_EPILOGUE", "direct" if mode == "direct" else None)
+
+
+def gpu_gemm(a_cpu: torch.Tensor, b_cpu: torch.Tensor, config: str | None = None, out_fill=float("nan"),
+             epilogue: str = "auto"):
     """Copy A, B to cuda:0, run mm_tn (C pre-filled with NaN so every element
     must be written), return C on the CPU and the device status word."""
     dev = torch.device("cuda", 0)
@@ -50,7 +61,7 @@ def gpu_gemm(a_cpu: torch.Tensor, b_cpu: torch.Tensor, config: str | None = None
     b = b_cpu.to(dev)
     out = torch.full((a.shape[0], b.shape[0]), out_fill, dtype=a.dtype, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    with forced_config(config):
+    with forced_config(config), epilogue_mode(epilogue):
         gt.mm_tn(a, b, out=out, status=status)
     torch.cuda.synchronize()
     return out.cpu(), int(status.item())

@@ -15,7 +15,7 @@ import torch
 import dense_tiled_gemm_03_gb300 as gt
 from dense_tiled_gemm_03_gb300.workloads import WORKLOADS, make_operands, workload_operands
 
-from _parity import (assert_parity, assert_sampled_parity, edge_indices, forced_config, gpu_gemm,
+from _parity import (assert_parity, assert_sampled_parity, edge_indices, epilogue_mode, forced_config, gpu_gemm,
                      require_gpu)
 
 pytestmark = pytest.mark.gpu
@@ -37,15 +37,36 @@ ODD_SHAPES = [(1, 1, 1), (1, 1, 64), (7, 13, 17), (128, 256, 64), (129, 257, 65)
               (300, 200, 1000), (64, 1024, 8), (513, 129, 200), (1000, 1000, 64)]
 
 
+@pytest.mark.parametrize("epilogue", ["auto", "direct"])
 @pytest.mark.parametrize("config", CONFIGS)
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("mnk", ODD_SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_odd_shapes(mnk, dtype, config):
+def test_odd_shapes(mnk, dtype, config, epilogue):
     m, n, k = mnk
     a, b = make_operands(m, n, k, dtype, "uniform", seed=m * 131 + n * 7 + k)
-    c, status = gpu_gemm(a, b, config)
+    c, status = gpu_gemm(a, b, config, epilogue=epilogue)
     assert status == 0
-    assert_parity(c, a, b, f"{mnk} {dtype} {config}")
+    assert_parity(c, a, b, f"{mnk} {dtype} {config} {epilogue}")
+
+
+@pytest.mark.parametrize("config", CONFIGS)
+@pytest.mark.parametrize("mn", [(257, 250), (1000, 1003), (129, 40), (300, 1000), (1001, 264)])
+def test_ragged_output_with_aligned_pitch(mn, config):
+    """Ragged M and N but a C pitch that is a multiple of 8: the epilogue goes
+    through TMA stores whose boxes are clipped at M and N; the pad columns of
+    C must stay untouched."""
+    m, n = mn
+    k = 320
+    ldc = (n + 7) // 8 * 8 + 8
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "bf16", "uniform", seed=m + n)
+    c_big = torch.full((m, ldc), float("nan"), dtype=torch.bfloat16, device=dev)
+    c = c_big[:, :n]
+    with forced_config(config):
+        gt.mm_tn(a_cpu.to(dev), b_cpu.to(dev), out=c)
+    torch.cuda.synchronize()
+    assert_parity(c.cpu(), a_cpu, b_cpu, f"{mn} {config}")
+    assert torch.isnan(c_big[:, n:].float()).all(), "wrote past N"
 
 
 # ------------------------------------------------------------ the five workloads
@@ -163,6 +184,26 @@ def test_padded_and_misaligned_strides(pad):
         assert torch.isnan(c_big[:, n:].float()).all(), "wrote outside C"
 
 
+@pytest.mark.parametrize("config", CONFIGS)
+@pytest.mark.parametrize("k", [203, 1001, 65])
+def test_k_tail_with_aligned_pitch_ignores_padding(k, config):
+    """K not a multiple of 8 but row pitches that are (no repack): the pad
+    columns past K hold NaN and must never reach the product."""
+    m, n = 300, 264
+    ld = (k + 7) // 8 * 8 + 8
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "fp16", "uniform", seed=k)
+    a_big = torch.full((m, ld), float("nan"), dtype=torch.float16)
+    a_big[:, :k] = a_cpu
+    b_big = torch.full((n, ld), float("nan"), dtype=torch.float16)
+    b_big[:, :k] = b_cpu
+    c = torch.full((m, n), float("nan"), dtype=torch.float16, device=dev)
+    with forced_config(config):
+        gt.mm_tn(a_big.to(dev)[:, :k], b_big.to(dev)[:, :k], out=c)
+    torch.cuda.synchronize()
+    assert_parity(c.cpu(), a_cpu, b_cpu, f"k={k} {config}")
+
+
 def test_misaligned_base_pointers():
     """Operands starting 2 bytes past a 16-byte boundary (repack path) and an
     output starting 2 bytes past one (predicated stores)."""
@@ -184,8 +225,9 @@ def test_misaligned_base_pointers():
     assert torch.isnan(c_buf[:1].float()).all()
 
 
+@pytest.mark.parametrize("epilogue", ["auto", "direct"])
 @pytest.mark.parametrize("config", CONFIGS)
-def test_repeated_launches_are_bit_identical(config):
+def test_repeated_launches_are_bit_identical(config, epilogue):
     """NaN canary + determinism: C is re-filled with NaN before each launch,
     every launch must overwrite all of it, and all launches agree bit for bit
     (a corrupted barrier shows up as sporadic NaNs or differences)."""
@@ -195,7 +237,7 @@ def test_repeated_launches_are_bit_identical(config):
     a, b = a_cpu.to(dev), b_cpu.to(dev)
     out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
     first = None
-    with forced_config(config):
+    with forced_config(config), epilogue_mode(epilogue):
         for _ in range(20):
             out.fill_(float("nan"))
             gt.mm_tn(a, b, out=out)
@@ -227,3 +269,32 @@ def test_plain_entry_point_and_host_entry_point_agree():
     assert torch.equal(c_host, c_ex)
     c_host = gt.mm_tn_host(a_cpu, b_cpu)   # pageable
     assert torch.equal(c_host, c_ex)
+
+
+# ------------------------------------------------------------ device watchdog
+
+@pytest.mark.parametrize("config", ["1cta_n256", "2cta_n256"])
+def test_watchdog_reports_timeout_and_context_survives(config):
+    """A wait that can never complete (the producer skips one k-block's loads
+    through the test hook) must end within the watchdog budget with
+    GEMM_TN_ERR_TIMEOUT in the status word; afterwards the context is usable
+    and a normal call is correct."""
+    import time
+    from _parity import env_var
+    m, n, k = 512, 512, 512
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "bf16", "uniform", seed=4)
+    a, b = a_cpu.to(dev), b_cpu.to(dev)
+    out = torch.zeros((m, n), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    t0 = time.perf_counter()
+    with forced_config(config), env_var("GEMM_TN_WATCHDOG_MS", "200"), env_var("GEMM_TN_TEST_DROP_LOAD", "2"):
+        gt.mm_tn(a, b, out=out, status=status)
+        torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(status.item()) == gt.GEMM_TN_ERR_TIMEOUT
+    assert elapsed < 5.0, f"watchdog took {elapsed:.1f} s"
+    status.zero_()
+    c, st = gpu_gemm(a_cpu, b_cpu, config)
+    assert st == 0
+    assert_parity(c, a_cpu, b_cpu, "after watchdog")
