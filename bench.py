@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--config", default=None, help="force a kernel configuration (GEMM_TN_FORCE_CONFIG)")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="budget of the whole --impl reference run (oracle work)")
     return ap.parse_args()
 
 
@@ -314,8 +316,8 @@ def run_native(args, dist: Dist, peaks, peak_src):
 
 def run_reference(args, dist: Dist):
     """The CPU oracle, timed as it stands on this host's cores: each step is a
-    bounded row sample of the workload, sized so the whole run takes about two
-    minutes."""
+    bounded row sample of the workload, sized so the whole run takes about
+    --ref-seconds (two minutes by default)."""
     from dense_tiled_gemm_03_gb300.workloads import WORKLOADS, workload_operands
     import oracle
 
@@ -328,7 +330,7 @@ def run_reference(args, dist: Dist):
     t0 = time.perf_counter()
     oracle.gemm_tn_reference(a_cpu[:probe], b_cpu)
     per_row = (time.perf_counter() - t0) / probe
-    rows = int(max(1, min(w.m, 120.0 / total / max(per_row, 1e-9))))
+    rows = int(max(1, min(w.m, args.ref_seconds / total / max(per_row, 1e-9))))
     for i in range(args.warmup):
         r0 = (i * rows) % w.m
         oracle.gemm_tn_reference(a_cpu[r0:r0 + rows], b_cpu)

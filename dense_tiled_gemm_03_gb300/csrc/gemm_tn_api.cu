@@ -248,6 +248,58 @@ uint64_t watchdog_ns() {
 // fixed_scratch: nullptr = repack workspace from cudaMallocAsync (the normal
 // path); otherwise a caller-designated device buffer of fixed_scratch_bytes
 // that is used instead and never freed (gemm_tn_ex_noalloc).
+// How the tiles of one call are shared out over the grid's workers (CTA
+// pairs or single CTAs). Whole waves of tiles go data-parallel; when the last
+// wave would leave workers idle, the final `clusters + remainder` tiles are
+// split by k-block iterations into one contiguous range per worker, each at
+// least one tile long, so every worker finishes at about the same time
+// ("Tiling a matmul", "Where it breaks": stream-K keeps all SMs busy). With
+// fewer tiles than workers, the whole problem is split that way, at least
+// kMinSkIters k-blocks per worker.
+struct WorkPlan {
+  int workers;
+  int64_t dp_tiles;
+  int64_t sk_iters;
+};
+
+constexpr int64_t kMinSkIters = 8;
+
+WorkPlan plan_work(int64_t tiles, int64_t k_blocks, int clusters, bool stream_k) {
+  WorkPlan p{static_cast<int>(std::min<int64_t>(tiles, clusters)), tiles, 0};
+  if (!stream_k) return p;
+  if (tiles >= clusters) {
+    const int64_t rem = tiles % clusters;
+    if (rem == 0) return p;
+    const int64_t sk_tiles = rem + clusters;
+    p.workers = clusters;
+    p.dp_tiles = tiles - sk_tiles;
+    p.sk_iters = sk_tiles * k_blocks;
+    return p;
+  }
+  const int64_t iters = tiles * k_blocks;
+  const int64_t w = std::min<int64_t>(clusters, iters / kMinSkIters);
+  if (w > tiles) {
+    p.workers = static_cast<int>(w);
+    p.dp_tiles = 0;
+    p.sk_iters = iters;
+  }
+  return p;
+}
+
+// The stream-K tail is opt-in (GEMM_TN_STREAMK=1). Measured on GB300 it
+// balances the SMs perfectly but lowers every SM's tensor-pipe activity more
+// than it saves: with all 152 SMs streaming operands at once each reaches
+// ~68% tensor activity, while in the data-parallel schedule the partial last
+// wave runs with fewer SMs at up to ~84% (fp16 4096^3: 88.6 us vs 84.8 us).
+bool stream_k_enabled() {
+  const char* s = std::getenv("GEMM_TN_STREAMK");
+  return s != nullptr && std::strcmp(s, "1") == 0;
+}
+
+// Tile rows per rasterization group: tiles in flight together then share
+// about 2048 rows of A and the matching columns of B in L2.
+int group_rows(const ConfigInfo& cfg) { return cfg.cta_group == 2 ? 8 : 16; }
+
 int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
              void* c, int64_t ldc, int* d_status, cudaStream_t stream, int drop_load_kb,
              void* fixed_scratch = nullptr, size_t fixed_scratch_bytes = 0) {
@@ -267,52 +319,77 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   }
   const bool bf16 = dtype == GEMM_TN_BF16;
 
-  // Operands the TMA cannot address directly go through a padded workspace.
+  const int cfg_id = choose_config(m, n, k);
+  const ConfigInfo& cfg = kConfigs[cfg_id];
+  const int64_t num_m_tiles = (m + cfg.tile_m - 1) / cfg.tile_m;
+  const int64_t num_n_tiles = (n + cfg.block_n - 1) / cfg.block_n;
+  const int64_t num_k_blocks = (k + kBlockK - 1) / kBlockK;
+  const int64_t tiles = num_m_tiles * num_n_tiles;
+  if (tiles > INT32_MAX) return fail(GEMM_TN_ERR_INVALID_VALUE, "too many output tiles");
+  const int clusters = resident_clusters(dev, cfg_id, bf16);
+  if (clusters <= 0) return fail(GEMM_TN_ERR_CUDA, "kernel cannot be resident on this device (occupancy query)");
+  // The no-alloc path keeps to whole tiles: its fixed scratch is for repacks.
+  const WorkPlan plan = plan_work(tiles, num_k_blocks, clusters, stream_k_enabled() && fixed_scratch == nullptr);
+  const int grid_ctas = plan.workers * cfg.cta_group;
+
+  // Workspace: [repacked A][repacked B][stream-K partials][stream-K flags].
+  // Operands the TMA cannot address directly are copied into padded rows.
   const bool repack_a = !tma_compatible(a, lda);
   const bool repack_b = !tma_compatible(b, ldb);
   const int64_t ld_pad = round_up(k, 8);
+  const size_t a_bytes = repack_a ? static_cast<size_t>(round_up(m * ld_pad * 2, 256)) : 0;
+  const size_t b_bytes = repack_b ? static_cast<size_t>(round_up(n * ld_pad * 2, 256)) : 0;
+  const size_t partial_bytes =
+      plan.sk_iters > 0 ? static_cast<size_t>(grid_ctas) * 128 * static_cast<size_t>(cfg.block_n) * 4 : 0;
+  const size_t flag_bytes = plan.sk_iters > 0 ? static_cast<size_t>(grid_ctas) * 4 * sizeof(int) : 0;
+  const size_t ws_bytes = a_bytes + b_bytes + partial_bytes + flag_bytes;
   void* workspace = nullptr;
   void* owned_workspace = nullptr;   // what this call allocated and must free
-  const void* a_use = a;
-  const void* b_use = b;
-  int64_t lda_use = lda, ldb_use = ldb;
-  if (repack_a || repack_b) {
-    const size_t a_bytes = repack_a ? static_cast<size_t>(round_up(m * ld_pad * 2, 256)) : 0;
-    const size_t b_bytes = repack_b ? static_cast<size_t>(n * ld_pad * 2) : 0;
-    cudaError_t e = cudaSuccess;
+  cudaError_t e = cudaSuccess;
+  if (ws_bytes > 0) {
     if (fixed_scratch != nullptr) {
-      if (a_bytes + b_bytes > fixed_scratch_bytes) {
+      if (ws_bytes > fixed_scratch_bytes) {
         char buf[160];
         std::snprintf(buf, sizeof(buf),
                       "repack needs %zu bytes of scratch, more than the %zu-byte static scratch of the no-alloc path",
-                      a_bytes + b_bytes, fixed_scratch_bytes);
+                      ws_bytes, fixed_scratch_bytes);
         return fail(GEMM_TN_ERR_INVALID_VALUE, buf);
       }
       workspace = fixed_scratch;
     } else {
-      e = cudaMallocAsync(&workspace, a_bytes + b_bytes, stream);
-      if (e != cudaSuccess) return fail_cuda(e, "cudaMallocAsync (repack workspace)");
+      e = cudaMallocAsync(&workspace, ws_bytes, stream);
+      if (e != cudaSuccess) return fail_cuda(e, "cudaMallocAsync (workspace)");
       owned_workspace = workspace;
     }
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    if (repack_a) {
-      e = launch_repack(a, lda, ws, ld_pad, m, k, dev->num_sms, stream);
-      a_use = ws;
-      lda_use = ld_pad;
-    }
-    if (e == cudaSuccess && repack_b) {
-      e = launch_repack(b, ldb, ws + a_bytes, ld_pad, n, k, dev->num_sms, stream);
-      b_use = ws + a_bytes;
-      ldb_use = ld_pad;
-    }
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const void* a_use = a;
+  const void* b_use = b;
+  int64_t lda_use = lda, ldb_use = ldb;
+  if (repack_a) {
+    e = launch_repack(a, lda, ws, ld_pad, m, k, dev->num_sms, stream);
+    a_use = ws;
+    lda_use = ld_pad;
+  }
+  if (e == cudaSuccess && repack_b) {
+    e = launch_repack(b, ldb, ws + a_bytes, ld_pad, n, k, dev->num_sms, stream);
+    b_use = ws + a_bytes;
+    ldb_use = ld_pad;
+  }
+  if (e != cudaSuccess) {
+    if (owned_workspace) cudaFreeAsync(owned_workspace, stream);
+    return fail_cuda(e, "repack launch");
+  }
+  float* partials = partial_bytes ? reinterpret_cast<float*>(ws + a_bytes + b_bytes) : nullptr;
+  int* flags = flag_bytes ? reinterpret_cast<int*>(ws + a_bytes + b_bytes + partial_bytes) : nullptr;
+  if (flags != nullptr) {
+    e = cudaMemsetAsync(flags, 0, flag_bytes, stream);
     if (e != cudaSuccess) {
       if (owned_workspace) cudaFreeAsync(owned_workspace, stream);
-      return fail_cuda(e, "repack launch");
+      return fail_cuda(e, "cudaMemsetAsync (stream-K flags)");
     }
   }
 
-  const int cfg_id = choose_config(m, n, k);
-  const ConfigInfo& cfg = kConfigs[cfg_id];
   alignas(64) gemm_tn_dev::GemmArgs args;
   std::memset(&args, 0, sizeof(args));
   st = encode_matrix_map(&args.tmap_a, bf16, a_use, m, k, lda_use, kBlockK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -333,28 +410,22 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   args.m = static_cast<int32_t>(m);
   args.n = static_cast<int32_t>(n);
   args.k = static_cast<int32_t>(k);
-  args.num_m_tiles = static_cast<int32_t>((m + cfg.tile_m - 1) / cfg.tile_m);
-  args.num_n_tiles = static_cast<int32_t>((n + cfg.block_n - 1) / cfg.block_n);
-  args.num_k_blocks = static_cast<int32_t>((k + kBlockK - 1) / kBlockK);
-  const int64_t tiles = static_cast<int64_t>(args.num_m_tiles) * args.num_n_tiles;
-  if (tiles > INT32_MAX) {
-    if (owned_workspace) cudaFreeAsync(owned_workspace, stream);
-    return fail(GEMM_TN_ERR_INVALID_VALUE, "too many output tiles");
-  }
+  args.num_m_tiles = static_cast<int32_t>(num_m_tiles);
+  args.num_n_tiles = static_cast<int32_t>(num_n_tiles);
+  args.num_k_blocks = static_cast<int32_t>(num_k_blocks);
   args.num_tiles = static_cast<int32_t>(tiles);
-  args.group_m = std::min<int32_t>(cfg.cta_group == 2 ? 8 : 16, args.num_m_tiles);
+  args.group_m = static_cast<int32_t>(std::min<int64_t>(group_rows(cfg), num_m_tiles));
   args.status = d_status;
   args.timeout_ns = watchdog_ns();
   args.drop_load_kb = drop_load_kb;
+  args.dp_tiles = static_cast<int32_t>(plan.dp_tiles);
+  args.num_workers = plan.workers;
+  args.sk_iters = plan.sk_iters;
+  args.partials = partials;
+  args.flags = flags;
 
-  const int clusters = resident_clusters(dev, cfg_id, bf16);
-  if (clusters <= 0) {
-    if (owned_workspace) cudaFreeAsync(owned_workspace, stream);
-    return fail(GEMM_TN_ERR_CUDA, "kernel cannot be resident on this device (occupancy query)");
-  }
-  const int grid = static_cast<int>(std::min<int64_t>(tiles, clusters)) * cfg.cta_group;
-  cudaError_t e = cfg.cta_group == 2 ? launch_gemm_2cta(cfg_id, bf16, args, grid, stream)
-                                     : launch_gemm_1cta(cfg_id, bf16, args, grid, stream);
+  e = cfg.cta_group == 2 ? launch_gemm_2cta(cfg_id, bf16, args, grid_ctas, stream)
+                         : launch_gemm_1cta(cfg_id, bf16, args, grid_ctas, stream);
   if (owned_workspace) {
     cudaError_t e2 = cudaFreeAsync(owned_workspace, stream);
     if (e == cudaSuccess) e = e2;

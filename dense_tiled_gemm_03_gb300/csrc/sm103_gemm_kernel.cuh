@@ -63,6 +63,16 @@ struct GemmArgs {
   int* status;            // nullable device int: first error code wins
   uint64_t timeout_ns;    // per-wait watchdog budget
   int32_t drop_load_kb;   // test hook: producer of tile 0 skips this k-block's loads (-1: never)
+  // Work split over the num_workers clusters of the grid. Tiles [0, dp_tiles)
+  // go whole and round-robin to the workers. The sk_iters k-block iterations
+  // of tiles [dp_tiles, num_tiles) (stream-K tail) are cut into num_workers
+  // contiguous ranges; a tile cut between workers is finished by the worker
+  // holding its first k-block, which adds the others' fp32 partials.
+  int32_t dp_tiles;
+  int32_t num_workers;
+  int64_t sk_iters;
+  float* partials;        // per CTA: block_n / 32 chunks x 128 rows x 32 fp32 (stream-K only)
+  int* flags;             // per CTA and epilogue warp: 1 once its partial rows are written (zeroed by the host)
 };
 
 template <int kCtaGroup_, int kBlockN_, int kStages_, bool kBf16_>
@@ -124,6 +134,77 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m_tiles, int num_n
   tn = in_group / rows;
 }
 
+// ---------------------------------------------------------------- work split
+
+struct WorkItem {
+  int tile;        // tile index in raster order
+  int kb_begin;    // first k-block of this item
+  int kb_end;      // one past the last k-block
+};
+
+// First stream-K iteration of `worker`'s range.
+__device__ __forceinline__ int64_t sk_range_begin(const GemmArgs& a, int worker) {
+  return a.sk_iters * worker / a.num_workers;
+}
+
+// Worker whose stream-K range holds iteration i (ranges are non-empty).
+__device__ __forceinline__ int sk_worker_of(const GemmArgs& a, int64_t i) {
+  int w = static_cast<int>(i * a.num_workers / a.sk_iters);
+  while (w + 1 < a.num_workers && sk_range_begin(a, w + 1) <= i) ++w;
+  while (w > 0 && sk_range_begin(a, w) > i) --w;
+  return w;
+}
+
+// The sequence of work items of one worker: its stream-K range first, cut at
+// tile boundaries (a contributed tail, whole tiles, then the head of the tile
+// it finishes), then its whole tiles. Running the range first means every
+// contributor's partial is written early, and the finisher's fix-up epilogue
+// overlaps the main loop of the whole tiles that follow. Every role of a CTA
+// walks the same sequence.
+struct WorkCursor {
+  int64_t dp_next, sk_cur, sk_end;
+
+  __device__ __forceinline__ WorkCursor(const GemmArgs& a, int worker)
+      : dp_next(worker), sk_cur(0), sk_end(0) {
+    if (a.sk_iters > 0) {
+      sk_cur = sk_range_begin(a, worker);
+      sk_end = sk_range_begin(a, worker + 1);
+    }
+  }
+
+  __device__ __forceinline__ bool next(const GemmArgs& a, WorkItem& w) {
+    if (sk_cur < sk_end) {
+      const int64_t t = sk_cur / a.num_k_blocks;
+      const int kb0 = static_cast<int>(sk_cur - t * a.num_k_blocks);
+      const int64_t left = sk_end - sk_cur;
+      const int kb1 = left < a.num_k_blocks - kb0 ? kb0 + static_cast<int>(left) : a.num_k_blocks;
+      w.tile = a.dp_tiles + static_cast<int>(t);
+      w.kb_begin = kb0;
+      w.kb_end = kb1;
+      sk_cur += kb1 - kb0;
+      return true;
+    }
+    if (dp_next < a.dp_tiles) {
+      w.tile = static_cast<int>(dp_next);
+      w.kb_begin = 0;
+      w.kb_end = a.num_k_blocks;
+      dp_next += a.num_workers;
+      return true;
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
 template <class Cfg>
 __device__ __forceinline__ void store_pair_bits(uint32_t& out, uint32_t lo, uint32_t hi) {
   const float flo = __uint_as_float(lo), fhi = __uint_as_float(hi);
@@ -150,6 +231,21 @@ struct Watchdog {
     const uint64_t deadline = globaltimer_ns() + args->timeout_ns;
     while (true) {
       if (mbar_try_wait<kCluster>(bar, parity)) return true;
+      if (*abort_flag) return false;
+      if (globaltimer_ns() > deadline) {
+        fail();
+        return false;
+      }
+    }
+  }
+
+  // Wait until a global flag written by another CTA reads 1; false on
+  // timeout or when another role has already given up.
+  __device__ __forceinline__ bool wait_flag(const int* flag) const {
+    if (ld_acquire_gpu(flag) == 1) return true;
+    const uint64_t deadline = globaltimer_ns() + args->timeout_ns;
+    while (true) {
+      if (ld_acquire_gpu(flag) == 1) return true;
       if (*abort_flag) return false;
       if (globaltimer_ns() > deadline) {
         fail();
@@ -230,8 +326,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
   const uint32_t tmem_base = *tmem_slot;
 
   const Watchdog<Cfg> wd{&args, abort_flag, smem_addr(const_cast<uint32_t*>(abort_flag))};
-  const int num_clusters = gridDim.x / Cfg::kCtaGroup;
-  const int cluster_id = blockIdx.x / Cfg::kCtaGroup;
+  const int worker = static_cast<int>(blockIdx.x) / Cfg::kCtaGroup;
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
@@ -241,20 +336,22 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       int issued_phase_of[Cfg::kStages];
       for (int s = 0; s < Cfg::kStages; ++s) issued_phase_of[s] = -1;
       bool ok = true;
-      int local_tile = 0;
-      for (int tile = cluster_id; tile < args.num_tiles && ok; tile += num_clusters, ++local_tile) {
+      int item_index = 0;
+      WorkCursor cursor(args, worker);
+      WorkItem item;
+      while (ok && cursor.next(args, item)) {
         int tm, tn;
-        tile_coords(tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tn);
+        tile_coords(item.tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tn);
         const int a_row = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM;
         const int b_row = tn * Cfg::kBlockN + static_cast<int>(cta_rank) * Cfg::kBRows;
-        for (int kb = 0; kb < args.num_k_blocks; ++kb) {
+        for (int kb = item.kb_begin; kb < item.kb_end; ++kb) {
           if (!wd.wait(empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
           }
           const uint32_t fb = full_bar(stage);
           if (leader) mbar_arrive_expect_tx(fb, Cfg::kCtaGroup * Cfg::kStageBytes);
-          const bool drop = local_tile == 0 && kb == args.drop_load_kb;
+          const bool drop = item_index == 0 && kb == args.drop_load_kb;
           if (!drop) {
             const int x = kb * Cfg::kBlockK;
             if constexpr (Cfg::kCtaGroup == 2) {
@@ -272,8 +369,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             phase ^= 1u;
           }
         }
+        ++item_index;
       }
-      (void)ok;
       if (leader) {
         // Loads may still be landing if another role gave up: wait (bounded)
         // for the last phase issued into every stage before the CTA may exit.
@@ -292,14 +389,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = cluster_id; tile < args.num_tiles && ok; tile += num_clusters) {
+      WorkCursor cursor(args, worker);
+      WorkItem item;
+      while (ok && cursor.next(args, item)) {
         if (!wd.wait(acc_empty_bar(acc), acc_phase ^ 1u)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
-        for (int kb = 0; kb < args.num_k_blocks; ++kb) {
+        for (int kb = item.kb_begin; kb < item.kb_end; ++kb) {
           if (!wd.wait(full_bar(stage), phase)) {
             ok = false;
             break;
@@ -311,7 +410,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
           for (int kk = 0; kk < Cfg::kBlockK / Cfg::kMmaK; ++kk) {
             // advancing 16 elements along K = 32 bytes = 2 descriptor units
             mma_f16<Cfg::kCtaGroup>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, Cfg::kIdesc,
-                                    (kb > 0 || kk > 0) ? 1u : 0u);
+                                    (kb > item.kb_begin || kk > 0) ? 1u : 0u);
           }
           if constexpr (Cfg::kCtaGroup == 2) {
             mma_commit_pair(empty_bar(stage), 0x3);
@@ -345,7 +444,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
   } else {
     // ------------------------------------------------------------------ epilogue
     const uint32_t quarter = warp & 3u;           // TMEM lanes this warp may read
-    uint8_t* warp_stage = smem + Cfg::kOffEpi + (warp - kFirstEpilogueWarp) * Cfg::kEpiWarpBytes;
+    const uint32_t epi_warp = warp - kFirstEpilogueWarp;
+    uint8_t* warp_stage = smem + Cfg::kOffEpi + epi_warp * Cfg::kEpiWarpBytes;
     uint32_t* stg = reinterpret_cast<uint32_t*>(warp_stage);
     const uint32_t stage_addr = smem_addr(warp_stage);
     const bool tma_store = args.c_tma_store != 0;
@@ -355,16 +455,50 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
     const uint32_t acc_empty_leader0 =
         (Cfg::kCtaGroup == 2) ? map_to_cta(acc_empty_bar(0), 0) : acc_empty_bar(0);
     uint16_t* cptr = static_cast<uint16_t*>(args.c);
-    for (int tile = cluster_id; tile < args.num_tiles; tile += num_clusters) {
+    // fp32 partial rows of this thread: [chunk][128 rows][32] per CTA slot
+    constexpr int kChunks = Cfg::kBlockN / 32;
+    const int64_t row_in_cta = static_cast<int64_t>(quarter) * 32 + lane;
+    bool ok = true;
+    WorkCursor cursor(args, worker);
+    WorkItem item;
+    while (ok && cursor.next(args, item)) {
       int tm, tn;
-      tile_coords(tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tn);
+      tile_coords(item.tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tn);
       if (!wd.wait(acc_full_bar(acc), acc_phase)) break;
       tc_fence_after_sync();
       const int row0 = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM + static_cast<int>(quarter) * 32;
       const int col_tile = tn * Cfg::kBlockN;
       const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + static_cast<uint32_t>(acc * Cfg::kAccCols);
       // 32-column chunks of this tile that lie inside N (warp-uniform, >= 1)
-      const int chunks = min(Cfg::kBlockN / 32, (args.n - col_tile + 31) / 32);
+      const int chunks = min(kChunks, (args.n - col_tile + 31) / 32);
+      // stream-K roles of this item: a contributor (does not hold the first
+      // k-block) writes fp32 partial rows; the finisher (holds the first
+      // k-block of a cut tile) adds the contributors' partials
+      const bool contributor = item.kb_begin > 0;
+      int first_contrib = 0, last_contrib = -1;
+      if (!contributor && item.kb_end < args.num_k_blocks) {
+        const int64_t t_local = item.tile - args.dp_tiles;
+        first_contrib = worker + 1;
+        last_contrib = sk_worker_of(args, (t_local + 1) * args.num_k_blocks - 1);
+        for (int w = first_contrib; w <= last_contrib && ok; ++w) {
+          const int cta = w * Cfg::kCtaGroup + static_cast<int>(cta_rank);
+          ok = wd.wait_flag(args.flags + cta * kNumEpilogueWarps + quarter);
+        }
+        if (!ok) break;
+      }
+      // finisher: partial rows of the next chunk are loaded one chunk ahead
+      const bool finisher = last_contrib >= first_contrib;
+      const int64_t part_row = row_in_cta;
+      auto partial_src = [&](int w, int chunk) {
+        const int cta = w * Cfg::kCtaGroup + static_cast<int>(cta_rank);
+        return reinterpret_cast<const float4*>(
+            args.partials + ((static_cast<int64_t>(cta) * kChunks + chunk) * 128 + part_row) * 32);
+      };
+      float4 pre[8];
+      if (finisher) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pre[j] = __ldcg(partial_src(first_contrib, 0) + j);
+      }
       for (int chunk = 0; chunk < chunks; ++chunk) {
         const int col0 = col_tile + chunk * 32;
         uint32_t r[32];
@@ -379,6 +513,40 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
               mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
             } else {
               mbar_arrive(acc_empty_bar(acc));
+            }
+          }
+        }
+        if (contributor) {
+          float4* dst = reinterpret_cast<float4*>(
+              args.partials + ((static_cast<int64_t>(blockIdx.x) * kChunks + chunk) * 128 + row_in_cta) * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          continue;
+        }
+        if (finisher) {
+          // add the contributors' partials in worker order: the first one was
+          // loaded ahead; the next chunk's first partial is issued now
+          for (int w = first_contrib; w <= last_contrib; ++w) {
+            float4 v[8];
+            if (w == first_contrib) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[j] = pre[j];
+              if (chunk + 1 < chunks) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) pre[j] = __ldcg(partial_src(first_contrib, chunk + 1) + j);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[j] = __ldcg(partial_src(w, chunk) + j);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + v[j].x);
+              r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + v[j].y);
+              r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v[j].z);
+              r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v[j].w);
             }
           }
         }
@@ -431,6 +599,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
           }
           __syncwarp();
         }
+      }
+      if (contributor) {
+        // publish this warp's partial rows: each lane's writes are made
+        // visible at GPU scope before lane 0 raises the flag
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(args.flags + blockIdx.x * kNumEpilogueWarps + quarter, 1);
       }
       if (++acc == Cfg::kNumAcc) {
         acc = 0;

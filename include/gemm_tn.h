@@ -32,6 +32,9 @@
  *     kernel stops, leaves C unspecified and, if the caller passed `d_status`,
  *     stores GEMM_TN_ERR_TIMEOUT there (first error wins; the caller zeroes
  *     it and reads it after synchronising).
+ *   - GEMM_TN_STREAMK=1 splits the last partial wave of tiles by k-block
+ *     ranges over all workers (stream-K), with an fp32 workspace from
+ *     cudaMallocAsync on `stream`; off by default (slower on GB300).
  *     The environment variable GEMM_TN_TEST_DROP_LOAD=<k-block> is a test
  *     hook of gemm_tn_ex: the kernel skips that k-block's loads of its first
  *     tiles so that a wait expires and the watchdog path runs.

@@ -298,3 +298,38 @@ def test_watchdog_reports_timeout_and_context_survives(config):
     c, st = gpu_gemm(a_cpu, b_cpu, config)
     assert st == 0
     assert_parity(c, a_cpu, b_cpu, "after watchdog")
+
+
+# ------------------------------------------------------------ stream-K tail
+
+@pytest.mark.parametrize("config", CONFIGS)
+@pytest.mark.parametrize("mnk", [(256, 512, 8192), (300, 1000, 3000), (2000, 2100, 640), (2304, 4352, 1000),
+                                 (128, 4096, 4096)], ids=lambda s: "x".join(map(str, s)))
+def test_stream_k_cut_tiles(mnk, config):
+    """Shapes whose tiles do not fill whole waves: the last tiles are cut by
+    k-block ranges across workers (up to ~16 contributors per tile when there
+    are fewer tiles than workers) and finished by the worker holding their
+    first k-block. Parity with stream-K on, and with it off."""
+    from _parity import env_var
+    m, n, k = mnk
+    a, b = make_operands(m, n, k, "bf16", "normal_over_sqrt_k", seed=m ^ n ^ k)
+    for sk in ("1", "0"):
+        with env_var("GEMM_TN_STREAMK", sk):
+            c, status = gpu_gemm(a, b, config)
+        assert status == 0
+        assert_parity(c, a, b, f"{mnk} {config} streamk={sk}")
+
+
+def test_stream_k_is_deterministic():
+    m, n, k = 300, 1000, 3000
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "fp16", "uniform", seed=99)
+    a, b = a_cpu.to(dev), b_cpu.to(dev)
+    outs = []
+    for _ in range(5):
+        out = torch.full((m, n), float("nan"), dtype=torch.float16, device=dev)
+        gt.mm_tn(a, b, out=out)
+        outs.append(out)
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
