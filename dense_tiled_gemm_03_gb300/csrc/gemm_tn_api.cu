@@ -40,10 +40,11 @@ constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
 constexpr int kBlockK = 64;
 
 const ConfigInfo kConfigs[kNumConfigs] = {
-    {"1cta_n256", 1, 128, 256, 256, 4, 0},
-    {"1cta_n128", 1, 128, 128, 128, 6, 0},
-    {"2cta_n256", 2, 256, 256, 128, 6, 0},
-    {"2cta_n128", 2, 256, 128, 64, 8, 0},
+    {"1cta_n256", 1, 128, 256, 256, 4, 1, 128},
+    {"1cta_n128", 1, 128, 128, 128, 6, 1, 128},
+    {"2cta_n256", 2, 256, 256, 128, 6, 1, 128},
+    {"2cta_n128", 2, 256, 128, 64, 8, 1, 128},
+    {"2cta_n256_mc", 2, 256, 256, 128, 6, 2, 64},
 };
 
 thread_local int t_last_cuda_error = 0;
@@ -203,17 +204,27 @@ int parse_forced_config() {
   return -1;
 }
 
-// The frozen table, from measurements on GB300 (bf16 8192^3: pair tile 1698
-// TFLOP/s vs 1565 for the single-CTA 128 x 256 tile; fp16 4096^3: 1346 vs
-// 1202; fp16 3001 x 5003 x 4097: 751 vs 623). Pair tiles (256 x 256) for every
-// shape with more than one 128-row block of output rows; a single-CTA 128 x 128
-// tile when M fits one block, so the N dimension alone supplies the tiles
-// (bf16 128 x 16384 x 16384: 5.2 TB/s vs 4.9 for the pair tile).
-int choose_config(int64_t m, int64_t /*n*/, int64_t /*k*/) {
+// The frozen table, from measurements on GB300.
+//  * M <= 128: single-CTA 128 x 128 tiles, so the N dimension alone supplies
+//    the tiles (bf16 128 x 16384 x 16384: 5.3 TB/s vs 4.9 for pair tiles).
+//  * Otherwise 256 x 256 tiles on CTA pairs (bf16 8192^3: 1698 TFLOP/s vs 1565
+//    for single-CTA 128 x 256 tiles), either as plain pairs (76 resident on
+//    GB300) or as 4-CTA clusters of two pairs sharing A through multicast (36
+//    resident: 144 of the 152 SMs). A multicast cluster streams ~5% more work
+//    per SM (fp16 4096^3: 1534 vs 1503 TFLOP/s; fp16 3001 x 5003 x 4097: 857 vs
+//    741), so it is chosen when its rounds of tiles, discounted by that 5%,
+//    are fewer than the pairs' rounds (bf16 8192^3: 15 rounds vs 14, so pairs).
+int choose_config(int64_t m, int64_t n, int64_t /*k*/, int resident_pairs = 76, int resident_quads = 36) {
   const int forced = parse_forced_config();
   if (forced >= 0) return forced;
   if (m <= 128) return kCfg1CtaN128;
-  return kCfg2CtaN256;
+  const int64_t tile_rows = (m + 255) / 256;
+  const int64_t pair_tiles = tile_rows * ((n + 255) / 256);
+  const int64_t quad_tiles = tile_rows * ((n + 511) / 512);
+  const double pair_rounds = static_cast<double>((pair_tiles + resident_pairs - 1) / std::max(resident_pairs, 1));
+  const double quad_rounds =
+      static_cast<double>((quad_tiles + resident_quads - 1) / std::max(resident_quads, 1)) / 1.05;
+  return quad_rounds < pair_rounds ? kCfg2CtaN256Mc : kCfg2CtaN256;
 }
 
 // GEMM_TN_EPILOGUE=direct forces the predicated element-store epilogue even
@@ -319,18 +330,22 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   }
   const bool bf16 = dtype == GEMM_TN_BF16;
 
-  const int cfg_id = choose_config(m, n, k);
+  const int cfg_id = choose_config(m, n, k, resident_clusters(dev, kCfg2CtaN256, bf16),
+                                   resident_clusters(dev, kCfg2CtaN256Mc, bf16));
   const ConfigInfo& cfg = kConfigs[cfg_id];
   const int64_t num_m_tiles = (m + cfg.tile_m - 1) / cfg.tile_m;
-  const int64_t num_n_tiles = (n + cfg.block_n - 1) / cfg.block_n;
+  // columns per scheduled tile: a multicast cluster covers two pairs' tiles
+  const int64_t cluster_n = static_cast<int64_t>(cfg.block_n) * cfg.cluster_pairs;
+  const int64_t num_n_tiles = (n + cluster_n - 1) / cluster_n;
   const int64_t num_k_blocks = (k + kBlockK - 1) / kBlockK;
   const int64_t tiles = num_m_tiles * num_n_tiles;
   if (tiles > INT32_MAX) return fail(GEMM_TN_ERR_INVALID_VALUE, "too many output tiles");
   const int clusters = resident_clusters(dev, cfg_id, bf16);
   if (clusters <= 0) return fail(GEMM_TN_ERR_CUDA, "kernel cannot be resident on this device (occupancy query)");
   // The no-alloc path keeps to whole tiles: its fixed scratch is for repacks.
-  const WorkPlan plan = plan_work(tiles, num_k_blocks, clusters, stream_k_enabled() && fixed_scratch == nullptr);
-  const int grid_ctas = plan.workers * cfg.cta_group;
+  const WorkPlan plan = plan_work(tiles, num_k_blocks, clusters,
+                                  stream_k_enabled() && fixed_scratch == nullptr && cfg.cluster_pairs == 1);
+  const int grid_ctas = plan.workers * cfg.cta_group * cfg.cluster_pairs;
 
   // Workspace: [repacked A][repacked B][stream-K partials][stream-K flags].
   // Operands the TMA cannot address directly are copied into padded rows.
@@ -392,7 +407,8 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
 
   alignas(64) gemm_tn_dev::GemmArgs args;
   std::memset(&args, 0, sizeof(args));
-  st = encode_matrix_map(&args.tmap_a, bf16, a_use, m, k, lda_use, kBlockK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  st = encode_matrix_map(&args.tmap_a, bf16, a_use, m, k, lda_use, kBlockK, cfg.a_box_rows,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
   if (st == GEMM_TN_OK)
     st = encode_matrix_map(&args.tmap_b, bf16, b_use, n, k, ldb_use, kBlockK, cfg.b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
   // C goes out through the TMA when its base and pitch allow; otherwise the
@@ -542,7 +558,25 @@ int gemm_tn_host(int dtype, int64_t m, int64_t n, int64_t k, const void* a_host,
 int gemm_tn_select_config(int dtype, int64_t m, int64_t n, int64_t k) {
   if (dtype != GEMM_TN_F16 && dtype != GEMM_TN_BF16) return -1;
   if (m <= 0 || n <= 0 || k <= 0 || m > kMaxDim || n > kMaxDim || k > kMaxDim) return -1;
-  return choose_config(m, n, k);
+  // resident cluster counts of the current device when it is a GB300,
+  // otherwise GB300's (76 CTA pairs, 36 four-CTA clusters)
+  int pairs = 76, quads = 36;
+  int dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    DeviceFacts* facts = nullptr;
+    if (current_device(&facts) == GEMM_TN_OK) {
+      const bool bf16 = dtype == GEMM_TN_BF16;
+      const int p = resident_clusters(facts, kCfg2CtaN256, bf16);
+      const int q = resident_clusters(facts, kCfg2CtaN256Mc, bf16);
+      if (p > 0 && q > 0) {
+        pairs = p;
+        quads = q;
+      }
+    }
+  } else {
+    cudaGetLastError();
+  }
+  return choose_config(m, n, k, pairs, quads);
 }
 
 int gemm_tn_num_configs(void) { return kNumConfigs; }

@@ -21,17 +21,19 @@ enum ConfigId : int {
   kCfg1CtaN128 = 1,   // one CTA per 128 x 128 tile, 6-stage ring (skinny / few tiles)
   kCfg2CtaN256 = 2,   // CTA pair per 256 x 256 tile (cta_group::2), 6-stage ring
   kCfg2CtaN128 = 3,   // CTA pair per 256 x 128 tile (cta_group::2), 8-stage ring
-  kNumConfigs = 4
+  kCfg2CtaN256Mc = 4, // 4-CTA cluster: two pairs on 256 x 512, A shared by TMA multicast
+  kNumConfigs = 5
 };
 
 struct ConfigInfo {
   const char* name;
   int cta_group;
-  int tile_m;      // rows per tile (128 * cta_group)
-  int block_n;     // columns per tile
-  int b_rows;      // rows of B one CTA loads (block_n / cta_group)
+  int tile_m;        // rows per tile (128 * cta_group)
+  int block_n;       // columns per tile (per CTA pair)
+  int b_rows;        // rows of B one CTA loads (block_n / cta_group)
   int stages;
-  int smem_bytes;
+  int cluster_pairs; // CTA pairs per cluster (2: A shared by multicast)
+  int a_box_rows;    // rows of A one TMA load brings (64 with multicast halves)
 };
 
 const ConfigInfo& config_info(int id);

@@ -1,6 +1,6 @@
 // sm103_gemm_2cta.cu -- instantiations of the tcgen05 GEMM kernel with a CTA
-// pair (a 2-CTA cluster on two SMs, cta_group::2) per 256 x 256 or 256 x 128
-// output tile.
+// pair (cta_group::2, two SMs) per 256 x 256 or 256 x 128 output tile, and the
+// 4-CTA cluster variant whose two pairs share A through TMA multicast.
 #include "gemm_tn_internal.h"
 #include "sm103_launch.cuh"
 
@@ -10,6 +10,9 @@ using CfgPairF16 = gemm_tn_dev::GemmConfig<2, 256, 6, false>;
 using CfgPairBf16 = gemm_tn_dev::GemmConfig<2, 256, 6, true>;
 using CfgPair128F16 = gemm_tn_dev::GemmConfig<2, 128, 8, false>;
 using CfgPair128Bf16 = gemm_tn_dev::GemmConfig<2, 128, 8, true>;
+// two pairs per cluster sharing A through TMA multicast
+using CfgPairMcF16 = gemm_tn_dev::GemmConfig<2, 256, 6, false, 2>;
+using CfgPairMcBf16 = gemm_tn_dev::GemmConfig<2, 256, 6, true, 2>;
 
 cudaError_t launch_gemm_2cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream) {
   switch (id) {
@@ -18,6 +21,9 @@ cudaError_t launch_gemm_2cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& arg
     case kCfg2CtaN128:
       return bf16 ? Launcher<CfgPair128Bf16>::launch(args, grid, stream)
                   : Launcher<CfgPair128F16>::launch(args, grid, stream);
+    case kCfg2CtaN256Mc:
+      return bf16 ? Launcher<CfgPairMcBf16>::launch(args, grid, stream)
+                  : Launcher<CfgPairMcF16>::launch(args, grid, stream);
     default:
       return cudaErrorInvalidValue;
   }
@@ -29,6 +35,8 @@ int max_resident_2cta(int id, bool bf16) {
       return bf16 ? Launcher<CfgPairBf16>::max_clusters() : Launcher<CfgPairF16>::max_clusters();
     case kCfg2CtaN128:
       return bf16 ? Launcher<CfgPair128Bf16>::max_clusters() : Launcher<CfgPair128F16>::max_clusters();
+    case kCfg2CtaN256Mc:
+      return bf16 ? Launcher<CfgPairMcBf16>::max_clusters() : Launcher<CfgPairMcF16>::max_clusters();
     default:
       return 0;
   }

@@ -75,9 +75,16 @@ struct GemmArgs {
   int* flags;             // per CTA and epilogue warp: 1 once its partial rows are written (zeroed by the host)
 };
 
-template <int kCtaGroup_, int kBlockN_, int kStages_, bool kBf16_>
+template <int kCtaGroup_, int kBlockN_, int kStages_, bool kBf16_, int kClusterPairs_ = 1>
 struct GemmConfig {
   static constexpr int kCtaGroup = kCtaGroup_;
+  // kClusterPairs == 2: a cluster of two CTA pairs side by side along N that
+  // share their rows of A. Each CTA loads one 64-row half of its A block and
+  // TMA-multicasts it to the CTA at the same position in the other pair.
+  static constexpr int kClusterPairs = kClusterPairs_;
+  static constexpr bool kMulticastA = kClusterPairs == 2;
+  static constexpr int kClusterSize = kCtaGroup * kClusterPairs;
+  static constexpr int kClusterN = kBlockN_ * kClusterPairs;   // output columns per cluster
   static constexpr int kBlockM = 128;                    // rows per CTA
   static constexpr int kTileM = kBlockM * kCtaGroup;     // rows per tile (MMA M)
   static constexpr int kBlockN = kBlockN_;               // columns per tile (MMA N)
@@ -104,7 +111,9 @@ struct GemmConfig {
   static constexpr uint32_t kOffB = kOffA + kStages * kATileBytes;
   static constexpr uint32_t kOffEpi = kOffB + kStages * kBTileBytes;
   static constexpr uint32_t kOffBar = (kOffEpi + kEpiBytes + 7u) & ~7u;
-  static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1;   // full, empty, acc_full, acc_empty, drain
+  // full, empty, acc_full, acc_empty, drain
+  static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1;
+  static constexpr uint32_t kAHalfBytes = kATileBytes / 2;
   static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
   static constexpr uint32_t kSmemUsed = kOffAbort + 4;
@@ -113,6 +122,7 @@ struct GemmConfig {
 
   static_assert(kBlockN % 32 == 0 && kBlockN >= 32 && kBlockN <= 256, "MMA N");
   static_assert(kCtaGroup == 1 || kCtaGroup == 2, "cta group");
+  static_assert(kClusterPairs == 1 || (kClusterPairs == 2 && kCtaGroup == 2), "A multicast pairs CTA pairs");
   static_assert(kBRows % 8 == 0 && kBRows <= 256, "TMA box rows");
   static_assert(kATileBytes % 1024 == 0 && kBTileBytes % 1024 == 0, "swizzle atoms stay 1024-aligned");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
@@ -226,7 +236,7 @@ struct Watchdog {
   // Wait for the phase of `bar` with parity `parity`; false on timeout or
   // when another role has already given up.
   __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
-    constexpr bool kCluster = Cfg::kCtaGroup == 2;
+    constexpr bool kCluster = Cfg::kClusterSize > 1;
     if (mbar_try_wait<kCluster>(bar, parity)) return true;
     const uint64_t deadline = globaltimer_ns() + args->timeout_ns;
     while (true) {
@@ -256,7 +266,7 @@ struct Watchdog {
 
   // Bounded wait used while draining after a failure: never sets the flag.
   __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
-    constexpr bool kCluster = Cfg::kCtaGroup == 2;
+    constexpr bool kCluster = Cfg::kClusterSize > 1;
     const uint64_t deadline = globaltimer_ns() + args->timeout_ns;
     while (!mbar_try_wait<kCluster>(bar, parity)) {
       if (globaltimer_ns() > deadline) return false;
@@ -267,8 +277,10 @@ struct Watchdog {
   __device__ __forceinline__ void fail() const {
     if (args->status != nullptr) atomicCAS(args->status, 0, kStatusTimeout);
     *abort_flag = 1u;
-    if constexpr (Cfg::kCtaGroup == 2) {
-      st_cluster_u32(map_to_cta(abort_addr, cluster_ctarank() ^ 1u), 1u);
+    if constexpr (Cfg::kClusterSize > 1) {
+      const uint32_t me = cluster_ctarank();
+      for (uint32_t r = 0; r < static_cast<uint32_t>(Cfg::kClusterSize); ++r)
+        if (r != me) st_cluster_u32(map_to_cta(abort_addr, r), 1u);
     }
   }
 };
@@ -282,7 +294,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
 
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
-  const uint32_t cta_rank = (Cfg::kCtaGroup == 2) ? cluster_ctarank() : 0u;
+  const uint32_t cluster_rank = (Cfg::kClusterSize > 1) ? cluster_ctarank() : 0u;
+  const uint32_t cta_rank = (Cfg::kCtaGroup == 2) ? (cluster_rank & 1u) : 0u;   // position in the CTA pair
+  const uint32_t pair = Cfg::kMulticastA ? (cluster_rank >> 1) : 0u;            // pair within the cluster
+  const uint32_t pair_leader = cluster_rank & ~1u;
   const bool leader = cta_rank == 0;
 
   auto a_tile = [&](int s) { return base + Cfg::kOffA + s * Cfg::kATileBytes; };
@@ -297,8 +312,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) {
+      // full: the pair leader's expect-tx arrival and both CTAs' bytes
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      // empty: one MMA commit per CTA pair that reads the stage
+      mbar_init(empty_bar(s), Cfg::kClusterPairs);
     }
     for (int a = 0; a < Cfg::kNumAcc; ++a) {
       mbar_init(acc_full_bar(a), 1);
@@ -317,7 +334,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
     tmem_relinquish<Cfg::kCtaGroup>();
   }
   tc_fence_before_sync();
-  if constexpr (Cfg::kCtaGroup == 2) {
+  if constexpr (Cfg::kClusterSize > 1) {
     cluster_sync_all();
   } else {
     __syncthreads();
@@ -326,7 +343,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
   const uint32_t tmem_base = *tmem_slot;
 
   const Watchdog<Cfg> wd{&args, abort_flag, smem_addr(const_cast<uint32_t*>(abort_flag))};
-  const int worker = static_cast<int>(blockIdx.x) / Cfg::kCtaGroup;
+  const int worker = static_cast<int>(blockIdx.x) / Cfg::kClusterSize;
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
@@ -340,8 +357,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       WorkCursor cursor(args, worker);
       WorkItem item;
       while (ok && cursor.next(args, item)) {
-        int tm, tn;
-        tile_coords(item.tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tn);
+        int tm, tj;
+        tile_coords(item.tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tj);
+        const int tn = tj * Cfg::kClusterPairs + static_cast<int>(pair);
         const int a_row = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM;
         const int b_row = tn * Cfg::kBlockN + static_cast<int>(cta_rank) * Cfg::kBRows;
         for (int kb = item.kb_begin; kb < item.kb_end; ++kb) {
@@ -350,12 +368,33 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             break;
           }
           const uint32_t fb = full_bar(stage);
-          if (leader) mbar_arrive_expect_tx(fb, Cfg::kCtaGroup * Cfg::kStageBytes);
           const bool drop = item_index == 0 && kb == args.drop_load_kb;
+          if constexpr (Cfg::kMulticastA) {
+            // A: this CTA loads one 64-row half of its A block and multicasts
+            // it to the CTA at the same position in the other pair; every
+            // destination pair's leader counts the bytes, so the leader
+            // expects both halves for both of its CTAs plus both B tiles,
+            // the same total as without multicast.
+            if (leader) mbar_arrive_expect_tx(fb, Cfg::kCtaGroup * Cfg::kStageBytes);
+            if (!drop) {
+              const int x = kb * Cfg::kBlockK;
+              const uint16_t mask = static_cast<uint16_t>((1u << cta_rank) | (1u << (2u + cta_rank)));
+              tma_load_2d_multicast_pair(&args.tmap_a, a_tile(stage) + pair * Cfg::kAHalfBytes, fb & 0xFEFFFFFFu, x,
+                                         a_row + static_cast<int>(pair) * (Cfg::kBlockM / 2), mask);
+              tma_load_2d_pair(&args.tmap_b, b_tile(stage), map_to_cta(fb, pair_leader), x, b_row);
+            }
+            issued_phase_of[stage] = static_cast<int>(phase);
+            if (++stage == Cfg::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
+          if (leader) mbar_arrive_expect_tx(fb, Cfg::kCtaGroup * Cfg::kStageBytes);
           if (!drop) {
             const int x = kb * Cfg::kBlockK;
             if constexpr (Cfg::kCtaGroup == 2) {
-              const uint32_t fb_leader = map_to_cta(fb, 0);
+              const uint32_t fb_leader = map_to_cta(fb, pair_leader);
               tma_load_2d_pair(&args.tmap_a, a_tile(stage), fb_leader, x, a_row);
               tma_load_2d_pair(&args.tmap_b, b_tile(stage), fb_leader, x, b_row);
             } else {
@@ -371,14 +410,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         }
         ++item_index;
       }
-      if (leader) {
-        // Loads may still be landing if another role gave up: wait (bounded)
-        // for the last phase issued into every stage before the CTA may exit.
-        // On the normal path these phases have completed already. The
-        // leader's full barriers count the peer's bytes too.
-        for (int s = 0; s < Cfg::kStages; ++s) {
-          if (issued_phase_of[s] >= 0) wd.drain(full_bar(s), static_cast<uint32_t>(issued_phase_of[s]));
-        }
+      // Loads may still be landing if another role gave up: wait (bounded)
+      // for the last phase issued into every stage before the CTA may exit.
+      // On the normal path these phases have completed already. The
+      // leader's full barriers count the peer's bytes (and, with multicast,
+      // the other pair's halves) too.
+      for (int s = 0; s < Cfg::kStages; ++s) {
+        if (issued_phase_of[s] >= 0 && leader) wd.drain(full_bar(s), static_cast<uint32_t>(issued_phase_of[s]));
       }
     }
   } else if (warp == kMmaWarp) {
@@ -412,7 +450,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             mma_f16<Cfg::kCtaGroup>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, Cfg::kIdesc,
                                     (kb > item.kb_begin || kk > 0) ? 1u : 0u);
           }
-          if constexpr (Cfg::kCtaGroup == 2) {
+          if constexpr (Cfg::kMulticastA) {
+            mma_commit_pair(empty_bar(stage), 0xF);   // both pairs' buffers hold halves of this A
+          } else if constexpr (Cfg::kCtaGroup == 2) {
             mma_commit_pair(empty_bar(stage), 0x3);
           } else {
             mma_commit(empty_bar(stage));
@@ -424,7 +464,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         }
         if (!ok) break;
         if constexpr (Cfg::kCtaGroup == 2) {
-          mma_commit_pair(acc_full_bar(acc), 0x3);
+          mma_commit_pair(acc_full_bar(acc), static_cast<uint16_t>(0x3u << pair_leader));
         } else {
           mma_commit(acc_full_bar(acc));
         }
@@ -435,7 +475,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       }
       // All MMAs issued by this thread must finish before TMEM is freed.
       if constexpr (Cfg::kCtaGroup == 2) {
-        mma_commit_pair(drain_bar, 0x1);
+        mma_commit_pair(drain_bar, static_cast<uint16_t>(1u << cluster_rank));
       } else {
         mma_commit(drain_bar);
       }
@@ -453,7 +493,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
     int acc = 0;
     uint32_t acc_phase = 0;
     const uint32_t acc_empty_leader0 =
-        (Cfg::kCtaGroup == 2) ? map_to_cta(acc_empty_bar(0), 0) : acc_empty_bar(0);
+        (Cfg::kCtaGroup == 2) ? map_to_cta(acc_empty_bar(0), pair_leader) : acc_empty_bar(0);
     uint16_t* cptr = static_cast<uint16_t*>(args.c);
     // fp32 partial rows of this thread: [chunk][128 rows][32] per CTA slot
     constexpr int kChunks = Cfg::kBlockN / 32;
@@ -462,15 +502,27 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
     WorkCursor cursor(args, worker);
     WorkItem item;
     while (ok && cursor.next(args, item)) {
-      int tm, tn;
-      tile_coords(item.tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tn);
+      int tm, tj;
+      tile_coords(item.tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tj);
+      const int tn = tj * Cfg::kClusterPairs + static_cast<int>(pair);
       if (!wd.wait(acc_full_bar(acc), acc_phase)) break;
       tc_fence_after_sync();
       const int row0 = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM + static_cast<int>(quarter) * 32;
       const int col_tile = tn * Cfg::kBlockN;
       const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + static_cast<uint32_t>(acc * Cfg::kAccCols);
-      // 32-column chunks of this tile that lie inside N (warp-uniform, >= 1)
-      const int chunks = min(kChunks, (args.n - col_tile + 31) / 32);
+      // 32-column chunks of this tile that lie inside N (warp-uniform; 0 when
+      // a multicast cluster's second pair lies wholly past N)
+      const int chunks = max(0, min(kChunks, (args.n - col_tile + 31) / 32));
+      if (chunks == 0) {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
+        if (++acc == Cfg::kNumAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+        continue;
+      }
       // stream-K roles of this item: a contributor (does not hold the first
       // k-block) writes fp32 partial rows; the finisher (holds the first
       // k-block of a cut tile) adds the contributors' partials
@@ -481,7 +533,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         first_contrib = worker + 1;
         last_contrib = sk_worker_of(args, (t_local + 1) * args.num_k_blocks - 1);
         for (int w = first_contrib; w <= last_contrib && ok; ++w) {
-          const int cta = w * Cfg::kCtaGroup + static_cast<int>(cta_rank);
+          const int cta = w * Cfg::kClusterSize + static_cast<int>(cluster_rank);
           ok = wd.wait_flag(args.flags + cta * kNumEpilogueWarps + quarter);
         }
         if (!ok) break;
@@ -490,7 +542,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       const bool finisher = last_contrib >= first_contrib;
       const int64_t part_row = row_in_cta;
       auto partial_src = [&](int w, int chunk) {
-        const int cta = w * Cfg::kCtaGroup + static_cast<int>(cta_rank);
+        const int cta = w * Cfg::kClusterSize + static_cast<int>(cluster_rank);
         return reinterpret_cast<const float4*>(
             args.partials + ((static_cast<int64_t>(cta) * kChunks + chunk) * 128 + part_row) * 32);
       };
@@ -618,7 +670,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
 
   // ------------------------------------------------------------------ teardown
   tc_fence_before_sync();
-  if constexpr (Cfg::kCtaGroup == 2) {
+  if constexpr (Cfg::kClusterSize > 1) {
     cluster_sync_all();
   } else {
     __syncthreads();

@@ -34,9 +34,9 @@ struct Launcher {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 0;
-    if (Cfg::kCtaGroup > 1) {
+    if (Cfg::kClusterSize > 1) {
       attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = Cfg::kCtaGroup;
+      attr[0].val.clusterDim.x = Cfg::kClusterSize;
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
       cfg.numAttrs = 1;
@@ -57,7 +57,7 @@ struct Launcher {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (Cfg::kCtaGroup == 1) {
+    if (Cfg::kClusterSize == 1) {
       int per_sm = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_tn_dev::gemm_tn_sm103_kernel<Cfg>,
                                                         gemm_tn_dev::kNumThreads, Cfg::kSmemBytes) != cudaSuccess) {
@@ -68,7 +68,7 @@ struct Launcher {
     }
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    fill_config(cfg, attr, sms - sms % Cfg::kCtaGroup, nullptr);
+    fill_config(cfg, attr, sms - sms % Cfg::kClusterSize, nullptr);
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_dev::gemm_tn_sm103_kernel<Cfg>, &cfg) != cudaSuccess) {
       cudaGetLastError();

@@ -113,6 +113,31 @@ __device__ __forceinline__ void tma_load_2d(const void* tmap, uint32_t dst, uint
       : "memory");
 }
 
+// 2-D tile load multicast to every CTA of `cta_mask` in this cluster: the box
+// lands at offset `dst` of each destination CTA's shared memory and each
+// destination's barrier at offset `bar` counts the bytes it received.
+__device__ __forceinline__ void tma_load_2d_multicast(const void* tmap, uint32_t dst, uint32_t bar, int32_t x,
+                                                      int32_t y, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
+// Multicast inside CTA pairs: the box lands at offset `dst` of every CTA in
+// `cta_mask`, and each destination pair's leader (even) CTA counts the bytes
+// on its barrier at the offset of `pair_bar` (a barrier address whose CTA
+// pair bit selects the even CTA).
+__device__ __forceinline__ void tma_load_2d_multicast_pair(const void* tmap, uint32_t dst, uint32_t pair_bar,
+                                                           int32_t x, int32_t y, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(pair_bar), "h"(cta_mask)
+      : "memory");
+}
+
 // Same, inside a CTA pair: the completion barrier may be in the peer CTA
 // (the pair's leader counts both CTAs' bytes).
 __device__ __forceinline__ void tma_load_2d_pair(const void* tmap, uint32_t dst, uint32_t cluster_bar,

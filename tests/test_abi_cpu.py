@@ -47,7 +47,7 @@ def test_version_status_strings_and_configs(lib):
     assert gt.gemm_tn_status_string(gt.GEMM_TN_ERR_TIMEOUT) == "GEMM_TN_ERR_TIMEOUT"
     assert gt.gemm_tn_status_string(99) == "GEMM_TN_ERR_UNKNOWN"
     names = [gt.gemm_tn_config_name(i) for i in range(gt.gemm_tn_num_configs())]
-    assert names == ["1cta_n256", "1cta_n128", "2cta_n256", "2cta_n128"]
+    assert names == ["1cta_n256", "1cta_n128", "2cta_n256", "2cta_n128", "2cta_n256_mc"]
     assert gt.gemm_tn_config_name(-1) == "invalid"
 
 
@@ -55,7 +55,10 @@ def test_config_table(lib, monkeypatch):
     monkeypatch.delenv("GEMM_TN_FORCE_CONFIG", raising=False)
     sel = lambda m, n, k: gt.gemm_tn_config_name(gt.gemm_tn_select_config(gt.GEMM_TN_BF16, m, n, k))
     assert sel(128, 16384, 16384) == "1cta_n128"   # skinny: one 128-row block of outputs
-    assert sel(8192, 8192, 8192) in ("1cta_n256", "2cta_n256")
+    # with GB300's resident clusters (76 pairs, 36 four-CTA clusters):
+    assert sel(8192, 8192, 8192) == "2cta_n256"      # 14 rounds of pair tiles vs 15 of multicast tiles
+    assert sel(4096, 4096, 4096) == "2cta_n256_mc"   # 4 rounds either way: multicast streams more per SM
+    assert sel(3001, 5003, 4097) == "2cta_n256_mc"
     assert gt.gemm_tn_select_config(gt.GEMM_TN_BF16, 0, 5, 5) == -1
     assert gt.gemm_tn_select_config(7, 5, 5, 5) == -1
     monkeypatch.setenv("GEMM_TN_FORCE_CONFIG", "1cta_n128")

@@ -20,7 +20,7 @@ from _parity import (assert_parity, assert_sampled_parity, edge_indices, epilogu
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = ["1cta_n256", "1cta_n128", "2cta_n128", "2cta_n256"]
+CONFIGS = ["1cta_n256", "1cta_n128", "2cta_n128", "2cta_n256", "2cta_n256_mc"]
 
 
 @pytest.fixture(scope="module", autouse=True)
