@@ -280,7 +280,9 @@ def run_native(args, dist: Dist, peaks, peak_src):
            "h2d_bytes_per_step": op_bytes, "d2h_bytes_per_step": w.m * w.n * 2 + 4,
            "steps": args.e2e_steps, "entry_point": "gemm_tn_host (pinned host buffers)"}
 
-    launches_per_step = 1  # the default workloads' operands are TMA-aligned: no repack kernels
+    # one GEMM kernel per step, plus one repack kernel when the operands' row
+    # pitch (K here: the operands are contiguous) is not a multiple of 8
+    launches_per_step = 1 + (1 if w.k % 8 else 0)
     line = {
         "metric": METRIC,
         "value": round(value, 2),

@@ -309,7 +309,15 @@ bool stream_k_enabled() {
 
 // Tile rows per rasterization group: tiles in flight together then share
 // about 2048 rows of A and the matching columns of B in L2.
-int group_rows(const ConfigInfo& cfg) { return cfg.cta_group == 2 ? 8 : 16; }
+// GEMM_TN_GROUP_M overrides it (tuning experiments).
+int group_rows(const ConfigInfo& cfg) {
+  const char* s = std::getenv("GEMM_TN_GROUP_M");
+  if (s != nullptr && *s != '\0') {
+    const long v = std::strtol(s, nullptr, 10);
+    if (v > 0 && v < 65536) return static_cast<int>(v);
+  }
+  return cfg.cta_group == 2 ? 8 : 16;
+}
 
 int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
              void* c, int64_t ldc, int* d_status, cudaStream_t stream, int drop_load_kb,
@@ -381,15 +389,18 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   const void* a_use = a;
   const void* b_use = b;
   int64_t lda_use = lda, ldb_use = ldb;
-  if (repack_a) {
-    e = launch_repack(a, lda, ws, ld_pad, m, k, dev->num_sms, stream);
-    a_use = ws;
-    lda_use = ld_pad;
-  }
-  if (e == cudaSuccess && repack_b) {
-    e = launch_repack(b, ldb, ws + a_bytes, ld_pad, n, k, dev->num_sms, stream);
-    b_use = ws + a_bytes;
-    ldb_use = ld_pad;
+  if (repack_a || repack_b) {
+    RepackRequest req[2] = {{a, lda, ws, ld_pad, repack_a ? m : 0, k},
+                            {b, ldb, ws + a_bytes, ld_pad, repack_b ? n : 0, k}};
+    e = launch_repack2(req, 2, dev->num_sms, stream);
+    if (repack_a) {
+      a_use = ws;
+      lda_use = ld_pad;
+    }
+    if (repack_b) {
+      b_use = ws + a_bytes;
+      ldb_use = ld_pad;
+    }
   }
   if (e != cudaSuccess) {
     if (owned_workspace) cudaFreeAsync(owned_workspace, stream);

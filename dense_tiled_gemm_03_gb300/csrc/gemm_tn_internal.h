@@ -45,8 +45,18 @@ cudaError_t launch_gemm(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, in
 // current device; 0 on error.
 int max_resident_clusters(int id, bool bf16);
 
-// Row repack: dst[r][0:ld_dst] = src[r][0:cols] padded with zeros, for r < rows.
-cudaError_t launch_repack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,
-                          int num_sms, cudaStream_t stream);
+// Row repack of one matrix: dst[r][0:ld_dst] = src[r][0:cols] padded with
+// zeros, for r < rows (ld_dst a multiple of 8, dst 16-byte aligned).
+struct RepackRequest {
+  const void* src;
+  int64_t ld_src;
+  void* dst;
+  int64_t ld_dst;
+  int64_t rows;
+  int64_t cols;
+};
+
+// One launch repacking up to two matrices (entries with rows <= 0 are skipped).
+cudaError_t launch_repack2(const RepackRequest* req, int num, int num_sms, cudaStream_t stream);
 
 }  // namespace gemm_tn_impl

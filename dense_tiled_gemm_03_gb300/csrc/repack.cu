@@ -3,11 +3,18 @@
 // row pitch that is not a multiple of 16 bytes). Each row of `cols` 16-bit
 // elements is copied to a destination whose pitch `ld_dst` is a multiple of 8
 // elements; the padding columns are written as zeros. HBM-bound: every source
-// element is read once and every destination element written once.
+// byte is read once from DRAM and every destination byte written once.
 //
 // "Tiling a matmul", section "Where it breaks" (edge tiles need padding or
 // predicated loads): this is the padding half, used only for misaligned
 // operands; ragged tile edges are handled by the GEMM kernel's bounded loads.
+//
+// One launch repacks up to two matrices (A and B). A CTA walks whole rows;
+// thread t of the CTA produces 16-byte destination chunks t, t + 256, ... of a
+// row. A source row starts at any 2-byte boundary, so each chunk is cut out of
+// the two aligned 16-byte source blocks that overlap it (funnel shifts). Only
+// aligned blocks holding at least one byte of the row are read, so no access
+// leaves the memory the row occupies by more than the rest of its 16-byte block.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -16,27 +23,64 @@
 
 namespace gemm_tn_dev {
 
-// One CTA walks whole rows; consecutive threads take consecutive 16-byte
-// chunks of a destination row, so the stores are full 16-byte vectors and the
-// 2-byte loads of a warp cover one contiguous 512-byte span of the source row.
-__global__ void __launch_bounds__(256) repack_rows_kernel(const uint16_t* __restrict__ src, int64_t ld_src,
-                                                          uint16_t* __restrict__ dst, int64_t ld_dst, int64_t rows,
-                                                          int64_t cols) {
-  const int64_t chunks = ld_dst / 8;
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const uint16_t* s = src + r * ld_src;
-    uint4* d = reinterpret_cast<uint4*>(dst + r * ld_dst);
+struct RepackJob {
+  const uint16_t* src;
+  int64_t ld_src;
+  uint16_t* dst;
+  int64_t ld_dst;
+  int64_t rows;
+  int64_t cols;
+};
+
+struct RepackArgs {
+  RepackJob job[2];
+  int num_jobs;
+};
+
+// 16 bytes starting `shift` bytes (even, 0..14) into the 32 bytes lo:hi.
+__device__ __forceinline__ uint4 extract16(const uint4& lo, const uint4& hi, uint32_t shift) {
+  uint32_t x0, x1, x2, x3, x4;
+  switch (shift >> 2) {
+    case 0: x0 = lo.x; x1 = lo.y; x2 = lo.z; x3 = lo.w; x4 = hi.x; break;
+    case 1: x0 = lo.y; x1 = lo.z; x2 = lo.w; x3 = hi.x; x4 = hi.y; break;
+    case 2: x0 = lo.z; x1 = lo.w; x2 = hi.x; x3 = hi.y; x4 = hi.z; break;
+    default: x0 = lo.w; x1 = hi.x; x2 = hi.y; x3 = hi.z; x4 = hi.w; break;
+  }
+  const uint32_t bits = (shift & 2u) * 8u;   // 0 or 16
+  return make_uint4(__funnelshift_r(x0, x1, bits), __funnelshift_r(x1, x2, bits), __funnelshift_r(x2, x3, bits),
+                    __funnelshift_r(x3, x4, bits));
+}
+
+__global__ void __launch_bounds__(256) repack_rows_kernel(const __grid_constant__ RepackArgs args) {
+  const int64_t rows_a = args.job[0].rows;
+  const int64_t total_rows = rows_a + (args.num_jobs > 1 ? args.job[1].rows : 0);
+  for (int64_t gr = blockIdx.x; gr < total_rows; gr += gridDim.x) {
+    const RepackJob& jb = args.job[gr < rows_a ? 0 : 1];
+    const int64_t r = gr < rows_a ? gr : gr - rows_a;
+    const uintptr_t s = reinterpret_cast<uintptr_t>(jb.src + r * jb.ld_src);
+    const uintptr_t end = s + static_cast<uintptr_t>(jb.cols) * 2;   // one past the row's last byte
+    uint4* d = reinterpret_cast<uint4*>(jb.dst + r * jb.ld_dst);
+    const int64_t chunks = jb.ld_dst / 8;
     for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
-      const int64_t c0 = c * 8;
-      uint32_t w[4];
+      const uintptr_t want = s + static_cast<uintptr_t>(c) * 16;
+      uint4 out = make_uint4(0u, 0u, 0u, 0u);
+      if (want < end) {
+        const uintptr_t base = want & ~static_cast<uintptr_t>(15);
+        const uint32_t shift = static_cast<uint32_t>(want - base);
+        const uint4 lo = *reinterpret_cast<const uint4*>(base);
+        const uint4 hi = (shift != 0 && base + 16 < end) ? *reinterpret_cast<const uint4*>(base + 16)
+                                                          : make_uint4(0u, 0u, 0u, 0u);
+        out = shift == 0 ? lo : extract16(lo, hi, shift);
+        const int64_t valid = jb.cols - c * 8;   // elements of this chunk inside the row
+        if (valid < 8) {
+          uint32_t w[4] = {out.x, out.y, out.z, out.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int64_t e0 = c0 + 2 * j, e1 = e0 + 1;
-        const uint32_t lo = e0 < cols ? s[e0] : 0u;
-        const uint32_t hi = e1 < cols ? s[e1] : 0u;
-        w[j] = lo | (hi << 16);
+          for (int e = 0; e < 8; ++e)
+            if (e >= valid) w[e >> 1] &= (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+          out = make_uint4(w[0], w[1], w[2], w[3]);
+        }
       }
-      d[c] = make_uint4(w[0], w[1], w[2], w[3]);
+      d[c] = out;
     }
   }
 }
@@ -45,13 +89,23 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const uint16_t* __rest
 
 namespace gemm_tn_impl {
 
-cudaError_t launch_repack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows, int64_t cols,
-                          int num_sms, cudaStream_t stream) {
-  if (rows <= 0) return cudaSuccess;
+cudaError_t launch_repack2(const RepackRequest* req, int num, int num_sms, cudaStream_t stream) {
+  gemm_tn_dev::RepackArgs args{};
+  int64_t rows = 0;
+  int n = 0;
+  for (int i = 0; i < num && n < 2; ++i) {
+    if (req[i].rows <= 0) continue;
+    args.job[n] = gemm_tn_dev::RepackJob{static_cast<const uint16_t*>(req[i].src), req[i].ld_src,
+                                         static_cast<uint16_t*>(req[i].dst), req[i].ld_dst, req[i].rows,
+                                         req[i].cols};
+    rows += req[i].rows;
+    ++n;
+  }
+  if (n == 0) return cudaSuccess;
+  args.num_jobs = n;
   const int64_t max_grid = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
   const unsigned grid = static_cast<unsigned>(rows < max_grid ? rows : max_grid);
-  gemm_tn_dev::repack_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(src), ld_src,
-                                                             static_cast<uint16_t*>(dst), ld_dst, rows, cols);
+  gemm_tn_dev::repack_rows_kernel<<<grid, 256, 0, stream>>>(args);
   return cudaGetLastError();
 }
 

@@ -225,6 +225,34 @@ def test_misaligned_base_pointers():
     assert torch.isnan(c_buf[:1].float()).all()
 
 
+@pytest.mark.parametrize("offset", [1, 3, 5, 7])
+@pytest.mark.parametrize("k", [1, 7, 9, 63, 65, 200])
+def test_repack_every_byte_offset(offset, k):
+    """Operands starting 2, 6, 10 or 14 bytes past a 16-byte boundary with
+    pitches that are not multiples of 8: the repack cuts every 16-byte chunk
+    out of two aligned source blocks; NaN guards around the data must never
+    reach C."""
+    m, n = 131, 77
+    ld = k + 3
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "fp16", "uniform", seed=offset * 100 + k)
+    def planted(t):
+        rows = t.shape[0]
+        buf = torch.full((offset + rows * ld + 16,), float("nan"), dtype=t.dtype)
+        view = buf[offset:offset + rows * ld].view(rows, ld)
+        view[:, :k] = t
+        return buf.to(dev), offset
+    a_buf, _ = planted(a_cpu)
+    b_buf, _ = planted(b_cpu)
+    a = a_buf[offset:offset + m * ld].view(m, ld)[:, :k]
+    b = b_buf[offset:offset + n * ld].view(n, ld)[:, :k]
+    assert a.data_ptr() % 16 == 2 * offset
+    c = torch.full((m, n), float("nan"), dtype=torch.float16, device=dev)
+    gt.mm_tn(a, b, out=c)
+    torch.cuda.synchronize()
+    assert_parity(c.cpu(), a_cpu, b_cpu, f"offset {offset} k {k}")
+
+
 @pytest.mark.parametrize("epilogue", ["auto", "direct"])
 @pytest.mark.parametrize("config", CONFIGS)
 def test_repeated_launches_are_bit_identical(config, epilogue):
