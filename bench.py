@@ -38,7 +38,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum); see profiles/. None until a
 # capture of the current kernel exists.
 NCU_TRAFFIC_BYTES = {
-    ("bf16_8192x8192x8192", "1cta_n256"): 951_858_432 + 123_698_432,   # gemm_tn_1cta_n256_bf16_8192.md
+    # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the current
+    # kernels (profiles/gemm_tn_*.md)
+    ("bf16_8192x8192x8192", "2cta_n256"): 1_123_382_272 + 126_294_016,
+    ("fp16_4096x4096x4096", "2cta_n256_mc"): 81_554_944 + 15_040_256,
+    ("bf16_128x16384x16384", "1cta_n128"): 541_129_472 + 3_346_944,
+    ("fp16_3001x5003x4097", "2cta_n256_mc"): 75_436_544 + 9_654_272,
 }
 
 
