@@ -361,3 +361,65 @@ def test_stream_k_is_deterministic():
     torch.cuda.synchronize()
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+# ------------------------------------------------------------ streams, threads, graphs
+
+def test_cuda_graph_capture_and_replay():
+    """The default path (TMA-aligned operands) issues only stream-ordered work,
+    so a call can be captured into a CUDA graph and replayed; after a warm-up
+    call has filled the per-device caches."""
+    m, n, k = 1024, 1536, 2048
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "bf16", "uniform", seed=21)
+    a, b = a_cpu.to(dev), b_cpu.to(dev)
+    out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        gt.mm_tn(a, b, out=out)            # warm-up: attribute and occupancy caches
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        gt.mm_tn(a, b, out=out)
+    out.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert_parity(out.cpu(), a_cpu, b_cpu, "graph replay")
+    # new operand values in the same buffers are picked up by the replay
+    a.copy_(b_cpu[:m].to(dev) if n >= m else a)
+    out.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert_parity(out.cpu(), a.cpu(), b_cpu, "graph replay after operand update")
+
+
+def test_concurrent_calls_from_two_threads_on_two_streams():
+    import threading
+    dev = torch.device("cuda", 0)
+    shapes = [(700, 900, 1100), (513, 1030, 777)]
+    data = [make_operands(m, n, k, "fp16", "uniform", seed=i) for i, (m, n, k) in enumerate(shapes)]
+    results = [None, None]
+    errors = []
+
+    def work(i):
+        try:
+            torch.cuda.set_device(dev)
+            s = torch.cuda.Stream(dev)
+            a, b = data[i][0].to(dev), data[i][1].to(dev)
+            with torch.cuda.stream(s):
+                outs = [gt.mm_tn(a, b) for _ in range(10)]
+            s.synchronize()
+            results[i] = [o.cpu() for o in outs]
+        except Exception as exc:  # pragma: no cover - reported below
+            errors.append(exc)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(2):
+        for o in results[i][1:]:
+            assert torch.equal(o, results[i][0])
+        assert_parity(results[i][0], data[i][0], data[i][1], f"thread {i}")
