@@ -491,6 +491,64 @@ int noalloc_scratch(void** out) {
   return GEMM_TN_OK;
 }
 
+// ---------------------------------------------------------------- host-buffer path
+//
+// Per-device resources of gemm_tn_host, created on its first call on a device
+// and kept until the process exits: two copy streams (host-to-device and
+// device-to-host), the events that chain copies and GEMMs, and a memory pool
+// that keeps the staging memory between calls instead of returning it to the
+// system at every synchronisation.
+struct HostPath {
+  static constexpr int kMaxChunks = 16;
+  bool ready = false;
+  std::mutex mutex;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_b = nullptr, ev_done = nullptr;
+  cudaEvent_t ev_a[kMaxChunks] = {}, ev_c[kMaxChunks] = {};
+  cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_host_path_mutex;
+HostPath g_host_path[64];
+
+int host_path(HostPath** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return fail(GEMM_TN_ERR_UNSUPPORTED_DEVICE, "no current CUDA device");
+  }
+  std::lock_guard<std::mutex> lock(g_host_path_mutex);
+  HostPath& hp = g_host_path[dev];
+  if (!hp.ready) {
+    cudaError_t e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking);
+    const unsigned flags = cudaEventDisableTiming;
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.ev_start, flags);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.ev_b, flags);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.ev_done, flags);
+    for (int i = 0; i < HostPath::kMaxChunks && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&hp.ev_a[i], flags);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.ev_c[i], flags);
+    }
+    if (e == cudaSuccess) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.handleTypes = cudaMemHandleTypeNone;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      e = cudaMemPoolCreate(&hp.pool, &props);
+    }
+    if (e == cudaSuccess) {
+      uint64_t keep = UINT64_MAX;
+      e = cudaMemPoolSetAttribute(hp.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    }
+    if (e != cudaSuccess) return fail_cuda(e, "host-path set-up");
+    hp.ready = true;
+  }
+  *out = &hp;
+  return GEMM_TN_OK;
+}
+
 }  // namespace
 
 const ConfigInfo& config_info(int id) { return kConfigs[id]; }
@@ -534,34 +592,79 @@ int gemm_tn_host(int dtype, int64_t m, int64_t n, int64_t k, const void* a_host,
   t_last_message[0] = '\0';
   int st = validate(dtype, m, n, k, a_host, k, b_host, k, c_host, n);
   if (st != GEMM_TN_OK || m == 0 || n == 0) return st;
+  DeviceFacts* facts = nullptr;
+  st = current_device(&facts);
+  if (st != GEMM_TN_OK) return st;
+  HostPath* hp = nullptr;
+  st = host_path(&hp);
+  if (st != GEMM_TN_OK) return st;
+  std::lock_guard<std::mutex> serial(hp->mutex);   // one host-buffer call per device at a time
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
-  const size_t a_bytes = static_cast<size_t>(m * k * 2), b_bytes = static_cast<size_t>(n * k * 2);
-  const size_t c_bytes = static_cast<size_t>(m * n * 2);
-  const size_t a_off = 0, b_off = static_cast<size_t>(round_up(static_cast<int64_t>(a_bytes), 256));
-  const size_t c_off = b_off + static_cast<size_t>(round_up(static_cast<int64_t>(b_bytes), 256));
+
+  // Device staging with 16-byte row pitches: no repack, TMA-store epilogue.
+  const int64_t ldk = round_up(std::max<int64_t>(k, 1), 8), ldn = round_up(n, 8);
+  const size_t a_bytes = static_cast<size_t>(round_up(m * ldk * 2, 256));
+  const size_t b_bytes = static_cast<size_t>(round_up(n * ldk * 2, 256));
+  const size_t c_bytes = static_cast<size_t>(round_up(m * ldn * 2, 256));
   uint8_t* dev_buf = nullptr;
-  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&dev_buf), c_off + c_bytes + sizeof(int), stream);
-  if (e != cudaSuccess) return fail_cuda(e, "cudaMallocAsync");
-  int* d_status = reinterpret_cast<int*>(dev_buf + c_off + c_bytes);
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&dev_buf), a_bytes + b_bytes + c_bytes + 256,
+                                          hp->pool, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaMallocFromPoolAsync (host-path staging)");
+  uint16_t* d_a = reinterpret_cast<uint16_t*>(dev_buf);
+  uint16_t* d_b = reinterpret_cast<uint16_t*>(dev_buf + a_bytes);
+  uint16_t* d_c = reinterpret_cast<uint16_t*>(dev_buf + a_bytes + b_bytes);
+  int* d_status = reinterpret_cast<int*>(dev_buf + a_bytes + b_bytes + c_bytes);
+
+  // Rows of A (and C) go in chunks of whole 256-row tiles, about 16 MB of A
+  // each, so the copies in both directions overlap the GEMMs of earlier chunks.
+  const int64_t a_host_bytes = m * k * 2;
+  int64_t chunks = std::min<int64_t>(HostPath::kMaxChunks, std::max<int64_t>(1, a_host_bytes / (16ll << 20)));
+  int64_t rows_per = round_up((m + chunks - 1) / chunks, 256);
+  chunks = (m + rows_per - 1) / rows_per;
+
   int rc = GEMM_TN_OK;
-  e = cudaMemsetAsync(d_status, 0, sizeof(int), stream);
-  if (e == cudaSuccess && a_bytes) e = cudaMemcpyAsync(dev_buf + a_off, a_host, a_bytes, cudaMemcpyHostToDevice, stream);
-  if (e == cudaSuccess && b_bytes) e = cudaMemcpyAsync(dev_buf + b_off, b_host, b_bytes, cudaMemcpyHostToDevice, stream);
-  if (e != cudaSuccess) {
-    rc = fail_cuda(e, "host-to-device copy");
-  } else {
-    rc = run_gemm(dtype, m, n, k, dev_buf + a_off, k, dev_buf + b_off, k, dev_buf + c_off, n, d_status, stream, -1);
+  auto check = [&](cudaError_t err, const char* what) {
+    if (rc == GEMM_TN_OK && err != cudaSuccess) rc = fail_cuda(err, what);
+  };
+  check(cudaMemsetAsync(d_status, 0, sizeof(int), stream), "cudaMemsetAsync (status)");
+  check(cudaEventRecord(hp->ev_start, stream), "cudaEventRecord");
+  check(cudaStreamWaitEvent(hp->h2d, hp->ev_start, 0), "cudaStreamWaitEvent");
+  if (k > 0) {
+    check(cudaMemcpy2DAsync(d_b, ldk * 2, b_host, k * 2, k * 2, n, cudaMemcpyHostToDevice, hp->h2d), "copy B");
+  }
+  check(cudaEventRecord(hp->ev_b, hp->h2d), "cudaEventRecord");
+  check(cudaStreamWaitEvent(stream, hp->ev_b, 0), "cudaStreamWaitEvent");
+  for (int64_t i = 0; i < chunks && rc == GEMM_TN_OK; ++i) {
+    const int64_t r0 = i * rows_per, rows = std::min(rows_per, m - r0);
+    if (k > 0) {
+      check(cudaMemcpy2DAsync(d_a + r0 * ldk, ldk * 2, static_cast<const uint8_t*>(a_host) + r0 * k * 2, k * 2,
+                              k * 2, rows, cudaMemcpyHostToDevice, hp->h2d),
+            "copy A");
+    }
+    check(cudaEventRecord(hp->ev_a[i], hp->h2d), "cudaEventRecord");
+    check(cudaStreamWaitEvent(stream, hp->ev_a[i], 0), "cudaStreamWaitEvent");
+    if (rc != GEMM_TN_OK) break;
+    const int gst = run_gemm(dtype, rows, n, k, d_a + r0 * ldk, ldk, d_b, ldk, d_c + r0 * ldn, ldn, d_status, stream,
+                             -1);
+    if (gst != GEMM_TN_OK) {
+      rc = gst;
+      break;
+    }
+    check(cudaEventRecord(hp->ev_c[i], stream), "cudaEventRecord");
+    check(cudaStreamWaitEvent(hp->d2h, hp->ev_c[i], 0), "cudaStreamWaitEvent");
+    check(cudaMemcpy2DAsync(static_cast<uint8_t*>(c_host) + r0 * n * 2, n * 2, d_c + r0 * ldn, ldn * 2, n * 2, rows,
+                            cudaMemcpyDeviceToHost, hp->d2h),
+          "copy C");
   }
   int h_status = 0;
-  if (rc == GEMM_TN_OK) {
-    e = cudaMemcpyAsync(c_host, dev_buf + c_off, c_bytes, cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(&h_status, d_status, sizeof(int), cudaMemcpyDeviceToHost, stream);
-    if (e != cudaSuccess) rc = fail_cuda(e, "device-to-host copy");
-  }
+  check(cudaMemcpyAsync(&h_status, d_status, sizeof(int), cudaMemcpyDeviceToHost, hp->d2h), "copy status");
+  // the staging buffer goes back to the pool only after every copy is done
+  cudaEventRecord(hp->ev_done, hp->d2h);
+  cudaStreamWaitEvent(stream, hp->ev_done, 0);
   cudaError_t ef = cudaFreeAsync(dev_buf, stream);
   cudaError_t es = cudaStreamSynchronize(stream);
-  if (rc == GEMM_TN_OK && ef != cudaSuccess) rc = fail_cuda(ef, "cudaFreeAsync");
-  if (rc == GEMM_TN_OK && es != cudaSuccess) rc = fail_cuda(es, "cudaStreamSynchronize");
+  check(ef, "cudaFreeAsync");
+  check(es, "cudaStreamSynchronize");
   if (rc == GEMM_TN_OK && h_status != 0) rc = fail(h_status, "device watchdog expired");
   return rc;
 }

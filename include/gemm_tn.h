@@ -127,10 +127,13 @@ GEMM_TN_API int gemm_tn_ex_noalloc(int dtype, int64_t m, int64_t n, int64_t k, c
 
 /*
  * gemm_tn_host -- C = A x B^T with contiguous operands in HOST memory
- * (pageable or pinned): copies A and B to the device, runs gemm_tn_ex, copies
- * C back and waits for `stream`. Device buffers come from cudaMallocAsync on
- * `stream` and are released before return. Returns GEMM_TN_ERR_TIMEOUT if the
- * watchdog fired.
+ * (pinned for full copy speed; pageable works): copies A and B to the current
+ * device, computes, copies C back and waits for everything before returning.
+ * B is copied first, then A in chunks of rows; each chunk's GEMM runs on
+ * `stream` while the next chunk of A is copied in and the previous chunk of C
+ * is copied out on two library-owned copy streams. Device staging memory comes
+ * from a library-owned pool that keeps it for later calls. Calls on one device
+ * are serialised. Returns GEMM_TN_ERR_TIMEOUT if the watchdog fired.
  */
 GEMM_TN_API int gemm_tn_host(int dtype, int64_t m, int64_t n, int64_t k, const void* a_host, const void* b_host,
                  void* c_host, gemm_tn_stream_t stream);

@@ -423,3 +423,18 @@ def test_concurrent_calls_from_two_threads_on_two_streams():
         for o in results[i][1:]:
             assert torch.equal(o, results[i][0])
         assert_parity(results[i][0], data[i][0], data[i][1], f"thread {i}")
+
+
+def test_host_entry_point_chunked_with_ragged_pitches():
+    """gemm_tn_host on a problem it splits into several row chunks, with K and
+    N whose host row pitches are not multiples of 16 bytes (the device staging
+    rows are padded by 2-D copies); pinned and pageable buffers."""
+    m, n, k = 5000, 1003, 4097
+    a_cpu, b_cpu = make_operands(m, n, k, "fp16", "normal_over_sqrt_k", seed=77)
+    c_pinned = gt.mm_tn_host(a_cpu.pin_memory(), b_cpu.pin_memory())
+    c_pageable = gt.mm_tn_host(a_cpu, b_cpu)
+    assert torch.equal(c_pinned, c_pageable)
+    rng = np.random.Generator(np.random.PCG64(5))
+    rows = edge_indices(m, 2560, rng, 24)
+    cols = edge_indices(n, 256, rng, 24)
+    assert_sampled_parity(c_pinned, a_cpu, b_cpu, rows, cols, "host path")
