@@ -275,12 +275,21 @@ struct WorkPlan {
 
 constexpr int64_t kMinSkIters = 8;
 
-WorkPlan plan_work(int64_t tiles, int64_t k_blocks, int clusters, bool stream_k) {
+WorkPlan plan_work(int64_t tiles, int64_t k_blocks, int clusters, int stream_k) {
   WorkPlan p{static_cast<int>(std::min<int64_t>(tiles, clusters)), tiles, 0};
-  if (!stream_k) return p;
+  if (stream_k == 0) return p;
   if (tiles >= clusters) {
     const int64_t rem = tiles % clusters;
     if (rem == 0) return p;
+    // mode 2: only the partial wave's tiles are split (each across about
+    // clusters / rem workers), when that leaves at least kMinSkIters k-blocks
+    // per worker
+    if (stream_k == 2 && rem * k_blocks >= clusters * kMinSkIters) {
+      p.workers = clusters;
+      p.dp_tiles = tiles - rem;
+      p.sk_iters = rem * k_blocks;
+      return p;
+    }
     const int64_t sk_tiles = rem + clusters;
     p.workers = clusters;
     p.dp_tiles = tiles - sk_tiles;
@@ -302,9 +311,34 @@ WorkPlan plan_work(int64_t tiles, int64_t k_blocks, int clusters, bool stream_k)
 // than it saves: with all 152 SMs streaming operands at once each reaches
 // ~68% tensor activity, while in the data-parallel schedule the partial last
 // wave runs with fewer SMs at up to ~84% (fp16 4096^3: 88.6 us vs 84.8 us).
-bool stream_k_enabled() {
+// Tail split: when the tiles leave a last, partial wave, cut each of its
+// tiles into `split` sub-tiles along N (2 or 4, keeping N >= 64 per MMA) so
+// that wave has up to `split` times as many, shorter units for the same
+// workers. Returns the split factor (1: none) and the first cut tile.
+// GEMM_TN_TAIL_SPLIT=0 turns it off.
+int tail_split(const ConfigInfo& cfg, int64_t tiles, int clusters, int64_t* split_begin) {
+  *split_begin = tiles;
+  const char* env = std::getenv("GEMM_TN_TAIL_SPLIT");
+  if (env != nullptr && std::strcmp(env, "0") == 0) return 1;
+  const int64_t full = tiles >= clusters ? tiles - tiles % clusters : 0;
+  const int64_t last = tiles - full;
+  if (last == 0) return 1;
+  for (int s : {4, 2}) {
+    if (cfg.block_n / s >= 64 && (cfg.b_rows / s) % 8 == 0 && last * s <= clusters) {
+      *split_begin = full;
+      return s;
+    }
+  }
+  return 1;
+}
+
+// GEMM_TN_STREAMK=2 splits only the partial wave's tiles (experimental).
+int stream_k_mode() {
   const char* s = std::getenv("GEMM_TN_STREAMK");
-  return s != nullptr && std::strcmp(s, "1") == 0;
+  if (s == nullptr) return 0;
+  if (std::strcmp(s, "1") == 0) return 1;
+  if (std::strcmp(s, "2") == 0) return 2;
+  return 0;
 }
 
 // Tile rows per rasterization group: tiles in flight together then share
@@ -351,8 +385,13 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   const int clusters = resident_clusters(dev, cfg_id, bf16);
   if (clusters <= 0) return fail(GEMM_TN_ERR_CUDA, "kernel cannot be resident on this device (occupancy query)");
   // The no-alloc path keeps to whole tiles: its fixed scratch is for repacks.
-  const WorkPlan plan = plan_work(tiles, num_k_blocks, clusters,
-                                  stream_k_enabled() && fixed_scratch == nullptr && cfg.cluster_pairs == 1);
+  WorkPlan plan = plan_work(tiles, num_k_blocks, clusters, fixed_scratch == nullptr ? stream_k_mode() : 0);
+  int64_t split_begin = tiles;
+  const int split = plan.sk_iters > 0 ? 1 : tail_split(cfg, tiles, clusters, &split_begin);
+  if (split > 1) {
+    const int64_t units = split_begin + (tiles - split_begin) * split;
+    plan.workers = static_cast<int>(std::min<int64_t>(units, clusters));
+  }
   const int grid_ctas = plan.workers * cfg.cta_group * cfg.cluster_pairs;
 
   // Workspace: [repacked A][repacked B][stream-K partials][stream-K flags].
@@ -422,6 +461,9 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
                          CU_TENSOR_MAP_SWIZZLE_128B);
   if (st == GEMM_TN_OK)
     st = encode_matrix_map(&args.tmap_b, bf16, b_use, n, k, ldb_use, kBlockK, cfg.b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st == GEMM_TN_OK && split > 1)
+    st = encode_matrix_map(&args.tmap_b_split, bf16, b_use, n, k, ldb_use, kBlockK, cfg.b_rows / split,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
   // C goes out through the TMA when its base and pitch allow; otherwise the
   // epilogue's predicated element stores handle any 2-byte-aligned layout.
   const bool c_tma = tma_compatible(c, ldc) && !force_direct_epilogue();
@@ -450,6 +492,8 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   args.sk_iters = plan.sk_iters;
   args.partials = partials;
   args.flags = flags;
+  args.split = split;
+  args.split_begin = static_cast<int32_t>(split_begin);
 
   e = cfg.cta_group == 2 ? launch_gemm_2cta(cfg_id, bf16, args, grid_ctas, stream)
                          : launch_gemm_1cta(cfg_id, bf16, args, grid_ctas, stream);

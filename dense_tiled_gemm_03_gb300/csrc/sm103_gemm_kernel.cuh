@@ -54,6 +54,7 @@ struct GemmArgs {
   CUtensorMap tmap_a;     // A: dims {K, M}, box {64, 128}, 128B swizzle
   CUtensorMap tmap_b;     // B: dims {K, N}, box {64, BN / cta_group}, 128B swizzle
   CUtensorMap tmap_c;     // C: dims {N, M}, box {32, 32}, 64B swizzle (valid when c_tma_store)
+  CUtensorMap tmap_b_split;  // B with box rows BN / cta_group / split (valid when split > 1)
   void* c;                // C [M, N], row stride ldc elements
   int64_t ldc;
   int32_t c_tma_store;    // 1: epilogue stores through the TMA; 0: predicated element stores
@@ -71,6 +72,11 @@ struct GemmArgs {
   int32_t dp_tiles;
   int32_t num_workers;
   int64_t sk_iters;
+  // Tail split: tiles [split_begin, num_tiles) -- the last, partial wave --
+  // are each cut into `split` sub-tiles of block_n / split columns, so that
+  // wave holds more, shorter units of work (split 1: no cut).
+  int32_t split;
+  int32_t split_begin;
   float* partials;        // per CTA: block_n / 32 chunks x 128 rows x 32 fp32 (stream-K only)
   int* flags;             // per CTA and epilogue warp: 1 once its partial rows are written (zeroed by the host)
 };
@@ -150,6 +156,8 @@ struct WorkItem {
   int tile;        // tile index in raster order
   int kb_begin;    // first k-block of this item
   int kb_end;      // one past the last k-block
+  int sub;         // sub-tile index along N within a cut tile (0 when whole)
+  int nsub;        // number of sub-tiles the tile is cut into (1 when whole)
 };
 
 // First stream-K iteration of `worker`'s range.
@@ -191,11 +199,24 @@ struct WorkCursor {
       w.tile = a.dp_tiles + static_cast<int>(t);
       w.kb_begin = kb0;
       w.kb_end = kb1;
+      w.sub = 0;
+      w.nsub = 1;
       sk_cur += kb1 - kb0;
       return true;
     }
-    if (dp_next < a.dp_tiles) {
-      w.tile = static_cast<int>(dp_next);
+    // whole tiles, then the sub-tiles of the cut tail tiles, round-robin
+    const int64_t units = a.split_begin + static_cast<int64_t>(a.dp_tiles - a.split_begin) * a.split;
+    if (dp_next < units) {
+      if (dp_next < a.split_begin) {
+        w.tile = static_cast<int>(dp_next);
+        w.sub = 0;
+        w.nsub = 1;
+      } else {
+        const int64_t u = dp_next - a.split_begin;
+        w.tile = a.split_begin + static_cast<int>(u / a.split);
+        w.sub = static_cast<int>(u % a.split);
+        w.nsub = a.split;
+      }
       w.kb_begin = 0;
       w.kb_end = a.num_k_blocks;
       dp_next += a.num_workers;
@@ -361,7 +382,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         tile_coords(item.tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tj);
         const int tn = tj * Cfg::kClusterPairs + static_cast<int>(pair);
         const int a_row = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM;
-        const int b_row = tn * Cfg::kBlockN + static_cast<int>(cta_rank) * Cfg::kBRows;
+        const int sub_n = Cfg::kBlockN / item.nsub;   // columns of this unit of work
+        const int b_row = tn * Cfg::kBlockN + item.sub * sub_n + static_cast<int>(cta_rank) * (Cfg::kBRows / item.nsub);
+        const void* tmap_b = item.nsub > 1 ? static_cast<const void*>(&args.tmap_b_split)
+                                           : static_cast<const void*>(&args.tmap_b);
+        const uint32_t b_bytes = Cfg::kBTileBytes / static_cast<uint32_t>(item.nsub);
         for (int kb = item.kb_begin; kb < item.kb_end; ++kb) {
           if (!wd.wait(empty_bar(stage), phase ^ 1u)) {
             ok = false;
@@ -375,13 +400,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             // destination pair's leader counts the bytes, so the leader
             // expects both halves for both of its CTAs plus both B tiles,
             // the same total as without multicast.
-            if (leader) mbar_arrive_expect_tx(fb, Cfg::kCtaGroup * Cfg::kStageBytes);
+            if (leader) mbar_arrive_expect_tx(fb, Cfg::kCtaGroup * (Cfg::kATileBytes + b_bytes));
             if (!drop) {
               const int x = kb * Cfg::kBlockK;
               const uint16_t mask = static_cast<uint16_t>((1u << cta_rank) | (1u << (2u + cta_rank)));
               tma_load_2d_multicast_pair(&args.tmap_a, a_tile(stage) + pair * Cfg::kAHalfBytes, fb & 0xFEFFFFFFu, x,
                                          a_row + static_cast<int>(pair) * (Cfg::kBlockM / 2), mask);
-              tma_load_2d_pair(&args.tmap_b, b_tile(stage), map_to_cta(fb, pair_leader), x, b_row);
+              tma_load_2d_pair(tmap_b, b_tile(stage), map_to_cta(fb, pair_leader), x, b_row);
             }
             issued_phase_of[stage] = static_cast<int>(phase);
             if (++stage == Cfg::kStages) {
@@ -390,16 +415,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             }
             continue;
           }
-          if (leader) mbar_arrive_expect_tx(fb, Cfg::kCtaGroup * Cfg::kStageBytes);
+          if (leader) mbar_arrive_expect_tx(fb, Cfg::kCtaGroup * (Cfg::kATileBytes + b_bytes));
           if (!drop) {
             const int x = kb * Cfg::kBlockK;
             if constexpr (Cfg::kCtaGroup == 2) {
               const uint32_t fb_leader = map_to_cta(fb, pair_leader);
               tma_load_2d_pair(&args.tmap_a, a_tile(stage), fb_leader, x, a_row);
-              tma_load_2d_pair(&args.tmap_b, b_tile(stage), fb_leader, x, b_row);
+              tma_load_2d_pair(tmap_b, b_tile(stage), fb_leader, x, b_row);
             } else {
               tma_load_2d(&args.tmap_a, a_tile(stage), fb, x, a_row);
-              tma_load_2d(&args.tmap_b, b_tile(stage), fb, x, b_row);
+              tma_load_2d(tmap_b, b_tile(stage), fb, x, b_row);
             }
           }
           issued_phase_of[stage] = static_cast<int>(phase);
@@ -436,6 +461,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
+        // a sub-tile of a cut tile multiplies with N = block_n / nsub
+        const uint32_t idesc = item.nsub == 1 ? Cfg::kIdesc
+                                              : mma_idesc_f16(Cfg::kBf16, Cfg::kTileM, Cfg::kBlockN / item.nsub);
         for (int kb = item.kb_begin; kb < item.kb_end; ++kb) {
           if (!wd.wait(full_bar(stage), phase)) {
             ok = false;
@@ -447,7 +475,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
 #pragma unroll
           for (int kk = 0; kk < Cfg::kBlockK / Cfg::kMmaK; ++kk) {
             // advancing 16 elements along K = 32 bytes = 2 descriptor units
-            mma_f16<Cfg::kCtaGroup>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, Cfg::kIdesc,
+            mma_f16<Cfg::kCtaGroup>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc,
                                     (kb > item.kb_begin || kk > 0) ? 1u : 0u);
           }
           if constexpr (Cfg::kMulticastA) {
@@ -508,11 +536,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       if (!wd.wait(acc_full_bar(acc), acc_phase)) break;
       tc_fence_after_sync();
       const int row0 = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM + static_cast<int>(quarter) * 32;
-      const int col_tile = tn * Cfg::kBlockN;
+      const int col_tile = tn * Cfg::kBlockN + item.sub * (Cfg::kBlockN / item.nsub);
       const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + static_cast<uint32_t>(acc * Cfg::kAccCols);
       // 32-column chunks of this tile that lie inside N (warp-uniform; 0 when
       // a multicast cluster's second pair lies wholly past N)
-      const int chunks = max(0, min(kChunks, (args.n - col_tile + 31) / 32));
+      const int chunks = max(0, min(kChunks / item.nsub, (args.n - col_tile + 31) / 32));
       if (chunks == 0) {
         tc_fence_before_sync();
         __syncwarp();

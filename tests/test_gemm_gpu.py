@@ -341,7 +341,7 @@ def test_stream_k_cut_tiles(mnk, config):
     from _parity import env_var
     m, n, k = mnk
     a, b = make_operands(m, n, k, "bf16", "normal_over_sqrt_k", seed=m ^ n ^ k)
-    for sk in ("1", "0"):
+    for sk in ("1", "2", "0"):
         with env_var("GEMM_TN_STREAMK", sk):
             c, status = gpu_gemm(a, b, config)
         assert status == 0
@@ -438,3 +438,19 @@ def test_host_entry_point_chunked_with_ragged_pitches():
     rows = edge_indices(m, 2560, rng, 24)
     cols = edge_indices(n, 256, rng, 24)
     assert_sampled_parity(c_pinned, a_cpu, b_cpu, rows, cols, "host path")
+
+
+@pytest.mark.parametrize("config", CONFIGS)
+@pytest.mark.parametrize("mnk", [(1000, 1000, 640), (2304, 4352, 1000), (3001, 5003, 577), (4096, 4096, 512),
+                                 (300, 2000, 700)], ids=lambda s: "x".join(map(str, s)))
+def test_tail_split_sub_tiles(mnk, config):
+    """The last, partial wave of tiles is cut into 2 or 4 sub-tiles along N
+    (runtime MMA N, narrower B boxes); parity with the cut on and off."""
+    from _parity import env_var
+    m, n, k = mnk
+    a, b = make_operands(m, n, k, "bf16", "uniform", seed=m + 3 * n + 7 * k)
+    for on in (None, "0"):
+        with env_var("GEMM_TN_TAIL_SPLIT", on):
+            c, status = gpu_gemm(a, b, config)
+        assert status == 0
+        assert_parity(c, a, b, f"{mnk} {config} tail_split={'off' if on else 'on'}")
