@@ -18,6 +18,7 @@ from ._native import (  # noqa: F401
     GEMM_TN_OK,
     LIBRARY_PATH,
     GemmTnError,
+    gemm_nn,
     gemm_tn,
     gemm_tn_config_name,
     gemm_tn_ex,
@@ -31,6 +32,7 @@ from ._native import (  # noqa: F401
     gemm_tn_status_string,
     gemm_tn_version,
     library,
+    mm_nn,
     mm_tn,
     mm_tn_host,
 )

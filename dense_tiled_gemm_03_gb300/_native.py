@@ -37,6 +37,7 @@ _ptr = ctypes.c_void_p
 _SIGNATURES = {
     "gemm_tn": (_int, [_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr]),
     "gemm_tn_ex": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]),
+    "gemm_nn": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]),
     "gemm_tn_ex_noalloc": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]),
     "gemm_tn_host": (_int, [_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr]),
     "gemm_tn_select_config": (_int, [_int, _i64, _i64, _i64]),
@@ -85,6 +86,11 @@ def gemm_tn(dtype, m, n, k, a, b, c, stream=None) -> int:
 
 def gemm_tn_ex(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status=None, stream=None) -> int:
     return library().gemm_tn_ex(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, stream)
+
+
+def gemm_nn(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status=None, stream=None) -> int:
+    """C = A x B with B stored [K, N] (N contiguous)."""
+    return library().gemm_nn(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, stream)
 
 
 def gemm_tn_ex_noalloc(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status=None, stream=None) -> int:
@@ -172,6 +178,33 @@ def mm_tn(a, b, out=None, status=None):
                         d_status, stream)
     if rc != GEMM_TN_OK:
         raise GemmTnError(rc, "gemm_tn_ex")
+    return out
+
+
+def mm_nn(a, b, out=None, status=None):
+    """C = A x B on the GPU through gemm_nn. a: [M, K], b: [K, N] CUDA tensors
+    of the same fp16/bf16 dtype with unit stride along their last dimension."""
+    import torch
+    if a.device.type != "cuda" or b.device != a.device:
+        raise ValueError("a and b must be CUDA tensors on one device")
+    if a.dtype != b.dtype:
+        raise TypeError("a and b must have the same dtype")
+    m, k = a.shape
+    kb, n = b.shape
+    if kb != k:
+        raise ValueError(f"inner dimensions differ: {tuple(a.shape)} x {tuple(b.shape)}")
+    if out is None:
+        out = torch.empty((m, n), dtype=a.dtype, device=a.device)
+    elif out.shape != (m, n) or out.dtype != a.dtype or out.device != a.device:
+        raise ValueError("out must be [M, N] with the dtype and device of a")
+    lda, ldb, ldc = _row_pitch(a, k), _row_pitch(b, n), _row_pitch(out, n)
+    stream = torch.cuda.current_stream(a.device).cuda_stream
+    d_status = status.data_ptr() if status is not None else None
+    with torch.cuda.device(a.device):
+        rc = gemm_nn(_dtype_code(a), m, n, k, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(), ldc,
+                     d_status, stream)
+    if rc != GEMM_TN_OK:
+        raise GemmTnError(rc, "gemm_nn")
     return out
 
 

@@ -32,6 +32,7 @@ int smem_bytes_1cta(int id);
 cudaError_t launch_gemm_2cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
 int max_resident_2cta(int id, bool bf16);
 int smem_bytes_2cta(int id);
+cudaError_t launch_gemm_nn(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
 
 namespace {
 
@@ -161,8 +162,9 @@ uintptr_t span_bytes(int64_t rows, int64_t cols, int64_t ld) {
   return static_cast<uintptr_t>(((rows - 1) * ld + cols) * 2);
 }
 
+// b_mn: B is [K, N] (N contiguous, ldb >= n) instead of [N, K].
 int validate(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
-             const void* c, int64_t ldc) {
+             const void* c, int64_t ldc, bool b_mn = false) {
   if (dtype != GEMM_TN_F16 && dtype != GEMM_TN_BF16) return fail(GEMM_TN_ERR_UNSUPPORTED_DTYPE, "dtype");
   if (m < 0 || n < 0 || k < 0 || m > kMaxDim || n > kMaxDim || k > kMaxDim)
     return fail(GEMM_TN_ERR_INVALID_VALUE, "sizes must be in [0, 2^31)");
@@ -172,13 +174,13 @@ int validate(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   if (reinterpret_cast<uintptr_t>(c) % 2) return fail(GEMM_TN_ERR_MISALIGNED, "C is not 2-byte aligned");
   if (k == 0) return GEMM_TN_OK;
   if (a == nullptr || b == nullptr) return fail(GEMM_TN_ERR_INVALID_VALUE, "A or B is NULL");
-  if (lda < k || ldb < k || lda > kMaxDim * 2 || ldb > kMaxDim * 2)
-    return fail(GEMM_TN_ERR_INVALID_VALUE, "lda or ldb < k");
+  if (lda < k || ldb < (b_mn ? n : k) || lda > kMaxDim * 2 || ldb > kMaxDim * 2)
+    return fail(GEMM_TN_ERR_INVALID_VALUE, b_mn ? "lda < k or ldb < n" : "lda or ldb < k");
   if (reinterpret_cast<uintptr_t>(a) % 2 || reinterpret_cast<uintptr_t>(b) % 2)
     return fail(GEMM_TN_ERR_MISALIGNED, "A or B is not 2-byte aligned");
   const uintptr_t c0 = reinterpret_cast<uintptr_t>(c), c1 = c0 + span_bytes(m, n, ldc);
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), a1 = a0 + span_bytes(m, k, lda);
-  const uintptr_t b0 = reinterpret_cast<uintptr_t>(b), b1 = b0 + span_bytes(n, k, ldb);
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(b), b1 = b0 + (b_mn ? span_bytes(k, n, ldb) : span_bytes(n, k, ldb));
   if (ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1))
     return fail(GEMM_TN_ERR_INVALID_VALUE, "C overlaps A or B");
   return GEMM_TN_OK;
@@ -316,7 +318,7 @@ WorkPlan plan_work(int64_t tiles, int64_t k_blocks, int clusters, int stream_k) 
 // that wave has up to `split` times as many, shorter units for the same
 // workers. Returns the split factor (1: none) and the first cut tile.
 // GEMM_TN_TAIL_SPLIT=0 turns it off.
-int tail_split(const ConfigInfo& cfg, int64_t tiles, int clusters, int64_t* split_begin) {
+int tail_split(const ConfigInfo& cfg, int64_t tiles, int clusters, int64_t* split_begin, bool b_mn) {
   *split_begin = tiles;
   const char* env = std::getenv("GEMM_TN_TAIL_SPLIT");
   if (env != nullptr && std::strcmp(env, "0") == 0) return 1;
@@ -324,7 +326,7 @@ int tail_split(const ConfigInfo& cfg, int64_t tiles, int clusters, int64_t* spli
   const int64_t last = tiles - full;
   if (last == 0) return 1;
   for (int s : {4, 2}) {
-    if (cfg.block_n / s >= 64 && (cfg.b_rows / s) % 8 == 0 && last * s <= clusters) {
+    if (cfg.block_n / s >= 64 && (cfg.b_rows / s) % (b_mn ? 64 : 8) == 0 && last * s <= clusters) {
       *split_begin = full;
       return s;
     }
@@ -355,10 +357,10 @@ int group_rows(const ConfigInfo& cfg) {
 
 int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
              void* c, int64_t ldc, int* d_status, cudaStream_t stream, int drop_load_kb,
-             void* fixed_scratch = nullptr, size_t fixed_scratch_bytes = 0) {
+             void* fixed_scratch = nullptr, size_t fixed_scratch_bytes = 0, bool b_mn = false) {
   t_last_cuda_error = 0;
   t_last_message[0] = '\0';
-  int st = validate(dtype, m, n, k, a, lda, b, ldb, c, ldc);
+  int st = validate(dtype, m, n, k, a, lda, b, ldb, c, ldc, b_mn);
   if (st != GEMM_TN_OK) return st;
   if (m == 0 || n == 0) return GEMM_TN_OK;
   DeviceFacts* dev = nullptr;
@@ -387,7 +389,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   // The no-alloc path keeps to whole tiles: its fixed scratch is for repacks.
   WorkPlan plan = plan_work(tiles, num_k_blocks, clusters, fixed_scratch == nullptr ? stream_k_mode() : 0);
   int64_t split_begin = tiles;
-  const int split = plan.sk_iters > 0 ? 1 : tail_split(cfg, tiles, clusters, &split_begin);
+  const int split = plan.sk_iters > 0 ? 1 : tail_split(cfg, tiles, clusters, &split_begin, b_mn);
   if (split > 1) {
     const int64_t units = split_begin + (tiles - split_begin) * split;
     plan.workers = static_cast<int>(std::min<int64_t>(units, clusters));
@@ -399,8 +401,11 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   const bool repack_a = !tma_compatible(a, lda);
   const bool repack_b = !tma_compatible(b, ldb);
   const int64_t ld_pad = round_up(k, 8);
+  // B rows: N rows of K elements, or (b_mn) K rows of N elements
+  const int64_t b_rows_mem = b_mn ? k : n, b_cols_mem = b_mn ? n : k;
+  const int64_t ldb_pad = round_up(b_cols_mem, 8);
   const size_t a_bytes = repack_a ? static_cast<size_t>(round_up(m * ld_pad * 2, 256)) : 0;
-  const size_t b_bytes = repack_b ? static_cast<size_t>(round_up(n * ld_pad * 2, 256)) : 0;
+  const size_t b_bytes = repack_b ? static_cast<size_t>(round_up(b_rows_mem * ldb_pad * 2, 256)) : 0;
   const size_t partial_bytes =
       plan.sk_iters > 0 ? static_cast<size_t>(grid_ctas) * 128 * static_cast<size_t>(cfg.block_n) * 4 : 0;
   const size_t flag_bytes = plan.sk_iters > 0 ? static_cast<size_t>(grid_ctas) * 4 * sizeof(int) : 0;
@@ -430,7 +435,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   int64_t lda_use = lda, ldb_use = ldb;
   if (repack_a || repack_b) {
     RepackRequest req[2] = {{a, lda, ws, ld_pad, repack_a ? m : 0, k},
-                            {b, ldb, ws + a_bytes, ld_pad, repack_b ? n : 0, k}};
+                            {b, ldb, ws + a_bytes, ldb_pad, repack_b ? b_rows_mem : 0, b_cols_mem}};
     e = launch_repack2(req, 2, dev->num_sms, stream);
     if (repack_a) {
       a_use = ws;
@@ -438,7 +443,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
     }
     if (repack_b) {
       b_use = ws + a_bytes;
-      ldb_use = ld_pad;
+      ldb_use = ldb_pad;
     }
   }
   if (e != cudaSuccess) {
@@ -459,9 +464,11 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   std::memset(&args, 0, sizeof(args));
   st = encode_matrix_map(&args.tmap_a, bf16, a_use, m, k, lda_use, kBlockK, cfg.a_box_rows,
                          CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st == GEMM_TN_OK)
+  if (st == GEMM_TN_OK && b_mn)   // [K, N]: 64 N x 64 K boxes
+    st = encode_matrix_map(&args.tmap_b, bf16, b_use, k, n, ldb_use, 64, kBlockK, CU_TENSOR_MAP_SWIZZLE_128B);
+  else if (st == GEMM_TN_OK)
     st = encode_matrix_map(&args.tmap_b, bf16, b_use, n, k, ldb_use, kBlockK, cfg.b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st == GEMM_TN_OK && split > 1)
+  if (st == GEMM_TN_OK && split > 1 && !b_mn)
     st = encode_matrix_map(&args.tmap_b_split, bf16, b_use, n, k, ldb_use, kBlockK, cfg.b_rows / split,
                            CU_TENSOR_MAP_SWIZZLE_128B);
   // C goes out through the TMA when its base and pitch allow; otherwise the
@@ -495,8 +502,11 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   args.split = split;
   args.split_begin = static_cast<int32_t>(split_begin);
 
-  e = cfg.cta_group == 2 ? launch_gemm_2cta(cfg_id, bf16, args, grid_ctas, stream)
-                         : launch_gemm_1cta(cfg_id, bf16, args, grid_ctas, stream);
+  if (b_mn)
+    e = launch_gemm_nn(cfg_id, bf16, args, grid_ctas, stream);
+  else
+    e = cfg.cta_group == 2 ? launch_gemm_2cta(cfg_id, bf16, args, grid_ctas, stream)
+                           : launch_gemm_1cta(cfg_id, bf16, args, grid_ctas, stream);
   if (owned_workspace) {
     cudaError_t e2 = cudaFreeAsync(owned_workspace, stream);
     if (e == cudaSuccess) e = e2;
@@ -612,6 +622,12 @@ int gemm_tn_ex(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_
                void* c, int64_t ldc, int* d_status, gemm_tn_stream_t stream) {
   return run_gemm(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, reinterpret_cast<cudaStream_t>(stream),
                   test_drop_load_kb());
+}
+
+int gemm_nn(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
+            void* c, int64_t ldc, int* d_status, gemm_tn_stream_t stream) {
+  return run_gemm(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, reinterpret_cast<cudaStream_t>(stream),
+                  test_drop_load_kb(), nullptr, 0, /*b_mn=*/true);
 }
 
 int gemm_tn_ex_noalloc(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b,

@@ -81,9 +81,13 @@ struct GemmArgs {
   int* flags;             // per CTA and epilogue warp: 1 once its partial rows are written (zeroed by the host)
 };
 
-template <int kCtaGroup_, int kBlockN_, int kStages_, bool kBf16_, int kClusterPairs_ = 1>
+template <int kCtaGroup_, int kBlockN_, int kStages_, bool kBf16_, int kClusterPairs_ = 1, bool kBMnMajor_ = false>
 struct GemmConfig {
   static constexpr int kCtaGroup = kCtaGroup_;
+  // kBMnMajor: B is stored [K, N] with N contiguous (C = A x B), loaded in
+  // 64 x 64 boxes and read by the MMA through MN-major descriptors.
+  static constexpr bool kBMnMajor = kBMnMajor_;
+  static constexpr uint32_t kBMnBoxBytes = 64 * 64 * 2;
   // kClusterPairs == 2: a cluster of two CTA pairs side by side along N that
   // share their rows of A. Each CTA loads one 64-row half of its A block and
   // TMA-multicasts it to the CTA at the same position in the other pair.
@@ -124,12 +128,13 @@ struct GemmConfig {
   static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
   static constexpr uint32_t kSmemUsed = kOffAbort + 4;
   static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;      // slack for aligning the base
-  static constexpr uint32_t kIdesc = mma_idesc_f16(kBf16, kTileM, kBlockN);
+  static constexpr uint32_t kIdesc = mma_idesc_f16(kBf16, kTileM, kBlockN, kBMnMajor);
 
   static_assert(kBlockN % 32 == 0 && kBlockN >= 32 && kBlockN <= 256, "MMA N");
   static_assert(kCtaGroup == 1 || kCtaGroup == 2, "cta group");
   static_assert(kClusterPairs == 1 || (kClusterPairs == 2 && kCtaGroup == 2), "A multicast pairs CTA pairs");
   static_assert(kBRows % 8 == 0 && kBRows <= 256, "TMA box rows");
+  static_assert(!kBMnMajor || kBRows % 64 == 0, "MN-major B is loaded in 64-wide boxes");
   static_assert(kATileBytes % 1024 == 0 && kBTileBytes % 1024 == 0, "swizzle atoms stay 1024-aligned");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns");
   static_assert(kOffBar >= kOffEpi + kEpiBytes, "barriers after every buffer");
@@ -384,9 +389,29 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         const int a_row = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM;
         const int sub_n = Cfg::kBlockN / item.nsub;   // columns of this unit of work
         const int b_row = tn * Cfg::kBlockN + item.sub * sub_n + static_cast<int>(cta_rank) * (Cfg::kBRows / item.nsub);
-        const void* tmap_b = item.nsub > 1 ? static_cast<const void*>(&args.tmap_b_split)
-                                           : static_cast<const void*>(&args.tmap_b);
+        const void* tmap_b = item.nsub > 1 && !Cfg::kBMnMajor ? static_cast<const void*>(&args.tmap_b_split)
+                                                              : static_cast<const void*>(&args.tmap_b);
         const uint32_t b_bytes = Cfg::kBTileBytes / static_cast<uint32_t>(item.nsub);
+        // B of one k-block into this CTA's stage buffer, completing on `bar`
+        // (the pair leader's barrier for CTA pairs): one box [rows x 64 K]
+        // when K-major, or 64-wide N boxes of [64 K x 64 N] when MN-major.
+        auto load_b = [&](int stage_, uint32_t bar, int kb_) {
+          if constexpr (Cfg::kBMnMajor) {
+            const int boxes = Cfg::kBRows / item.nsub / 64;
+            for (int j = 0; j < boxes; ++j) {
+              if constexpr (Cfg::kCtaGroup == 2) {
+                tma_load_2d_pair(tmap_b, b_tile(stage_) + j * Cfg::kBMnBoxBytes, bar, b_row + 64 * j,
+                                 kb_ * Cfg::kBlockK);
+              } else {
+                tma_load_2d(tmap_b, b_tile(stage_) + j * Cfg::kBMnBoxBytes, bar, b_row + 64 * j, kb_ * Cfg::kBlockK);
+              }
+            }
+          } else if constexpr (Cfg::kCtaGroup == 2) {
+            tma_load_2d_pair(tmap_b, b_tile(stage_), bar, kb_ * Cfg::kBlockK, b_row);
+          } else {
+            tma_load_2d(tmap_b, b_tile(stage_), bar, kb_ * Cfg::kBlockK, b_row);
+          }
+        };
         for (int kb = item.kb_begin; kb < item.kb_end; ++kb) {
           if (!wd.wait(empty_bar(stage), phase ^ 1u)) {
             ok = false;
@@ -406,7 +431,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
               const uint16_t mask = static_cast<uint16_t>((1u << cta_rank) | (1u << (2u + cta_rank)));
               tma_load_2d_multicast_pair(&args.tmap_a, a_tile(stage) + pair * Cfg::kAHalfBytes, fb & 0xFEFFFFFFu, x,
                                          a_row + static_cast<int>(pair) * (Cfg::kBlockM / 2), mask);
-              tma_load_2d_pair(tmap_b, b_tile(stage), map_to_cta(fb, pair_leader), x, b_row);
+              load_b(stage, map_to_cta(fb, pair_leader), kb);
             }
             issued_phase_of[stage] = static_cast<int>(phase);
             if (++stage == Cfg::kStages) {
@@ -421,10 +446,10 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             if constexpr (Cfg::kCtaGroup == 2) {
               const uint32_t fb_leader = map_to_cta(fb, pair_leader);
               tma_load_2d_pair(&args.tmap_a, a_tile(stage), fb_leader, x, a_row);
-              tma_load_2d_pair(tmap_b, b_tile(stage), fb_leader, x, b_row);
+              load_b(stage, fb_leader, kb);
             } else {
               tma_load_2d(&args.tmap_a, a_tile(stage), fb, x, a_row);
-              tma_load_2d(tmap_b, b_tile(stage), fb, x, b_row);
+              load_b(stage, fb, kb);
             }
           }
           issued_phase_of[stage] = static_cast<int>(phase);
@@ -462,8 +487,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
         // a sub-tile of a cut tile multiplies with N = block_n / nsub
-        const uint32_t idesc = item.nsub == 1 ? Cfg::kIdesc
-                                              : mma_idesc_f16(Cfg::kBf16, Cfg::kTileM, Cfg::kBlockN / item.nsub);
+        const uint32_t idesc =
+            item.nsub == 1 ? Cfg::kIdesc
+                           : mma_idesc_f16(Cfg::kBf16, Cfg::kTileM, Cfg::kBlockN / item.nsub, Cfg::kBMnMajor);
         for (int kb = item.kb_begin; kb < item.kb_end; ++kb) {
           if (!wd.wait(full_bar(stage), phase)) {
             ok = false;
@@ -471,11 +497,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
           }
           tc_fence_after_sync();
           const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage));
-          const uint64_t b_desc = sw128_kmajor_desc(b_tile(stage));
+          const uint64_t b_desc = Cfg::kBMnMajor ? sw128_mnmajor_desc(b_tile(stage), Cfg::kBMnBoxBytes)
+                                                 : sw128_kmajor_desc(b_tile(stage));
+          // one K=16 step: 32 bytes along a K-major row, or two 1024-byte
+          // 8-row K groups of an MN-major tile
+          constexpr uint32_t kBStep = Cfg::kBMnMajor ? (2048u >> 4) : 2u;
 #pragma unroll
           for (int kk = 0; kk < Cfg::kBlockK / Cfg::kMmaK; ++kk) {
             // advancing 16 elements along K = 32 bytes = 2 descriptor units
-            mma_f16<Cfg::kCtaGroup>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc,
+            mma_f16<Cfg::kCtaGroup>(d_tmem, a_desc + 2u * kk, b_desc + kBStep * kk, idesc,
                                     (kb > item.kb_begin || kk > 0) ? 1u : 0u);
           }
           if constexpr (Cfg::kMulticastA) {

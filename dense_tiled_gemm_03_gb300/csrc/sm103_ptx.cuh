@@ -291,16 +291,32 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_tile_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile (the
+// contiguous dimension is M or N) stored as TMA boxes of 64 MN-elements x 64
+// K-rows with the 128-byte swizzle: each K-row is one 128-byte swizzle row,
+// 8-row K groups are 1024 bytes apart (stride-dimension offset) and
+// consecutive 64-element MN blocks are `mn_block_bytes` apart
+// (leading-dimension offset).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_tile_addr, uint32_t mn_block_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_tile_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(mn_block_bytes >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16, dense, fp32 accumulator,
-// both operands K-major.
+// A K-major, B K-major or (b_mn_major) MN-major.
 //   bits  4-5  D format (1: fp32)
 //   bits  7-9  A format (0: fp16, 1: bf16)
 //   bits 10-12 B format (same)
 //   bit  15/16 A/B major (0: K-major)
 //   bits 17-22 N >> 3
 //   bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t mma_idesc_f16(bool bf16, int mma_m, int mma_n) {
-  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+__host__ __device__ constexpr uint32_t mma_idesc_f16(bool bf16, int mma_m, int mma_n, bool b_mn_major = false) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(mma_n >> 3) << 17) | (static_cast<uint32_t>(mma_m >> 4) << 24);
 }
 

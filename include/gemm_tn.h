@@ -95,6 +95,18 @@ GEMM_TN_API int gemm_tn_ex(int dtype, int64_t m, int64_t n, int64_t k, const voi
                int64_t ldb, void* c, int64_t ldc, int* d_status, gemm_tn_stream_t stream);
 
 /*
+ * gemm_nn -- C = A x B with B stored [K, N], N contiguous (rows ldb >= n
+ * elements apart): C[i][j] = sum_k A[i][k] * B[k][j]. A and C as in
+ * gemm_tn_ex. The kernel reads B in that layout directly (MN-major operand
+ * descriptors), with no transpose pass; the GEMM the TileLang page writes
+ * ("TileLang: a tile language one level below Triton", section "The first
+ * kernel: GEMM", B declared (K, N)). Arguments, errors, watchdog and
+ * workspace behaviour are those of gemm_tn_ex.
+ */
+GEMM_TN_API int gemm_nn(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b,
+                        int64_t ldb, void* c, int64_t ldc, int* d_status, gemm_tn_stream_t stream);
+
+/*
  * gemm_tn_ex_noalloc -- gemm_tn_ex for callers that cannot allocate device
  * memory: the pages this library follows have no counterpart of it.
  *

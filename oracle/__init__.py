@@ -28,7 +28,7 @@ import numpy as np
 
 from . import build as _build
 
-__all__ = ["gemm_tn_reference", "parity_report", "ParityReport", "ALLOW_REL", "ALLOW_ABS",
+__all__ = ["gemm_tn_reference", "gemm_nn_reference", "parity_report", "ParityReport", "ALLOW_REL", "ALLOW_ABS",
            "host_threads", "load_library"]
 
 #: The pass criterion's two constants: |c - ref| <= ALLOW_REL * bound + ALLOW_ABS.
@@ -101,6 +101,15 @@ def gemm_tn_reference(a, b, nthreads: int | None = None, lib: ctypes.CDLL | None
         if rc != 0:
             raise RuntimeError(f"oracle_gemm_tn_f64 failed with {rc}")
     return ref, bound
+
+
+def gemm_nn_reference(a, b, nthreads: int | None = None):
+    """ref, bound for C = A x B with B stored [K, N]: C[i][j] = sum_k a[i, k] *
+    b[k, j]. The same plain product as gemm_tn_reference with B's rows and
+    columns exchanged ("TileLang: a tile language one level below Triton",
+    section "The first kernel: GEMM": B declared (K, N))."""
+    B = _as_f64(b)
+    return gemm_tn_reference(a, np.ascontiguousarray(B.T), nthreads=nthreads)
 
 
 @dataclass

@@ -454,3 +454,67 @@ def test_tail_split_sub_tiles(mnk, config):
             c, status = gpu_gemm(a, b, config)
         assert status == 0
         assert_parity(c, a, b, f"{mnk} {config} tail_split={'off' if on else 'on'}")
+
+
+
+# ------------------------------------------------------------ B stored [K, N] (gemm_nn)
+
+def _nn_parity(m, n, k, dtype, config, seed, ldb_pad=0, epilogue="auto"):
+    import oracle
+    from _parity import env_var
+    dev = torch.device("cuda", 0)
+    a_cpu, bt_cpu = make_operands(m, n, k, dtype, "uniform", seed=seed)   # bt: [N, K]
+    b_cpu = bt_cpu.T.contiguous()                                          # [K, N]
+    b_big = torch.zeros((k, n + ldb_pad), dtype=b_cpu.dtype)
+    b_big[:, :n] = b_cpu
+    b = b_big.to(dev)[:, :n]
+    c = torch.full((m, n), float("nan"), dtype=a_cpu.dtype, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    with forced_config(config), epilogue_mode(epilogue):
+        gt.mm_nn(a_cpu.to(dev), b, out=c, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref, bound = oracle.gemm_nn_reference(a_cpu, b_cpu)
+    rep = oracle.parity_report(c.cpu(), ref, bound)
+    assert rep.ok, f"nn {m}x{n}x{k} {dtype} {config}: {rep}"
+
+
+@pytest.mark.parametrize("config", CONFIGS)
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("mnk", [(1, 1, 1), (7, 13, 17), (128, 256, 64), (129, 257, 65), (300, 200, 1000),
+                                 (513, 640, 200), (1000, 1000, 64), (2304, 4352, 1000)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_nn_parity(mnk, dtype, config):
+    _nn_parity(*mnk, dtype, config, seed=sum(mnk))
+
+
+@pytest.mark.parametrize("ldb_pad", [3, 8])
+def test_nn_padded_and_misaligned_b(ldb_pad):
+    _nn_parity(300, 333, 200, "fp16", None, seed=ldb_pad, ldb_pad=ldb_pad)
+
+
+@pytest.mark.parametrize("config", CONFIGS)
+def test_nn_small_integers_are_exact(config):
+    m, n, k = 300, 400, 64
+    a, bt = make_operands(m, n, k, "bf16", "int_small", seed=78)
+    b = bt.T.contiguous()
+    dev = torch.device("cuda", 0)
+    with forced_config(config):
+        c = gt.mm_nn(a.to(dev), b.to(dev))
+    torch.cuda.synchronize()
+    assert torch.equal(c.cpu().double(), (a.long() @ b.long()).double())
+
+
+def test_nn_headline_shape_sampled():
+    """bf16 8192^3 with B stored [K, N]: every column of sampled rows and
+    every row of sampled columns."""
+    import oracle
+    w = WORKLOADS["bf16_8192x8192x8192"]
+    a_cpu, bt_cpu = workload_operands(w)
+    b_cpu = bt_cpu.T.contiguous()
+    dev = torch.device("cuda", 0)
+    c = gt.mm_nn(a_cpu.to(dev), b_cpu.to(dev)).cpu()
+    rng = np.random.Generator(np.random.PCG64(8))
+    rows = edge_indices(w.m, 256, rng, 8)
+    cols = edge_indices(w.n, 256, rng, 8)
+    assert_sampled_parity(c, a_cpu, bt_cpu, rows, cols, "nn headline")

@@ -196,3 +196,18 @@ def test_each_planted_mistake_is_caught(plant, tmp_path):
     lib = oracle.load_library(plant=plant, out_dir=tmp_path)
     assert _pins_failed(lib), f"planted mistake {plant} went unnoticed"
     assert oracle_build.library_path(plant, tmp_path).exists()
+
+
+@pytest.mark.parametrize("mnk", [(24, 24, 24), (31, 17, 45), (17, 40, 9)])
+def test_nn_reference_is_a_times_b(mnk):
+    """C = A x B with B [K, N]: small integers give the exact integer product
+    A @ B (and not A @ B^T on square shapes)."""
+    m, n, k = mnk
+    a = _rand((m, k), torch.float16, 300 + m, kind="int")
+    b = _rand((k, n), torch.float16, 400 + n, kind="int")
+    ref, bound = oracle.gemm_nn_reference(a, b)
+    ai, bi = a.to(torch.int64).numpy(), b.to(torch.int64).numpy()
+    np.testing.assert_array_equal(ref, (ai @ bi).astype(np.float64))
+    np.testing.assert_array_equal(bound, (np.abs(ai) @ np.abs(bi)).astype(np.float64))
+    if m == n == k:
+        assert not np.array_equal(ref, (ai @ bi.T).astype(np.float64))
