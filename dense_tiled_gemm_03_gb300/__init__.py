@@ -17,8 +17,10 @@ from ._native import (  # noqa: F401
     GEMM_TN_F16,
     GEMM_TN_OK,
     LIBRARY_PATH,
+    GemmTnEpilogue,
     GemmTnError,
     gemm_nn,
+    gemm_tn_fused,
     gemm_tn,
     gemm_tn_config_name,
     gemm_tn_ex,
@@ -33,6 +35,7 @@ from ._native import (  # noqa: F401
     gemm_tn_version,
     library,
     mm_nn,
+    mm_tn_fused,
     mm_tn,
     mm_tn_host,
 )

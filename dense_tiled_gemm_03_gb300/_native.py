@@ -27,6 +27,16 @@ GEMM_TN_ERR_UNSUPPORTED_DEVICE = 4
 GEMM_TN_ERR_CUDA = 5
 GEMM_TN_ERR_TIMEOUT = 6
 
+GEMM_TN_ACT_NONE, GEMM_TN_ACT_RELU, GEMM_TN_ACT_GELU = 0, 1, 2
+GEMM_TN_OUT_INPUT, GEMM_TN_OUT_F32 = 0, 1
+
+
+class GemmTnEpilogue(ctypes.Structure):
+    """struct gemm_tn_epilogue of include/gemm_tn.h."""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
+                ("activation", ctypes.c_int), ("out_dtype", ctypes.c_int)]
+
+
 _lock = threading.Lock()
 _lib: ctypes.CDLL | None = None
 
@@ -37,6 +47,8 @@ _ptr = ctypes.c_void_p
 _SIGNATURES = {
     "gemm_tn": (_int, [_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr]),
     "gemm_tn_ex": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]),
+    "gemm_tn_fused": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64,
+                             ctypes.POINTER(GemmTnEpilogue), _ptr, _ptr]),
     "gemm_nn": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]),
     "gemm_tn_ex_noalloc": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]),
     "gemm_tn_host": (_int, [_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr]),
@@ -86,6 +98,12 @@ def gemm_tn(dtype, m, n, k, a, b, c, stream=None) -> int:
 
 def gemm_tn_ex(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status=None, stream=None) -> int:
     return library().gemm_tn_ex(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, stream)
+
+
+def gemm_tn_fused(dtype, m, n, k, a, lda, b, ldb, c, ldc, epilogue, d_status=None, stream=None) -> int:
+    """D = act(alpha * A x B^T + beta * C + bias) over C (epilogue: GemmTnEpilogue)."""
+    ep = ctypes.byref(epilogue) if epilogue is not None else None
+    return library().gemm_tn_fused(dtype, m, n, k, a, lda, b, ldb, c, ldc, ep, d_status, stream)
 
 
 def gemm_nn(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status=None, stream=None) -> int:
@@ -178,6 +196,42 @@ def mm_tn(a, b, out=None, status=None):
                         d_status, stream)
     if rc != GEMM_TN_OK:
         raise GemmTnError(rc, "gemm_tn_ex")
+    return out
+
+
+_ACTIVATIONS = {"none": GEMM_TN_ACT_NONE, "relu": GEMM_TN_ACT_RELU, "gelu": GEMM_TN_ACT_GELU}
+
+
+def mm_tn_fused(a, b, out=None, alpha=1.0, beta=0.0, bias=None, activation="none", out_fp32=False, status=None):
+    """act(alpha * A x B^T + beta * out + bias) through gemm_tn_fused. a: [M, K],
+    b: [N, K] CUDA fp16/bf16; bias: optional fp32 CUDA [N]; out: [M, N] in
+    a's dtype, or fp32 with out_fp32 (its contents are read when beta != 0)."""
+    import torch
+    if a.device.type != "cuda" or b.device != a.device:
+        raise ValueError("a and b must be CUDA tensors on one device")
+    if a.dtype != b.dtype:
+        raise TypeError("a and b must have the same dtype")
+    m, k = a.shape
+    n, kb = b.shape
+    if kb != k:
+        raise ValueError(f"inner dimensions differ: {tuple(a.shape)} x {tuple(b.shape)}^T")
+    out_dtype = torch.float32 if out_fp32 else a.dtype
+    if out is None:
+        out = torch.zeros((m, n), dtype=out_dtype, device=a.device)
+    elif out.shape != (m, n) or out.dtype != out_dtype or out.device != a.device:
+        raise ValueError("out must be [M, N] on a's device, fp32 with out_fp32 else a's dtype")
+    if bias is not None and (bias.dtype != torch.float32 or bias.shape != (n,) or bias.device != a.device):
+        raise ValueError("bias must be a CUDA fp32 [N] tensor")
+    ep = GemmTnEpilogue(float(alpha), float(beta), bias.data_ptr() if bias is not None else None,
+                        _ACTIVATIONS[activation], GEMM_TN_OUT_F32 if out_fp32 else GEMM_TN_OUT_INPUT)
+    lda, ldb, ldc = _row_pitch(a, k), _row_pitch(b, k), _row_pitch(out, n)
+    stream = torch.cuda.current_stream(a.device).cuda_stream
+    d_status = status.data_ptr() if status is not None else None
+    with torch.cuda.device(a.device):
+        rc = gemm_tn_fused(_dtype_code(a), m, n, k, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(), ldc, ep,
+                           d_status, stream)
+    if rc != GEMM_TN_OK:
+        raise GemmTnError(rc, "gemm_tn_fused")
     return out
 
 

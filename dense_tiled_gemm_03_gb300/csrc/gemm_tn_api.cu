@@ -33,6 +33,9 @@ cudaError_t launch_gemm_2cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& arg
 int max_resident_2cta(int id, bool bf16);
 int smem_bytes_2cta(int id);
 cudaError_t launch_gemm_nn(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_fused(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_fused_k0(bool bf16, void* c, int64_t ldc, bool out_f32, int64_t m, int64_t n, float beta,
+                            const float* bias, int activation, int num_sms, cudaStream_t stream);
 
 namespace {
 
@@ -357,7 +360,8 @@ int group_rows(const ConfigInfo& cfg) {
 
 int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
              void* c, int64_t ldc, int* d_status, cudaStream_t stream, int drop_load_kb,
-             void* fixed_scratch = nullptr, size_t fixed_scratch_bytes = 0, bool b_mn = false) {
+             void* fixed_scratch = nullptr, size_t fixed_scratch_bytes = 0, bool b_mn = false,
+             const gemm_tn_epilogue* fused = nullptr) {
   t_last_cuda_error = 0;
   t_last_message[0] = '\0';
   int st = validate(dtype, m, n, k, a, lda, b, ldb, c, ldc, b_mn);
@@ -367,15 +371,23 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   st = current_device(&dev);
   if (st != GEMM_TN_OK) return st;
 
+  const bool out_f32 = fused != nullptr && fused->out_dtype == GEMM_TN_OUT_F32;
   if (k == 0) {  // the empty sum
+    if (fused != nullptr) {
+      cudaError_t e = launch_fused_k0(dtype == GEMM_TN_BF16, c, ldc, out_f32, m, n, fused->beta, fused->bias,
+                                      fused->activation, dev->num_sms, stream);
+      return e == cudaSuccess ? GEMM_TN_OK : fail_cuda(e, "fused epilogue (K = 0)");
+    }
     cudaError_t e = cudaMemset2DAsync(c, static_cast<size_t>(ldc) * 2, 0, static_cast<size_t>(n) * 2,
                                       static_cast<size_t>(m), stream);
     return e == cudaSuccess ? GEMM_TN_OK : fail_cuda(e, "cudaMemset2DAsync");
   }
   const bool bf16 = dtype == GEMM_TN_BF16;
 
-  const int cfg_id = choose_config(m, n, k, resident_clusters(dev, kCfg2CtaN256, bf16),
-                                   resident_clusters(dev, kCfg2CtaN256Mc, bf16));
+  int cfg_id = choose_config(m, n, k, resident_clusters(dev, kCfg2CtaN256, bf16),
+                             resident_clusters(dev, kCfg2CtaN256Mc, bf16));
+  // the fused epilogue is built for the pair 256 x 256 and single-CTA 128 x 128 tiles
+  if (fused != nullptr && cfg_id != kCfg1CtaN128) cfg_id = m <= 128 ? kCfg1CtaN128 : kCfg2CtaN256;
   const ConfigInfo& cfg = kConfigs[cfg_id];
   const int64_t num_m_tiles = (m + cfg.tile_m - 1) / cfg.tile_m;
   // columns per scheduled tile: a multicast cluster covers two pairs' tiles
@@ -387,7 +399,8 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   const int clusters = resident_clusters(dev, cfg_id, bf16);
   if (clusters <= 0) return fail(GEMM_TN_ERR_CUDA, "kernel cannot be resident on this device (occupancy query)");
   // The no-alloc path keeps to whole tiles: its fixed scratch is for repacks.
-  WorkPlan plan = plan_work(tiles, num_k_blocks, clusters, fixed_scratch == nullptr ? stream_k_mode() : 0);
+  WorkPlan plan = plan_work(tiles, num_k_blocks, clusters,
+                            fixed_scratch == nullptr && fused == nullptr ? stream_k_mode() : 0);
   int64_t split_begin = tiles;
   const int split = plan.sk_iters > 0 ? 1 : tail_split(cfg, tiles, clusters, &split_begin, b_mn);
   if (split > 1) {
@@ -473,7 +486,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
                            CU_TENSOR_MAP_SWIZZLE_128B);
   // C goes out through the TMA when its base and pitch allow; otherwise the
   // epilogue's predicated element stores handle any 2-byte-aligned layout.
-  const bool c_tma = tma_compatible(c, ldc) && !force_direct_epilogue();
+  const bool c_tma = !out_f32 && tma_compatible(c, ldc) && !force_direct_epilogue();
   if (st == GEMM_TN_OK && c_tma)
     st = encode_matrix_map(&args.tmap_c, bf16, c, m, n, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (st != GEMM_TN_OK) {
@@ -501,8 +514,17 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   args.flags = flags;
   args.split = split;
   args.split_begin = static_cast<int32_t>(split_begin);
+  if (fused != nullptr) {
+    args.alpha = fused->alpha;
+    args.beta = fused->beta;
+    args.bias = fused->bias;
+    args.activation = fused->activation;
+    args.out_f32 = out_f32 ? 1 : 0;
+  }
 
-  if (b_mn)
+  if (fused != nullptr)
+    e = launch_gemm_fused(cfg_id, bf16, args, grid_ctas, stream);
+  else if (b_mn)
     e = launch_gemm_nn(cfg_id, bf16, args, grid_ctas, stream);
   else
     e = cfg.cta_group == 2 ? launch_gemm_2cta(cfg_id, bf16, args, grid_ctas, stream)
@@ -622,6 +644,33 @@ int gemm_tn_ex(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_
                void* c, int64_t ldc, int* d_status, gemm_tn_stream_t stream) {
   return run_gemm(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, reinterpret_cast<cudaStream_t>(stream),
                   test_drop_load_kb());
+}
+
+int gemm_tn_fused(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
+                  void* c, int64_t ldc, const gemm_tn_epilogue* epilogue, int* d_status, gemm_tn_stream_t stream) {
+  t_last_cuda_error = 0;
+  t_last_message[0] = '\0';
+  if (epilogue == nullptr) return fail(GEMM_TN_ERR_INVALID_VALUE, "epilogue is NULL");
+  if (epilogue->activation < GEMM_TN_ACT_NONE || epilogue->activation > GEMM_TN_ACT_GELU)
+    return fail(GEMM_TN_ERR_INVALID_VALUE, "unknown activation");
+  if (epilogue->out_dtype != GEMM_TN_OUT_INPUT && epilogue->out_dtype != GEMM_TN_OUT_F32)
+    return fail(GEMM_TN_ERR_INVALID_VALUE, "unknown output dtype");
+  int st = validate(dtype, m, n, k, a, lda, b, ldb, c, ldc);
+  if (st != GEMM_TN_OK || m == 0 || n == 0) return st;
+  const int64_t out_elem = epilogue->out_dtype == GEMM_TN_OUT_F32 ? 4 : 2;
+  if (reinterpret_cast<uintptr_t>(c) % out_elem) return fail(GEMM_TN_ERR_MISALIGNED, "C is not aligned to its element");
+  if (epilogue->bias != nullptr && reinterpret_cast<uintptr_t>(epilogue->bias) % 4)
+    return fail(GEMM_TN_ERR_MISALIGNED, "bias is not 4-byte aligned");
+  if (k > 0) {  // an fp32 C spans twice the bytes the 16-bit overlap check assumed
+    const uintptr_t c0 = reinterpret_cast<uintptr_t>(c);
+    const uintptr_t c1 = c0 + static_cast<uintptr_t>(((m - 1) * ldc + n) * out_elem);
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), a1 = a0 + span_bytes(m, k, lda);
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(b), b1 = b0 + span_bytes(n, k, ldb);
+    if (ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1))
+      return fail(GEMM_TN_ERR_INVALID_VALUE, "C overlaps A or B");
+  }
+  return run_gemm(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, reinterpret_cast<cudaStream_t>(stream),
+                  test_drop_load_kb(), nullptr, 0, false, epilogue);
 }
 
 int gemm_nn(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,

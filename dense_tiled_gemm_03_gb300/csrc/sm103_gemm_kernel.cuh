@@ -77,13 +77,21 @@ struct GemmArgs {
   // wave holds more, shorter units of work (split 1: no cut).
   int32_t split;
   int32_t split_begin;
+  // Fused epilogue (kFused kernels): D = act(alpha * acc + beta * C + bias[j]),
+  // stored in the input dtype or (out_f32) as fp32.
+  float alpha, beta;
+  const float* bias;      // nullable [N]
+  int32_t activation;     // 0 none, 1 relu, 2 gelu
+  int32_t out_f32;
   float* partials;        // per CTA: block_n / 32 chunks x 128 rows x 32 fp32 (stream-K only)
   int* flags;             // per CTA and epilogue warp: 1 once its partial rows are written (zeroed by the host)
 };
 
-template <int kCtaGroup_, int kBlockN_, int kStages_, bool kBf16_, int kClusterPairs_ = 1, bool kBMnMajor_ = false>
+template <int kCtaGroup_, int kBlockN_, int kStages_, bool kBf16_, int kClusterPairs_ = 1, bool kBMnMajor_ = false,
+          bool kFused_ = false>
 struct GemmConfig {
   static constexpr int kCtaGroup = kCtaGroup_;
+  static constexpr bool kFused = kFused_;
   // kBMnMajor: B is stored [K, N] with N contiguous (C = A x B), loaded in
   // 64 x 64 boxes and read by the MMA through MN-major descriptors.
   static constexpr bool kBMnMajor = kBMnMajor_;
@@ -658,6 +666,103 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
               r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + v[j].z);
               r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + v[j].w);
             }
+          }
+        }
+        if constexpr (Cfg::kFused) {
+          // fused epilogue on this thread's row (row0 + lane), columns
+          // [col0, col0 + 32): scale, add the bias and beta * C, activate
+          const int row = row0 + static_cast<int>(lane);
+          const bool row_ok = row < args.m;
+          const bool full = col0 + 32 <= args.n;
+          const int64_t rbase = static_cast<int64_t>(row) * args.ldc + col0;
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = args.alpha * __uint_as_float(r[j]);
+          if (args.bias != nullptr) {
+            const float* bp = args.bias + col0;
+            if (full && (reinterpret_cast<uintptr_t>(bp) & 15u) == 0) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 t = __ldg(reinterpret_cast<const float4*>(bp) + j);
+                v[4 * j] += t.x;
+                v[4 * j + 1] += t.y;
+                v[4 * j + 2] += t.z;
+                v[4 * j + 3] += t.w;
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j < args.n) v[j] += __ldg(bp + j);
+            }
+          }
+          if (args.beta != 0.0f && row_ok) {
+            if (args.out_f32) {
+              const float* src = static_cast<const float*>(args.c) + rbase;
+              if (full && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 t = reinterpret_cast<const float4*>(src)[j];
+                  v[4 * j] += args.beta * t.x;
+                  v[4 * j + 1] += args.beta * t.y;
+                  v[4 * j + 2] += args.beta * t.z;
+                  v[4 * j + 3] += args.beta * t.w;
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (col0 + j < args.n) v[j] += args.beta * src[j];
+              }
+            } else {
+              const uint16_t* src = static_cast<const uint16_t*>(args.c) + rbase;
+              auto widen = [](uint32_t bits16) {
+                if constexpr (Cfg::kBf16) {
+                  return __uint_as_float(bits16 << 16);
+                } else {
+                  return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
+                }
+              };
+              if (full && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const uint4 t = reinterpret_cast<const uint4*>(src)[j];
+                  const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) {
+                    v[8 * j + 2 * q] += args.beta * widen(w4[q] & 0xFFFFu);
+                    v[8 * j + 2 * q + 1] += args.beta * widen(w4[q] >> 16);
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (col0 + j < args.n) v[j] += args.beta * widen(src[j]);
+              }
+            }
+          }
+          if (args.activation == 1) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j], 0.0f);
+          } else if (args.activation == 2) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.5f * v[j] * (1.0f + erff(v[j] * 0.70710678118654752f));
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
+          if (args.out_f32) {
+            // fp32 output: each thread writes its row's 32 values (128 bytes)
+            if (row_ok) {
+              float* dst = static_cast<float*>(args.c) + rbase;
+              if (full && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  reinterpret_cast<float4*>(dst)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (col0 + j < args.n) dst[j] = v[j];
+              }
+            }
+            continue;
           }
         }
         // this thread holds row (row0 + lane), columns [col0, col0 + 32)

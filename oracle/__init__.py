@@ -28,7 +28,7 @@ import numpy as np
 
 from . import build as _build
 
-__all__ = ["gemm_tn_reference", "gemm_nn_reference", "parity_report", "ParityReport", "ALLOW_REL", "ALLOW_ABS",
+__all__ = ["gemm_tn_reference", "gemm_nn_reference", "fused_reference", "fused_parity_report", "parity_report", "ParityReport", "ALLOW_REL", "ALLOW_ABS",
            "host_threads", "load_library"]
 
 #: The pass criterion's two constants: |c - ref| <= ALLOW_REL * bound + ALLOW_ABS.
@@ -110,6 +110,53 @@ def gemm_nn_reference(a, b, nthreads: int | None = None):
     section "The first kernel: GEMM": B declared (K, N))."""
     B = _as_f64(b)
     return gemm_tn_reference(a, np.ascontiguousarray(B.T), nthreads=nthreads)
+
+
+#: activation codes of the fused epilogue (same numbering as the C ABI)
+ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
+#: largest slope of each activation (GELU's derivative peaks at ~1.129)
+ACT_LIPSCHITZ = {ACT_NONE: 1.0, ACT_RELU: 1.0, ACT_GELU: 1.13}
+
+
+def _activation(x: np.ndarray, act: int) -> np.ndarray:
+    if act == ACT_NONE:
+        return x
+    if act == ACT_RELU:
+        return np.maximum(x, 0.0)
+    if act == ACT_GELU:  # x * Phi(x), Phi the standard normal CDF
+        from scipy.special import erf
+        return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))
+    raise ValueError(f"unknown activation {act}")
+
+
+def fused_reference(a, b, alpha=1.0, beta=0.0, c_in=None, bias=None, activation=ACT_NONE, b_kn=False):
+    """D = act(alpha * (A x B^T) + beta * C_in + bias[j]) in fp64, with the
+    magnitude bound of the pre-activation value:
+        pre_bound[i][j] = |alpha| * sum_k |a_ik b_jk| + |beta * c_ij| + |bias_j|.
+    The GEMM part is gemm_tn_reference (gemm_nn_reference with b_kn); the
+    epilogue is the product's definition written out element by element
+    (scale, add, add, activate). Returns (d, pre_bound)."""
+    ref, bound = gemm_nn_reference(a, b) if b_kn else gemm_tn_reference(a, b)
+    pre = float(alpha) * ref
+    pre_bound = abs(float(alpha)) * bound
+    if beta != 0.0 and c_in is not None:
+        cin = _as_f64(c_in)
+        pre = pre + float(beta) * cin
+        pre_bound = pre_bound + np.abs(float(beta) * cin)
+    if bias is not None:
+        bb = _as_f64(bias).reshape(1, -1)
+        pre = pre + bb
+        pre_bound = pre_bound + np.abs(bb)
+    return _activation(pre, activation), pre_bound
+
+
+def fused_parity_report(d, d_ref: np.ndarray, pre_bound: np.ndarray, activation=ACT_NONE) -> "ParityReport":
+    """The GEMM criterion carried through the epilogue: an error e in the
+    pre-activation value moves the output by at most L*e (L the activation's
+    largest slope), so |d - d_ref| <= L * (1e-2 * pre_bound + 1e-3)."""
+    lip = ACT_LIPSCHITZ[activation]
+    return parity_report(d, d_ref, lip * pre_bound + (lip - 1.0) * ALLOW_ABS / ALLOW_REL) if lip != 1.0 \
+        else parity_report(d, d_ref, pre_bound)
 
 
 @dataclass

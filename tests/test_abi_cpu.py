@@ -110,3 +110,20 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_native, "LIBRARY_PATH", tmp_path / "libgemm_tn.so")
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         _native.library()
+
+
+
+def test_fused_entry_validation(lib):
+    ep = gt.GemmTnEpilogue(1.0, 0.0, None, 7, 0)
+    assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, C, 4, ep, None, None) == gt.GEMM_TN_ERR_INVALID_VALUE
+    assert "activation" in gt.gemm_tn_last_error_message()
+    ep = gt.GemmTnEpilogue(1.0, 0.0, None, 0, 5)
+    assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, C, 4, ep, None, None) == gt.GEMM_TN_ERR_INVALID_VALUE
+    ep = gt.GemmTnEpilogue(1.0, 0.0, None, 0, 1)          # fp32 C must be 4-byte aligned
+    assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, C + 2, 4, ep, None, None) == gt.GEMM_TN_ERR_MISALIGNED
+    ep = gt.GemmTnEpilogue(1.0, 0.0, A + 2, 0, 0)         # bias must be 4-byte aligned
+    assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, C, 4, ep, None, None) == gt.GEMM_TN_ERR_MISALIGNED
+    # an fp32 C of 4 x 4 spans 64 bytes: starting 40 bytes before B overlaps it
+    ep = gt.GemmTnEpilogue(1.0, 0.0, None, 0, 1)
+    assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, B - 40, 4, ep, None, None) == gt.GEMM_TN_ERR_INVALID_VALUE
+    assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, C, 4, None, None, None) == gt.GEMM_TN_ERR_INVALID_VALUE

@@ -518,3 +518,67 @@ def test_nn_headline_shape_sampled():
     rows = edge_indices(w.m, 256, rng, 8)
     cols = edge_indices(w.n, 256, rng, 8)
     assert_sampled_parity(c, a_cpu, bt_cpu, rows, cols, "nn headline")
+
+
+
+# ------------------------------------------------------------ fused epilogue (gemm_tn_fused)
+
+def _fused_case(m, n, k, dtype, activation, out_fp32, alpha, beta, with_bias, seed, ldc_pad=0):
+    import oracle
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, dtype, "uniform", seed=seed)
+    g = torch.Generator().manual_seed(seed)
+    bias = (torch.rand(n, generator=g) * 4 - 2).float() if with_bias else None
+    out_dtype = torch.float32 if out_fp32 else a_cpu.dtype
+    c_in = (torch.rand((m, n), generator=g) * 2 - 1).to(out_dtype)
+    c_big = torch.full((m, n + ldc_pad), float("nan"), dtype=out_dtype)
+    c_big[:, :n] = c_in
+    c_big = c_big.to(dev)
+    c = c_big[:, :n]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    gt.mm_tn_fused(a_cpu.to(dev), b_cpu.to(dev), out=c, alpha=alpha, beta=beta,
+                   bias=bias.to(dev) if bias is not None else None, activation=activation, out_fp32=out_fp32,
+                   status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    act = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "gelu": oracle.ACT_GELU}[activation]
+    d_ref, pre_bound = oracle.fused_reference(a_cpu, b_cpu, alpha, beta, c_in, bias, act)
+    rep = oracle.fused_parity_report(c.cpu(), d_ref, pre_bound, act)
+    assert rep.ok, f"fused {m}x{n}x{k} {dtype} {activation} f32={out_fp32} a={alpha} b={beta}: {rep}"
+    if ldc_pad:
+        assert torch.isnan(c_big[:, n:].float()).all(), "wrote outside C"
+
+
+@pytest.mark.parametrize("activation", ["none", "relu", "gelu"])
+@pytest.mark.parametrize("out_fp32", [False, True])
+@pytest.mark.parametrize("mnk", [(129, 257, 65), (300, 1000, 640), (64, 640, 512), (1000, 1003, 200)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_fused_epilogue_parity(mnk, activation, out_fp32):
+    m, n, k = mnk
+    _fused_case(m, n, k, "bf16", activation, out_fp32, alpha=0.75, beta=0.5, with_bias=True, seed=m + n + k)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("beta,with_bias", [(0.0, False), (1.0, False), (0.0, True)])
+def test_fused_epilogue_terms(dtype, beta, with_bias):
+    _fused_case(777, 900, 333, dtype, "relu", False, alpha=1.5, beta=beta, with_bias=with_bias, seed=9, ldc_pad=5)
+
+
+@pytest.mark.parametrize("out_fp32", [False, True])
+def test_fused_epilogue_k_zero(out_fp32):
+    _fused_case(100, 70, 0, "fp16", "gelu", out_fp32, alpha=2.0, beta=0.5, with_bias=True, seed=3)
+
+
+def test_fused_headline_shape_sampled():
+    """bf16 8192^3 with bias + GELU and fp32 output: sampled rows and columns."""
+    import oracle
+    w = WORKLOADS["bf16_8192x8192x8192"]
+    a_cpu, b_cpu = workload_operands(w)
+    dev = torch.device("cuda", 0)
+    bias = torch.linspace(-1, 1, w.n, dtype=torch.float32)
+    c = gt.mm_tn_fused(a_cpu.to(dev), b_cpu.to(dev), bias=bias.to(dev), activation="gelu", out_fp32=True).cpu()
+    rng = np.random.Generator(np.random.PCG64(9))
+    rows = torch.as_tensor(edge_indices(w.m, 256, rng, 8))
+    d_ref, pb = oracle.fused_reference(a_cpu.index_select(0, rows), b_cpu, bias=bias, activation=oracle.ACT_GELU)
+    rep = oracle.fused_parity_report(c.index_select(0, rows), d_ref, pb, oracle.ACT_GELU)
+    assert rep.ok, rep

@@ -211,3 +211,44 @@ def test_nn_reference_is_a_times_b(mnk):
     np.testing.assert_array_equal(bound, (np.abs(ai) @ np.abs(bi)).astype(np.float64))
     if m == n == k:
         assert not np.array_equal(ref, (ai @ bi.T).astype(np.float64))
+
+
+# ---------------------------------------------------------------- fused epilogue
+
+def test_fused_reference_closed_forms():
+    """Scale, add and activation pinned to values fixed by arithmetic."""
+    a = _rand((8, 16), torch.float16, 500, kind="int")
+    b = _rand((6, 16), torch.float16, 501, kind="int")
+    exact = (a.long() @ b.long().T).double().numpy()
+    # alpha scales exactly (powers of two), no epilogue terms otherwise
+    d, pb = oracle.fused_reference(a, b, alpha=2.0)
+    np.testing.assert_array_equal(d, 2.0 * exact)
+    # alpha 0, beta 1: D = C_in + bias, exactly
+    c_in = torch.arange(48, dtype=torch.float32).reshape(8, 6) - 20
+    bias = torch.tensor([0.5, -1.0, 2.0, 0.0, -0.25, 4.0])
+    d, pb = oracle.fused_reference(a, b, alpha=0.0, beta=1.0, c_in=c_in, bias=bias)
+    np.testing.assert_array_equal(d, c_in.double().numpy() + bias.double().numpy()[None, :])
+    # relu keeps the non-negative part
+    d, _ = oracle.fused_reference(a, b, activation=oracle.ACT_RELU)
+    np.testing.assert_array_equal(d, np.maximum(exact, 0.0))
+
+
+def test_gelu_reference_properties():
+    """GELU(x) = x * Phi(x): GELU(0) = 0, GELU(x) - GELU(-x) = x, Phi(1) and
+    Phi(2) from the normal CDF's tabulated values, and GELU(x) ~ x for large x."""
+    x = np.array([0.0, 1.0, 2.0, -1.0, -2.0, 8.0, -8.0])
+    g = oracle._activation(x, oracle.ACT_GELU)
+    assert g[0] == 0.0
+    np.testing.assert_allclose(g[1] - g[3], 1.0, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(g[2] - g[4], 2.0, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(g[1], 0.8413447460685429, rtol=1e-15)      # Phi(1)
+    np.testing.assert_allclose(g[2] / 2.0, 0.9772498680518208, rtol=1e-15)  # Phi(2)
+    assert abs(g[5] - 8.0) < 1e-13 and abs(g[6]) < 1e-13
+
+
+def test_fused_tolerance_scales_with_the_activation_slope():
+    ref = np.zeros((2, 2))
+    pb = np.ones((2, 2))
+    d = ref + 1.05 * (oracle.ALLOW_REL * 1.0 + oracle.ALLOW_ABS)   # 5% over the plain allowance
+    assert not oracle.fused_parity_report(d, ref, pb, oracle.ACT_NONE).ok
+    assert oracle.fused_parity_report(d, ref, pb, oracle.ACT_GELU).ok    # GELU allows 13% more
