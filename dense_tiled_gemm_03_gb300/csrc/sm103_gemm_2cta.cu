@@ -13,8 +13,25 @@ using CfgPair128Bf16 = gemm_tn_dev::GemmConfig<2, 128, 8, true>;
 // two pairs per cluster sharing A through TMA multicast
 using CfgPairMcF16 = gemm_tn_dev::GemmConfig<2, 256, 6, false, 2>;
 using CfgPairMcBf16 = gemm_tn_dev::GemmConfig<2, 256, 6, true, 2>;
+// the same two configurations able to run the cut sub-tiles of a last wave
+using CfgPairSplitF16 = gemm_tn_dev::GemmConfig<2, 256, 6, false, 1, false, false, true>;
+using CfgPairSplitBf16 = gemm_tn_dev::GemmConfig<2, 256, 6, true, 1, false, false, true>;
+using CfgPairMcSplitF16 = gemm_tn_dev::GemmConfig<2, 256, 6, false, 2, false, false, true>;
+using CfgPairMcSplitBf16 = gemm_tn_dev::GemmConfig<2, 256, 6, true, 2, false, false, true>;
 
 cudaError_t launch_gemm_2cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream) {
+  if (args.split > 1) {
+    switch (id) {
+      case kCfg2CtaN256:
+        return bf16 ? Launcher<CfgPairSplitBf16>::launch(args, grid, stream)
+                    : Launcher<CfgPairSplitF16>::launch(args, grid, stream);
+      case kCfg2CtaN256Mc:
+        return bf16 ? Launcher<CfgPairMcSplitBf16>::launch(args, grid, stream)
+                    : Launcher<CfgPairMcSplitF16>::launch(args, grid, stream);
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
   switch (id) {
     case kCfg2CtaN256:
       return bf16 ? Launcher<CfgPairBf16>::launch(args, grid, stream) : Launcher<CfgPairF16>::launch(args, grid, stream);

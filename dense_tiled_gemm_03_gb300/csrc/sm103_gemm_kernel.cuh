@@ -76,7 +76,9 @@ struct GemmArgs {
   // are each cut into `split` sub-tiles of block_n / split columns, so that
   // wave holds more, shorter units of work (split 1: no cut).
   int32_t split;
+  int32_t split_log2;     // log2(split)
   int32_t split_begin;
+  int32_t dp_units;       // split_begin + (dp_tiles - split_begin) * split
   // Fused epilogue (kFused kernels): D = act(alpha * acc + beta * C + bias[j]),
   // stored in the input dtype or (out_f32) as fp32.
   float alpha, beta;
@@ -88,10 +90,14 @@ struct GemmArgs {
 };
 
 template <int kCtaGroup_, int kBlockN_, int kStages_, bool kBf16_, int kClusterPairs_ = 1, bool kBMnMajor_ = false,
-          bool kFused_ = false>
+          bool kFused_ = false, bool kTailSplit_ = false>
 struct GemmConfig {
   static constexpr int kCtaGroup = kCtaGroup_;
   static constexpr bool kFused = kFused_;
+  // kTailSplit: the instantiation that can run the cut sub-tiles of the last
+  // wave; the others keep every unit a whole tile (the split arithmetic
+  // measurably slows the main loops when compiled in but unused).
+  static constexpr bool kTailSplit = kTailSplit_;
   // kBMnMajor: B is stored [K, N] with N contiguous (C = A x B), loaded in
   // 64 x 64 boxes and read by the MMA through MN-major descriptors.
   static constexpr bool kBMnMajor = kBMnMajor_;
@@ -171,6 +177,7 @@ struct WorkItem {
   int kb_end;      // one past the last k-block
   int sub;         // sub-tile index along N within a cut tile (0 when whole)
   int nsub;        // number of sub-tiles the tile is cut into (1 when whole)
+  int nsub_log2;   // log2(nsub)
 };
 
 // First stream-K iteration of `worker`'s range.
@@ -192,8 +199,10 @@ __device__ __forceinline__ int sk_worker_of(const GemmArgs& a, int64_t i) {
 // contributor's partial is written early, and the finisher's fix-up epilogue
 // overlaps the main loop of the whole tiles that follow. Every role of a CTA
 // walks the same sequence.
+template <bool kTailSplit>
 struct WorkCursor {
-  int64_t dp_next, sk_cur, sk_end;
+  int dp_next;
+  int64_t sk_cur, sk_end;
 
   __device__ __forceinline__ WorkCursor(const GemmArgs& a, int worker)
       : dp_next(worker), sk_cur(0), sk_end(0) {
@@ -214,21 +223,24 @@ struct WorkCursor {
       w.kb_end = kb1;
       w.sub = 0;
       w.nsub = 1;
+      w.nsub_log2 = 0;
       sk_cur += kb1 - kb0;
       return true;
     }
     // whole tiles, then the sub-tiles of the cut tail tiles, round-robin
-    const int64_t units = a.split_begin + static_cast<int64_t>(a.dp_tiles - a.split_begin) * a.split;
-    if (dp_next < units) {
-      if (dp_next < a.split_begin) {
-        w.tile = static_cast<int>(dp_next);
+    // (32-bit arithmetic and shifts: the split is a power of two)
+    if (dp_next < (kTailSplit ? a.dp_units : a.dp_tiles)) {
+      if (!kTailSplit || dp_next < a.split_begin) {
+        w.tile = dp_next;
         w.sub = 0;
         w.nsub = 1;
+        w.nsub_log2 = 0;
       } else {
-        const int64_t u = dp_next - a.split_begin;
-        w.tile = a.split_begin + static_cast<int>(u / a.split);
-        w.sub = static_cast<int>(u % a.split);
+        const int u = dp_next - a.split_begin;
+        w.tile = a.split_begin + (u >> a.split_log2);
+        w.sub = u & (a.split - 1);
         w.nsub = a.split;
+        w.nsub_log2 = a.split_log2;
       }
       w.kb_begin = 0;
       w.kb_end = a.num_k_blocks;
@@ -388,24 +400,24 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       for (int s = 0; s < Cfg::kStages; ++s) issued_phase_of[s] = -1;
       bool ok = true;
       int item_index = 0;
-      WorkCursor cursor(args, worker);
+      WorkCursor<Cfg::kTailSplit> cursor(args, worker);
       WorkItem item;
       while (ok && cursor.next(args, item)) {
         int tm, tj;
         tile_coords(item.tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tj);
         const int tn = tj * Cfg::kClusterPairs + static_cast<int>(pair);
         const int a_row = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM;
-        const int sub_n = Cfg::kBlockN / item.nsub;   // columns of this unit of work
-        const int b_row = tn * Cfg::kBlockN + item.sub * sub_n + static_cast<int>(cta_rank) * (Cfg::kBRows / item.nsub);
+        const int sub_n = Cfg::kBlockN >> item.nsub_log2;   // columns of this unit of work
+        const int b_row = tn * Cfg::kBlockN + item.sub * sub_n + static_cast<int>(cta_rank) * (Cfg::kBRows >> item.nsub_log2);
         const void* tmap_b = item.nsub > 1 && !Cfg::kBMnMajor ? static_cast<const void*>(&args.tmap_b_split)
                                                               : static_cast<const void*>(&args.tmap_b);
-        const uint32_t b_bytes = Cfg::kBTileBytes / static_cast<uint32_t>(item.nsub);
+        const uint32_t b_bytes = Cfg::kBTileBytes >> item.nsub_log2;
         // B of one k-block into this CTA's stage buffer, completing on `bar`
         // (the pair leader's barrier for CTA pairs): one box [rows x 64 K]
         // when K-major, or 64-wide N boxes of [64 K x 64 N] when MN-major.
         auto load_b = [&](int stage_, uint32_t bar, int kb_) {
           if constexpr (Cfg::kBMnMajor) {
-            const int boxes = Cfg::kBRows / item.nsub / 64;
+            const int boxes = (Cfg::kBRows >> item.nsub_log2) / 64;
             for (int j = 0; j < boxes; ++j) {
               if constexpr (Cfg::kCtaGroup == 2) {
                 tma_load_2d_pair(tmap_b, b_tile(stage_) + j * Cfg::kBMnBoxBytes, bar, b_row + 64 * j,
@@ -485,7 +497,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      WorkCursor cursor(args, worker);
+      WorkCursor<Cfg::kTailSplit> cursor(args, worker);
       WorkItem item;
       while (ok && cursor.next(args, item)) {
         if (!wd.wait(acc_empty_bar(acc), acc_phase ^ 1u)) {
@@ -497,7 +509,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         // a sub-tile of a cut tile multiplies with N = block_n / nsub
         const uint32_t idesc =
             item.nsub == 1 ? Cfg::kIdesc
-                           : mma_idesc_f16(Cfg::kBf16, Cfg::kTileM, Cfg::kBlockN / item.nsub, Cfg::kBMnMajor);
+                           : mma_idesc_f16(Cfg::kBf16, Cfg::kTileM, Cfg::kBlockN >> item.nsub_log2, Cfg::kBMnMajor);
         for (int kb = item.kb_begin; kb < item.kb_end; ++kb) {
           if (!wd.wait(full_bar(stage), phase)) {
             ok = false;
@@ -565,7 +577,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
     constexpr int kChunks = Cfg::kBlockN / 32;
     const int64_t row_in_cta = static_cast<int64_t>(quarter) * 32 + lane;
     bool ok = true;
-    WorkCursor cursor(args, worker);
+    WorkCursor<Cfg::kTailSplit> cursor(args, worker);
     WorkItem item;
     while (ok && cursor.next(args, item)) {
       int tm, tj;
@@ -574,11 +586,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       if (!wd.wait(acc_full_bar(acc), acc_phase)) break;
       tc_fence_after_sync();
       const int row0 = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM + static_cast<int>(quarter) * 32;
-      const int col_tile = tn * Cfg::kBlockN + item.sub * (Cfg::kBlockN / item.nsub);
+      const int col_tile = tn * Cfg::kBlockN + item.sub * (Cfg::kBlockN >> item.nsub_log2);
       const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + static_cast<uint32_t>(acc * Cfg::kAccCols);
       // 32-column chunks of this tile that lie inside N (warp-uniform; 0 when
       // a multicast cluster's second pair lies wholly past N)
-      const int chunks = max(0, min(kChunks / item.nsub, (args.n - col_tile + 31) / 32));
+      const int chunks = max(0, min(kChunks >> item.nsub_log2, (args.n - col_tile + 31) / 32));
       if (chunks == 0) {
         tc_fence_before_sync();
         __syncwarp();
