@@ -40,10 +40,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC_BYTES = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the current
     # kernels (profiles/gemm_tn_*.md)
-    ("bf16_8192x8192x8192", "2cta_n256"): 1_123_382_272 + 126_294_016,
-    ("fp16_4096x4096x4096", "2cta_n256_mc"): 81_554_944 + 15_040_256,
-    ("bf16_128x16384x16384", "1cta_n128"): 541_129_472 + 3_346_944,
-    ("fp16_3001x5003x4097", "2cta_n256_mc"): 75_436_544 + 9_654_272,
+    ("bf16_8192x8192x8192", "2cta_n256"): 1_062_835_456 + 124_839_424,
+    ("fp16_4096x4096x4096", "2cta_n256_mc"): 81_862_912 + 14_420_736,
+    ("bf16_128x16384x16384", "1cta_n128"): 541_118_720 + 3_267_072,
+    ("fp16_3001x5003x4097", "2cta_n256_mc"): 82_356_480 + 13_108_992,
 }
 
 
