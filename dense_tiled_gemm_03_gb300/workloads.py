@@ -82,3 +82,59 @@ def make_operands(m: int, n: int, k: int, dtype: str | torch.dtype, dist: str = 
 def workload_operands(w: Workload | str) -> tuple[torch.Tensor, torch.Tensor]:
     w = WORKLOADS[w] if isinstance(w, str) else w
     return make_operands(w.m, w.n, w.k, w.dtype, w.dist, w.seed)
+
+
+# ---------------------------------------------------------------- attention
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """Q, K, V and O of shape [batch, seq, heads, dim] ("TileLang: a tile
+    language one level below Triton", section "FlashAttention: online softmax
+    as tile code": its kernel's tensors are (batch, seq, heads, dim))."""
+    name: str
+    dtype: str            # storage dtype of Q, K, V and O
+    batch: int
+    seq: int
+    heads: int
+    dim: int
+    causal: bool
+    seed: int
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return DTYPES[self.dtype]
+
+    @property
+    def shape(self) -> tuple[int, int, int, int]:
+        return (self.batch, self.seq, self.heads, self.dim)
+
+    @property
+    def flops(self) -> int:
+        """Multiply-adds of the two products counted as 2 FLOP each: 4 * S^2 * D
+        per batch and head, over the visible (query, key) pairs only when
+        causal: S (S + 1) / 2 of the S^2."""
+        pairs = self.seq * (self.seq + 1) // 2 if self.causal else self.seq * self.seq
+        return 4 * self.batch * self.heads * pairs * self.dim
+
+
+ATTN_WORKLOADS = {
+    w.name: w for w in [
+        # the section's own call: flash_attn(batch 1, heads 8, seq 1024, dim 64), fp16, causal
+        AttnWorkload("attn_fp16_b1_s1024_h8_d64_causal", "fp16", 1, 1024, 8, 64, True, 2001),
+        AttnWorkload("attn_fp16_b4_s4096_h16_d64_causal", "fp16", 4, 4096, 16, 64, True, 2002),
+        AttnWorkload("attn_bf16_b2_s8192_h32_d128_causal", "bf16", 2, 8192, 32, 128, True, 2003),
+        AttnWorkload("attn_bf16_b2_s4096_h16_d128", "bf16", 2, 4096, 16, 128, False, 2004),
+    ]
+}
+
+
+def make_qkv(batch: int, seq: int, heads: int, dim: int, dtype: str | torch.dtype,
+             seed: int = 0) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Q, K, V [batch, seq, heads, dim] on the CPU, contiguous, in the storage
+    dtype: a numpy Generator(PCG64(seed)) draws Q, then K, then V as standard
+    normals in fp32, rounded to nearest-even by torch."""
+    tdt = DTYPES[dtype] if isinstance(dtype, str) else dtype
+    gen = np.random.Generator(np.random.PCG64(seed))
+    shape = (batch, seq, heads, dim)
+    return tuple(torch.from_numpy(gen.standard_normal(size=shape, dtype=np.float32)).to(tdt)
+                 for _ in range(3))

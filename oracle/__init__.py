@@ -12,9 +12,13 @@ Contents:
     with NaN/Inf anywhere in c counted as a failure.
   * ``tiling_model``       -- the traffic / shared-memory model and the counted
     tiled loop of "Tiling a matmul" (pure Python).
+  * ``attention_reference`` -- the attention forward pass that consumes the
+    GEMM (C, ``attention_oracle.c``): O = softmax(scale * Q K^T, causal mask) V
+    per batch and head, with bound = sum_j p_j |V_j|; checked with the same
+    criterion by ``parity_report``.
 
-Parity pins: every function here is pinned by ``tests/test_oracle_pins.py`` and
-``tests/test_tiling_model.py`` to values fixed by the pages or by mathematics
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``,
+``tests/test_attention_oracle_pins.py`` and ``tests/test_tiling_model.py`` to values fixed by the pages or by mathematics
 (exact rational brute force, identity/permutation/integer closed forms, the
 pages' printed tables); none is "parity unpinned".
 """
@@ -28,7 +32,7 @@ import numpy as np
 
 from . import build as _build
 
-__all__ = ["gemm_tn_reference", "gemm_nn_reference", "fused_reference", "fused_parity_report", "parity_report", "ParityReport", "ALLOW_REL", "ALLOW_ABS",
+__all__ = ["attention_reference", "gemm_tn_reference", "gemm_nn_reference", "fused_reference", "fused_parity_report", "parity_report", "ParityReport", "ALLOW_REL", "ALLOW_ABS",
            "host_threads", "load_library"]
 
 #: The pass criterion's two constants: |c - ref| <= ALLOW_REL * bound + ALLOW_ABS.
@@ -57,6 +61,11 @@ def load_library(plant: int = 0, out_dir=None) -> ctypes.CDLL:
     fn = lib.oracle_gemm_tn_f64
     fn.restype = ctypes.c_int
     fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    fa = lib.oracle_attention_f64
+    fa.restype = ctypes.c_int
+    fa.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                   ctypes.c_int64, ctypes.c_int64, ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
                    ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     _LIBS[key] = lib
     return lib
@@ -110,6 +119,41 @@ def gemm_nn_reference(a, b, nthreads: int | None = None):
     section "The first kernel: GEMM": B declared (K, N))."""
     B = _as_f64(b)
     return gemm_tn_reference(a, np.ascontiguousarray(B.T), nthreads=nthreads)
+
+
+def attention_reference(q, k, v, causal: bool = True, scale: float | None = None, rows=None,
+                        nthreads: int | None = None, lib: ctypes.CDLL | None = None):
+    """out, bound of the attention forward pass ("TileLang: a tile language one
+    level below Triton", section "FlashAttention: online softmax as tile code").
+
+    q, k, v: [batch, seq, heads, dim] (torch or numpy, read exactly as fp64).
+    For every batch b, head h and query position i in ``rows`` (all positions
+    when None), with the visible keys j <= i (causal) or all j:
+        s_j = scale * q[b, i, h] . k[b, j, h]      (scale default 1/sqrt(dim))
+        p_j = exp(s_j - max s) / sum_j' exp(s_j' - max s)
+        out[b, r, h, d] = sum_j p_j v[b, j, h, d]
+        bound[b, r, h, d] = sum_j p_j |v[b, j, h, d]|
+    Returns two fp64 arrays of shape [batch, len(rows), heads, dim]. ``lib``
+    selects another build (the pinning tests pass deliberately wrong ones).
+    """
+    Q, K, V = _as_f64(q), _as_f64(k), _as_f64(v)
+    if Q.ndim != 4 or Q.shape != K.shape or Q.shape != V.shape:
+        raise ValueError(f"expected q, k, v of one shape [B, S, H, D], got {Q.shape}, {K.shape}, {V.shape}")
+    B, S, H, D = Q.shape
+    sc = float(scale) if scale is not None else (1.0 / np.sqrt(D) if D else 1.0)
+    rows_arr = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    R = S if rows_arr is None else rows_arr.size
+    out = np.zeros((B, R, H, D), dtype=np.float64)
+    bound = np.zeros((B, R, H, D), dtype=np.float64)
+    if B and R and H and D:
+        lib = lib or load_library()
+        rc = lib.oracle_attention_f64(Q.ctypes.data, K.ctypes.data, V.ctypes.data, B, S, H, D, sc,
+                                      1 if causal else 0,
+                                      None if rows_arr is None else rows_arr.ctypes.data, R,
+                                      out.ctypes.data, bound.ctypes.data, int(nthreads or host_threads()))
+        if rc != 0:
+            raise RuntimeError(f"oracle_attention_f64 failed with {rc}")
+    return out, bound
 
 
 #: activation codes of the fused epilogue (same numbering as the C ABI)

@@ -1,8 +1,9 @@
 """Build step for the CPU oracle's C part (test infrastructure).
 
-Compiles ``gemm_oracle.c`` into ``oracle/liboracle_<machine>.so`` with gcc:
--O2, no fast-math and -ffp-contract=off, so the fp64 loop rounds exactly as its
-source reads on both x86_64 and aarch64 hosts.
+Compiles ``gemm_oracle.c`` and ``attention_oracle.c`` into
+``oracle/liboracle_<machine>.so`` with gcc: -O2, no fast-math and
+-ffp-contract=off, so the fp64 loops round exactly as their source reads on
+both x86_64 and aarch64 hosts.
 """
 from __future__ import annotations
 
@@ -12,7 +13,7 @@ import subprocess
 from pathlib import Path
 
 HERE = Path(__file__).resolve().parent
-SOURCE = HERE / "gemm_oracle.c"
+SOURCES = (HERE / "gemm_oracle.c", HERE / "attention_oracle.c")
 
 CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
           "-fno-fast-math", "-Wall", "-Wextra"]
@@ -29,11 +30,11 @@ def build(plant: int = 0, out_dir: Path | None = None, force: bool = False) -> P
     variant for the pinning tests). Returns the path of the shared object."""
     out = library_path(plant, out_dir)
     if (not force and out.exists()
-            and out.stat().st_mtime >= SOURCE.stat().st_mtime):
+            and all(out.stat().st_mtime >= src.stat().st_mtime for src in SOURCES)):
         return out
     out.parent.mkdir(parents=True, exist_ok=True)
     tmp = out.with_suffix(f".tmp{os.getpid()}.so")
-    cmd = ["gcc", *CFLAGS, f"-DORACLE_PLANT={int(plant)}", str(SOURCE), "-o", str(tmp), "-lm"]
+    cmd = ["gcc", *CFLAGS, f"-DORACLE_PLANT={int(plant)}", *map(str, SOURCES), "-o", str(tmp), "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
