@@ -1,5 +1,6 @@
 """GB300-native tiled dense GEMM, C = A x B^T (A [M,K], B [N,K], K-major,
-fp16/bf16 in, fp32 accumulate, fp16/bf16 out).
+fp16/bf16 in, fp32 accumulate, fp16/bf16 out), and the attention forward pass
+built on the same pipeline (``flash_attn``).
 
 The product is the C-ABI library ``libgemm_tn.so`` (hand-written sm_103a CUDA:
 TMA, mbarrier rings, tcgen05 tensor cores with TMEM accumulators); this
@@ -19,6 +20,8 @@ from ._native import (  # noqa: F401
     LIBRARY_PATH,
     GemmTnEpilogue,
     GemmTnError,
+    flash_attn,
+    flash_attn_fwd,
     gemm_nn,
     gemm_tn_fused,
     gemm_tn,

@@ -1,4 +1,5 @@
-"""ctypes binding of ``libgemm_tn.so`` (the C ABI in ``include/gemm_tn.h``).
+"""ctypes binding of ``libgemm_tn.so`` (the C ABI in ``include/gemm_tn.h`` and
+``include/flash_attn.h``).
 
 Argument marshalling only: every step of the product runs in the library's
 CUDA kernels. The functions keep the C names and signatures; ``mm_tn`` and
@@ -59,6 +60,8 @@ _SIGNATURES = {
     "gemm_tn_last_cuda_error": (_int, []),
     "gemm_tn_last_error_message": (ctypes.c_char_p, []),
     "gemm_tn_version": (_int, []),
+    "flash_attn_fwd": (_int, [_int, _i64, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr, ctypes.c_float, _int, _ptr,
+                              _ptr]),
 }
 
 
@@ -122,6 +125,14 @@ GEMM_TN_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 def gemm_tn_host(dtype, m, n, k, a_host, b_host, c_host, stream=None) -> int:
     return library().gemm_tn_host(dtype, m, n, k, a_host, b_host, c_host, stream)
+
+
+def flash_attn_fwd(dtype, batch, seq, heads, head_dim, q, k, v, o, softmax_scale=0.0, causal=1, d_status=None,
+                   stream=None) -> int:
+    """O = softmax(scale * Q K^T, mask) V on [batch, seq, heads, head_dim] arrays
+    (see include/flash_attn.h)."""
+    return library().flash_attn_fwd(dtype, batch, seq, heads, head_dim, q, k, v, o, float(softmax_scale),
+                                    1 if causal else 0, d_status, stream)
 
 
 def gemm_tn_select_config(dtype, m, n, k) -> int:
@@ -281,4 +292,35 @@ def mm_tn_host(a, b, out=None, device=None):
         rc = gemm_tn_host(_dtype_code(a), m, n, k, a.data_ptr(), b.data_ptr(), out.data_ptr(), stream)
     if rc != GEMM_TN_OK:
         raise GemmTnError(rc, "gemm_tn_host")
+    return out
+
+
+def flash_attn(q, k, v, causal=True, scale=None, out=None, status=None):
+    """Attention forward pass through flash_attn_fwd. q, k, v: contiguous CUDA
+    tensors [batch, seq, heads, head_dim] of one fp16/bf16 dtype (head_dim 64 or
+    128, 16-byte aligned); scale: the factor on Q.K (None: 1/sqrt(head_dim));
+    out: optional contiguous tensor of the same shape and dtype; status:
+    optional one-element int32 CUDA tensor for the device watchdog. Runs on the
+    current CUDA stream of q's device."""
+    import torch
+    if q.device.type != "cuda" or k.device != q.device or v.device != q.device:
+        raise ValueError("q, k and v must be CUDA tensors on one device")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must have the same dtype")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must have one shape [batch, seq, heads, head_dim]")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k and v must be contiguous")
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or out.device != q.device or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor with q's shape, dtype and device")
+    b, s, h, d = q.shape
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    d_status = status.data_ptr() if status is not None else None
+    with torch.cuda.device(q.device):
+        rc = flash_attn_fwd(_dtype_code(q), b, s, h, d, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            0.0 if scale is None else float(scale), causal, d_status, stream)
+    if rc != GEMM_TN_OK:
+        raise GemmTnError(rc, "flash_attn_fwd")
     return out

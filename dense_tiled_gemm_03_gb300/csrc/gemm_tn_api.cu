@@ -14,12 +14,14 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
 
+#include "../../include/flash_attn.h"
 #include "../../include/gemm_tn.h"
 #include "gemm_tn_internal.h"
 #include "sm103_gemm_kernel.cuh"
@@ -148,6 +150,30 @@ int encode_matrix_map(CUtensorMap* map, bool bf16, const void* ptr, int64_t rows
   const CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                             const_cast<void*>(ptr), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return fail(GEMM_TN_ERR_CUDA, buf);
+  }
+  return GEMM_TN_OK;
+}
+
+// [batch, seq, heads, dim] 16-bit array as a 3-D map {heads * dim, seq,
+// batch}, moved in boxes of {64, 128, 1} (128-byte rows, 128-byte swizzle);
+// rows past seq read as zero.
+int encode_bshd_map(CUtensorMap* map, bool bf16, const void* ptr, int64_t batch, int64_t seq, int64_t heads,
+                    int64_t dim) {
+  auto encode = encode_fn();
+  if (encode == nullptr) return fail(GEMM_TN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(heads * dim), static_cast<cuuint64_t>(seq),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(heads * dim * 2), static_cast<cuuint64_t>(seq * heads * dim * 2)};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  const CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                            const_cast<void*>(ptr), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[96];
     std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
@@ -785,6 +811,59 @@ int gemm_tn_host(int dtype, int64_t m, int64_t n, int64_t k, const void* a_host,
   check(es, "cudaStreamSynchronize");
   if (rc == GEMM_TN_OK && h_status != 0) rc = fail(h_status, "device watchdog expired");
   return rc;
+}
+
+int flash_attn_fwd(int dtype, int64_t batch, int64_t seq, int64_t heads, int64_t head_dim, const void* q,
+                   const void* k, const void* v, void* o, float softmax_scale, int causal, int* d_status,
+                   gemm_tn_stream_t stream) {
+  t_last_cuda_error = 0;
+  t_last_message[0] = '\0';
+  if (dtype != GEMM_TN_F16 && dtype != GEMM_TN_BF16) return fail(GEMM_TN_ERR_UNSUPPORTED_DTYPE, "dtype");
+  if (batch < 0 || seq < 0 || heads < 0) return fail(GEMM_TN_ERR_INVALID_VALUE, "negative size");
+  if (head_dim != 64 && head_dim != 128) return fail(GEMM_TN_ERR_INVALID_VALUE, "head_dim must be 64 or 128");
+  if (!(softmax_scale >= 0.0f) || !std::isfinite(softmax_scale))
+    return fail(GEMM_TN_ERR_INVALID_VALUE, "softmax_scale must be finite and non-negative");
+  if (batch == 0 || seq == 0 || heads == 0) return GEMM_TN_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return fail(GEMM_TN_ERR_INVALID_VALUE, "NULL pointer");
+  // one batch [seq, heads, dim] must stay under 2^39 bytes (tensor-map strides),
+  // and the grid and the kernel's indices under 2^31
+  const int64_t q_tiles = (seq + 127) / 128;
+  if (seq > kMaxDim || heads > kMaxDim || batch > kMaxDim || heads * head_dim > (int64_t{1} << 30) ||
+      seq * heads * head_dim > (int64_t{1} << 38) || batch * heads > kMaxDim || q_tiles * batch * heads > kMaxDim)
+    return fail(GEMM_TN_ERR_INVALID_VALUE, "sizes past the limits");
+  for (const void* p : {static_cast<const void*>(q), k, v, static_cast<const void*>(o)})
+    if (reinterpret_cast<uintptr_t>(p) % 16) return fail(GEMM_TN_ERR_MISALIGNED, "pointer not 16-byte aligned");
+  const uintptr_t bytes = static_cast<uintptr_t>(batch * seq * heads * head_dim * 2);
+  const uintptr_t o0 = reinterpret_cast<uintptr_t>(o);
+  for (const void* p : {q, k, v}) {
+    const uintptr_t p0 = reinterpret_cast<uintptr_t>(p);
+    if (ranges_overlap(o0, o0 + bytes, p0, p0 + bytes)) return fail(GEMM_TN_ERR_INVALID_VALUE, "O overlaps an input");
+  }
+  DeviceFacts* facts = nullptr;
+  int st = current_device(&facts);
+  if (st != GEMM_TN_OK) return st;
+
+  const bool bf16 = dtype == GEMM_TN_BF16;
+  gemm_tn_dev::FlashArgs args{};
+  if ((st = encode_bshd_map(&args.tmap_q, bf16, q, batch, seq, heads, head_dim)) != GEMM_TN_OK) return st;
+  if ((st = encode_bshd_map(&args.tmap_k, bf16, k, batch, seq, heads, head_dim)) != GEMM_TN_OK) return st;
+  if ((st = encode_bshd_map(&args.tmap_v, bf16, v, batch, seq, heads, head_dim)) != GEMM_TN_OK) return st;
+  const double scale = softmax_scale > 0.0f ? static_cast<double>(softmax_scale) : 1.0 / std::sqrt(static_cast<double>(head_dim));
+  args.o = o;
+  args.batch = static_cast<int>(batch);
+  args.seq = static_cast<int>(seq);
+  args.heads = static_cast<int>(heads);
+  args.num_q_tiles = static_cast<int>(q_tiles);
+  args.scale_log2 = static_cast<float>(scale * 1.4426950408889634);   // log2(e)
+  args.causal = causal != 0 ? 1 : 0;
+  args.status = d_status;
+  args.timeout_ns = watchdog_ns();
+  args.drop_load_block = test_drop_load_kb();
+  const unsigned grid = static_cast<unsigned>(q_tiles * batch * heads);
+  const cudaError_t e = launch_flash_attn(static_cast<int>(head_dim), bf16, args, grid,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "flash attention launch");
+  return GEMM_TN_OK;
 }
 
 int gemm_tn_select_config(int dtype, int64_t m, int64_t n, int64_t k) {

@@ -9,7 +9,22 @@
 
 namespace gemm_tn_dev {
 struct GemmArgs;
-}
+
+// Kernel arguments of the attention forward pass (sm103_flash_attn.cu).
+struct FlashArgs {
+  CUtensorMap tmap_q;   // 3-D {heads * dim, seq, batch} maps, boxes {64, 128, 1},
+  CUtensorMap tmap_k;   // 128-byte swizzle, zero fill past seq
+  CUtensorMap tmap_v;
+  void* o;              // [batch, seq, heads, dim], 16-byte aligned
+  int batch, seq, heads;
+  int num_q_tiles;      // ceil(seq / 128)
+  float scale_log2;     // softmax scale * log2(e), > 0
+  int causal;
+  int* status;          // optional device status word (watchdog)
+  uint64_t timeout_ns;
+  int drop_load_block;  // test hook: key tile whose K load the first CTA skips (-1: none)
+};
+}  // namespace gemm_tn_dev
 
 namespace gemm_tn_impl {
 
@@ -55,6 +70,11 @@ struct RepackRequest {
   int64_t rows;
   int64_t cols;
 };
+
+// Attention forward pass: one CTA per 128 queries of one (batch, head);
+// grid = num_q_tiles * batch * heads. head_dim 64 or 128.
+cudaError_t launch_flash_attn(int head_dim, bool bf16, const gemm_tn_dev::FlashArgs& args, unsigned grid,
+                              cudaStream_t stream);
 
 // One launch repacking up to two matrices (entries with rows <= 0 are skipped).
 cudaError_t launch_repack2(const RepackRequest* req, int num, int num_sms, cudaStream_t stream);

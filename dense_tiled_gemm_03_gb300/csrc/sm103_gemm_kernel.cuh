@@ -583,7 +583,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       int tm, tj;
       tile_coords(item.tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tj);
       const int tn = tj * Cfg::kClusterPairs + static_cast<int>(pair);
-      if (!wd.wait(acc_full_bar(acc), acc_phase)) break;
+      // warp-uniform outcome: the tcgen05 loads below are warp-collective
+      if (!__all_sync(0xffffffffu, wd.wait(acc_full_bar(acc), acc_phase))) break;
       tc_fence_after_sync();
       const int row0 = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM + static_cast<int>(quarter) * 32;
       const int col_tile = tn * Cfg::kBlockN + item.sub * (Cfg::kBlockN >> item.nsub_log2);
@@ -612,7 +613,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         last_contrib = sk_worker_of(args, (t_local + 1) * args.num_k_blocks - 1);
         for (int w = first_contrib; w <= last_contrib && ok; ++w) {
           const int cta = w * Cfg::kClusterSize + static_cast<int>(cluster_rank);
-          ok = wd.wait_flag(args.flags + cta * kNumEpilogueWarps + quarter);
+          ok = __all_sync(0xffffffffu, wd.wait_flag(args.flags + cta * kNumEpilogueWarps + quarter));
         }
         if (!ok) break;
       }

@@ -127,3 +127,41 @@ def test_fused_entry_validation(lib):
     ep = gt.GemmTnEpilogue(1.0, 0.0, None, 0, 1)
     assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, B - 40, 4, ep, None, None) == gt.GEMM_TN_ERR_INVALID_VALUE
     assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, C, 4, None, None, None) == gt.GEMM_TN_ERR_INVALID_VALUE
+
+
+# flash_attn_fwd (include/flash_attn.h): every argument error is reported
+# before any device call. Fake 16-byte-aligned addresses 1 MiB apart; one
+# [1, 128, 2, 64] array spans 32 KiB.
+QA, KA, VA, OA = 1 << 20, 2 << 20, 3 << 20, 4 << 20
+
+
+@pytest.mark.parametrize("args, expected", [
+    ((2, 1, 128, 2, 64, QA, KA, VA, OA, 0.0, 1), gt.GEMM_TN_ERR_UNSUPPORTED_DTYPE),
+    ((0, -1, 128, 2, 64, QA, KA, VA, OA, 0.0, 1), gt.GEMM_TN_ERR_INVALID_VALUE),
+    ((0, 1, 128, 2, 32, QA, KA, VA, OA, 0.0, 1), gt.GEMM_TN_ERR_INVALID_VALUE),      # head_dim
+    ((0, 1, 128, 2, 256, QA, KA, VA, OA, 0.0, 1), gt.GEMM_TN_ERR_INVALID_VALUE),
+    ((0, 1, 128, 2, 64, QA, KA, VA, OA, -0.5, 1), gt.GEMM_TN_ERR_INVALID_VALUE),     # scale
+    ((0, 1, 128, 2, 64, QA, KA, VA, OA, float("inf"), 1), gt.GEMM_TN_ERR_INVALID_VALUE),
+    ((0, 1, 128, 2, 64, QA, KA, VA, OA, float("nan"), 1), gt.GEMM_TN_ERR_INVALID_VALUE),
+    ((0, 1, 128, 2, 64, None, KA, VA, OA, 0.0, 1), gt.GEMM_TN_ERR_INVALID_VALUE),
+    ((1, 1, 128, 2, 64, QA, KA, VA, None, 0.0, 0), gt.GEMM_TN_ERR_INVALID_VALUE),
+    ((0, 1, 128, 2, 64, QA + 8, KA, VA, OA, 0.0, 1), gt.GEMM_TN_ERR_MISALIGNED),
+    ((0, 1, 128, 2, 64, QA, KA, VA, OA + 2, 0.0, 1), gt.GEMM_TN_ERR_MISALIGNED),
+    ((0, 1, 128, 2, 64, QA, KA, VA, VA + 32752, 0.0, 1), gt.GEMM_TN_ERR_INVALID_VALUE),   # O overlaps V's end
+    ((0, 1, 128, 2, 64, QA, KA, VA, QA - 16, 0.0, 1), gt.GEMM_TN_ERR_INVALID_VALUE),      # O overlaps Q's start
+    ((0, 1, 1 << 31, 2, 64, QA, KA, VA, OA, 0.0, 1), gt.GEMM_TN_ERR_INVALID_VALUE),       # seq too long
+    ((0, 1 << 20, 1 << 12, 1 << 10, 64, QA, KA, VA, OA, 0.0, 1), gt.GEMM_TN_ERR_INVALID_VALUE),  # grid too large
+])
+def test_flash_attn_validation_rejects_before_any_device_call(lib, args, expected):
+    assert gt.flash_attn_fwd(*args, None, None) == expected
+    assert gt.gemm_tn_last_error_message() != ""
+
+
+def test_flash_attn_empty_sizes_are_noops_and_adjacent_o_is_legal(lib):
+    for b, s, h in [(0, 128, 2), (1, 0, 2), (1, 128, 0)]:
+        assert gt.flash_attn_fwd(0, b, s, h, 64, None, None, None, None, 0.0, 1, None, None) == gt.GEMM_TN_OK
+    # V spans [VA, VA + 32768): O starting right after it passes validation
+    rc = gt.flash_attn_fwd(1, 1, 128, 2, 64, QA, KA, VA, VA + 32768, 0.0, 1, None, None)
+    assert rc in (gt.GEMM_TN_OK, gt.GEMM_TN_ERR_UNSUPPORTED_DEVICE, gt.GEMM_TN_ERR_CUDA)
+    if rc != gt.GEMM_TN_OK:
+        assert "overlaps" not in gt.gemm_tn_last_error_message()
