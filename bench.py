@@ -15,6 +15,10 @@ the work divided by the slowest rank's time.
 
 --impl reference times the CPU oracle (the only reference implementation of
 this path) on bounded samples of the same workload.
+
+--workload attn_* measures the attention forward pass (flash_attn_fwd) on one
+of the seeded [batch, seq, heads, dim] workloads instead, with the same line:
+TFLOP/s = 4 * batch * heads * (visible query-key pairs) * dim / device time.
 """
 from __future__ import annotations
 
@@ -32,6 +36,8 @@ if str(ROOT) not in sys.path:
     sys.path.insert(0, str(ROOT))
 
 METRIC = "TFLOP/s (2MNK/t) for C=A·Bᵀ bf16 8192³ on 1 GB300; % of dense tensor peak"
+ATTN_METRIC = ("TFLOP/s (4·B·H·visible pairs·D / t) for the attention forward pass "
+               "softmax(scale·QKᵀ, mask)·V on 1 GB300; % of dense tensor peak")
 L2_BYTES = 126 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # Algorithmic DRAM traffic per launch measured by ncu for the default workload
@@ -44,6 +50,10 @@ NCU_TRAFFIC_BYTES = {
     ("fp16_4096x4096x4096", "2cta_n256_mc"): 81_862_912 + 14_420_736,
     ("bf16_128x16384x16384", "1cta_n128"): 541_118_720 + 3_267_072,
     ("fp16_3001x5003x4097", "2cta_n256_mc"): 82_356_480 + 13_108_992,
+}
+# the same for the attention kernel, keyed by workload
+NCU_TRAFFIC_ATTN_BYTES: dict[str, int] = {
+    "attn_bf16_b2_s8192_h32_d128_causal": 3_672_053_760 + 116_816_384,
 }
 
 
@@ -319,6 +329,194 @@ def run_native(args, dist: Dist, peaks, peak_src):
     return line
 
 
+# ------------------------------------------------------------------ attention
+
+def attn_sample_rows(w, budget_flops: float) -> list[int]:
+    """Query rows spread over the sequence whose oracle work (all batches and
+    heads) stays near budget_flops."""
+    per_row = 4.0 * w.batch * w.heads * w.dim * ((w.seq + 1) / 2 if w.causal else w.seq)
+    n = int(max(1, min(w.seq, budget_flops / per_row)))
+    step = w.seq / n
+    return sorted({min(w.seq - 1, int(i * step + step / 2)) for i in range(n)})
+
+
+def attn_rows_flops(w, rows) -> float:
+    return sum(4.0 * w.batch * w.heads * w.dim * ((r + 1) if w.causal else w.seq) for r in rows)
+
+
+def cpu_oracle_attn_rate(w, q, k, v, seconds: float):
+    """Time the fp64 attention oracle on a bounded sample of query rows;
+    returns (TFLOP/s, cores, description)."""
+    import oracle
+    cores = oracle.host_threads()
+    probe = attn_sample_rows(w, 2e9)
+    t0 = time.perf_counter()
+    oracle.attention_reference(q, k, v, causal=w.causal, rows=probe)
+    dt = time.perf_counter() - t0
+    rate = attn_rows_flops(w, probe) / max(dt, 1e-6)
+    rows = attn_sample_rows(w, rate * seconds)
+    t0 = time.perf_counter()
+    oracle.attention_reference(q, k, v, causal=w.causal, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = attn_rows_flops(w, rows)
+    return flops / dt / 1e12, cores, (f"{len(rows)} of {w.seq} query rows spread over the sequence, every batch "
+                                      f"and head, {dt:.1f} s")
+
+
+def run_native_attn(args, dist: Dist, peaks, peak_src):
+    import torch
+    import dense_tiled_gemm_03_gb300 as gt
+    from dense_tiled_gemm_03_gb300 import build as native_build
+    from dense_tiled_gemm_03_gb300.workloads import ATTN_WORKLOADS, make_qkv
+
+    if dist.rank == 0 or not native_build.LIBRARY.exists():
+        native_build.build()
+    dist.barrier()
+    w = ATTN_WORKLOADS[args.workload]
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    q_cpu, k_cpu, v_cpu = make_qkv(w.batch, w.seq, w.heads, w.dim, w.dtype, seed=w.seed)
+    q, k, v = q_cpu.to(dev), k_cpu.to(dev), v_cpu.to(dev)
+    o = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    tensor_bytes = q.numel() * 2
+    io_bytes = 4 * tensor_bytes   # Q, K, V read once, O written once
+    flush = io_bytes < 2 * L2_BYTES
+    scratch = torch.empty(L2_BYTES * 2 // 4, dtype=torch.int32, device=dev) if flush else None
+
+    def step():
+        gt.flash_attn(q, k, v, causal=w.causal, out=o, status=status)
+
+    for _ in range(args.warmup):
+        if flush:
+            scratch.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_smi_id(dev))
+    if dist.rank == 0:
+        sampler.start()
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    region0.record(stream)
+    for i in range(args.steps):
+        if flush:
+            scratch.fill_(1)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    region1.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clocks = sampler.stop() if dist.rank == 0 else None
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device watchdog fired: {gt.gemm_tn_status_string(int(status.item()))}")
+    avg_launch_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+    step_ms = avg_launch_ms if flush else region0.elapsed_time(region1) / args.steps
+    step_ms = dist.max(step_ms)
+    avg_launch_ms = dist.max(avg_launch_ms)
+    value = dist.world * w.flops / (step_ms * 1e-3) / 1e12
+    tensor_peak = float(peaks["bf16_tflops"])
+    achieved = w.flops / (avg_launch_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": round(achieved / tensor_peak, 4),
+                "frac_of_sustained": round(achieved / float(peaks.get("bf16_tflops_sustained", tensor_peak)), 4),
+                "traffic": NCU_TRAFFIC_ATTN_BYTES.get(w.name), "algorithmic_bytes": io_bytes,
+                "peak_source": f"{peak_src} (bf16_tflops burst; kernel timed alone)",
+                "kernel": f"flash_attn_fwd_kernel<dim {w.dim}, {w.dtype}>"}
+
+    # end to end: pinned host Q, K, V in, O back to pinned host memory, each step
+    pins = [t.pin_memory() for t in (q_cpu, k_cpu, v_cpu)]
+    pin_o = torch.empty_like(q_cpu).pin_memory()
+    dq, dk, dv, do = (torch.empty_like(q) for _ in range(4))
+
+    def e2e_step():
+        for dst, src in zip((dq, dk, dv), pins):
+            dst.copy_(src, non_blocking=True)
+        gt.flash_attn(dq, dk, dv, causal=w.causal, out=do, status=status)
+        pin_o.copy_(do, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    e2e_step()
+    dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e2e_s = dist.max((time.perf_counter() - t0) / args.e2e_steps)
+    e2e = {"value": round(dist.world * w.flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": 3 * tensor_bytes, "d2h_bytes_per_step": tensor_bytes, "steps": args.e2e_steps,
+           "entry_point": "flash_attn_fwd with pinned host copies on the same stream"}
+    line = {
+        "metric": ATTN_METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": dist.world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seq": w.seq, "heads": w.heads, "dim": w.dim,
+                   "causal": w.causal, "seed": w.seed,
+                   "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU",
+                   "l2": "L2 flushed between launches" if flush else
+                   f"inputs larger than L2 ({io_bytes / 1e6:.0f} MB of Q, K, V and O vs {L2_BYTES / 1e6:.0f} MB)",
+                   "accumulate": "fp32"},
+        "pct_of_peak": round(100 * achieved / tensor_peak, 2),
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        rate, cores, sample = cpu_oracle_attn_rate(w, q_cpu, k_cpu, v_cpu, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(rate, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    return line
+
+
+def run_reference_attn(args, dist: Dist):
+    """The attention oracle as it stands, on bounded row samples per step."""
+    from dense_tiled_gemm_03_gb300.workloads import ATTN_WORKLOADS, make_qkv
+    import oracle
+
+    w = ATTN_WORKLOADS[args.workload]
+    q, k, v = make_qkv(w.batch, w.seq, w.heads, w.dim, w.dtype, seed=w.seed)
+    cores = oracle.host_threads()
+    total = args.steps + args.warmup
+    probe = attn_sample_rows(w, 2e9)
+    t0 = time.perf_counter()
+    oracle.attention_reference(q, k, v, causal=w.causal, rows=probe)
+    rate = attn_rows_flops(w, probe) / max(time.perf_counter() - t0, 1e-6)
+    rows = attn_sample_rows(w, rate * args.ref_seconds / total)
+    for _ in range(args.warmup):
+        oracle.attention_reference(q, k, v, causal=w.causal, rows=rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention_reference(q, k, v, causal=w.causal, rows=rows)
+    dt = time.perf_counter() - t0
+    value = args.steps * attn_rows_flops(w, rows) / dt / 1e12
+    sample = f"{len(rows)} of {w.seq} query rows per step (every batch and head) of {w.name}"
+    return {
+        "impl": "reference", "metric": ATTN_METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seq": w.seq, "heads": w.heads, "dim": w.dim,
+                   "causal": w.causal, "seed": w.seed},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, dist: Dist):
@@ -379,12 +577,14 @@ def main():
         raise SystemExit("--gpus must be >= 1")
     dist = Dist()
     try:
+        attn = args.workload.startswith("attn_")
         if args.impl == "reference":
             if dist.rank == 0:
-                print(json.dumps(run_reference(args, dist)), flush=True)
+                line = run_reference_attn(args, dist) if attn else run_reference(args, dist)
+                print(json.dumps(line), flush=True)
             return
         peaks, src = load_peaks()
-        line = run_native(args, dist, peaks, src)
+        line = run_native_attn(args, dist, peaks, src) if attn else run_native(args, dist, peaks, src)
         if dist.rank == 0:
             print(json.dumps(line), flush=True)
     finally:
