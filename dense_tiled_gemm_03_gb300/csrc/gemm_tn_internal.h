@@ -18,6 +18,7 @@ struct FlashArgs {
   void* o;              // [batch, seq, heads, dim], 16-byte aligned
   int batch, seq, heads;
   int num_q_tiles;      // ceil(seq / 128)
+  int head_group;       // (batch, head) pairs whose query tiles run interleaved
   float scale_log2;     // softmax scale * log2(e), > 0
   int causal;
   int* status;          // optional device status word (watchdog)
@@ -72,9 +73,10 @@ struct RepackRequest {
 };
 
 // Attention forward pass: one CTA per 128 queries of one (batch, head);
-// grid = num_q_tiles * batch * heads. head_dim 64 or 128.
-cudaError_t launch_flash_attn(int head_dim, bool bf16, const gemm_tn_dev::FlashArgs& args, unsigned grid,
-                              cudaStream_t stream);
+// grid = num_q_tiles * batch * heads. head_dim 64 or 128; splits = softmax
+// warp groups sharing each row (2 or 4).
+cudaError_t launch_flash_attn(int head_dim, bool bf16, int splits, const gemm_tn_dev::FlashArgs& args,
+                              unsigned grid, cudaStream_t stream);
 
 // One launch repacking up to two matrices (entries with rows <= 0 are skipped).
 cudaError_t launch_repack2(const RepackRequest* req, int num, int num_sms, cudaStream_t stream);
