@@ -276,14 +276,6 @@ int test_drop_load_kb() {
   return (end != s && v >= 0 && v < INT32_MAX) ? static_cast<int>(v) : -1;
 }
 
-// Softmax warp groups per query row of the attention kernel (2 or 4);
-// GEMM_TN_FA_SPLITS overrides the default of 2 (for measurement).
-int flash_attn_splits() {
-  const char* s = std::getenv("GEMM_TN_FA_SPLITS");
-  if (s != nullptr && std::strcmp(s, "4") == 0) return 4;
-  return 2;
-}
-
 uint64_t watchdog_ns() {
   const char* s = std::getenv("GEMM_TN_WATCHDOG_MS");
   long ms = 4000;
@@ -835,7 +827,7 @@ int flash_attn_fwd(int dtype, int64_t batch, int64_t seq, int64_t heads, int64_t
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return fail(GEMM_TN_ERR_INVALID_VALUE, "NULL pointer");
   // one batch [seq, heads, dim] must stay under 2^39 bytes (tensor-map strides),
   // and the grid and the kernel's indices under 2^31
-  const int64_t q_tiles = (seq + 127) / 128;
+  const int64_t q_tiles = (seq + flash_attn_rows_per_cta() - 1) / flash_attn_rows_per_cta();   // CTAs per head
   if (seq > kMaxDim || heads > kMaxDim || batch > kMaxDim || heads * head_dim > (int64_t{1} << 30) ||
       seq * heads * head_dim > (int64_t{1} << 38) || batch * heads > kMaxDim || q_tiles * batch * heads > kMaxDim)
     return fail(GEMM_TN_ERR_INVALID_VALUE, "sizes past the limits");
@@ -872,7 +864,7 @@ int flash_attn_fwd(int dtype, int64_t batch, int64_t seq, int64_t heads, int64_t
   const int64_t kv_bytes = 2 * seq * head_dim * 2;
   args.head_group = static_cast<int>(std::min<int64_t>(batch * heads, std::max<int64_t>(1, (48ll << 20) / kv_bytes)));
   const unsigned grid = static_cast<unsigned>(q_tiles * batch * heads);
-  const cudaError_t e = launch_flash_attn(static_cast<int>(head_dim), bf16, flash_attn_splits(), args, grid,
+  const cudaError_t e = launch_flash_attn(static_cast<int>(head_dim), bf16, args, grid,
                                           reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "flash attention launch");
   return GEMM_TN_OK;

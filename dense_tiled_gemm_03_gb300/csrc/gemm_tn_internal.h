@@ -17,7 +17,7 @@ struct FlashArgs {
   CUtensorMap tmap_v;
   void* o;              // [batch, seq, heads, dim], 16-byte aligned
   int batch, seq, heads;
-  int num_q_tiles;      // ceil(seq / 128)
+  int num_q_tiles;      // CTAs per (batch, head): ceil(seq / flash_attn_rows_per_cta())
   int head_group;       // (batch, head) pairs whose query tiles run interleaved
   float scale_log2;     // softmax scale * log2(e), > 0
   int causal;
@@ -72,11 +72,11 @@ struct RepackRequest {
   int64_t cols;
 };
 
-// Attention forward pass: one CTA per 128 queries of one (batch, head);
-// grid = num_q_tiles * batch * heads. head_dim 64 or 128; splits = softmax
-// warp groups sharing each row (2 or 4).
-cudaError_t launch_flash_attn(int head_dim, bool bf16, int splits, const gemm_tn_dev::FlashArgs& args,
-                              unsigned grid, cudaStream_t stream);
+// Attention forward pass: one CTA per flash_attn_rows_per_cta() queries of
+// one (batch, head); grid = num_q_tiles * batch * heads. head_dim 64 or 128.
+int flash_attn_rows_per_cta();
+cudaError_t launch_flash_attn(int head_dim, bool bf16, const gemm_tn_dev::FlashArgs& args, unsigned grid,
+                              cudaStream_t stream);
 
 // One launch repacking up to two matrices (entries with rows <= 0 are skipped).
 cudaError_t launch_repack2(const RepackRequest* req, int num, int num_sms, cudaStream_t stream);
