@@ -68,3 +68,32 @@ def test_reference_arm_single_process():
     line = json.loads(res.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["n_gpus"] == 1
     assert line["config"]["workload"] == "fp16_256x256x256"
+
+
+def test_reference_arm_attention_workload():
+    """--workload attn_* times the attention oracle on a bounded row sample and
+    prints the same line with the attention metric."""
+    cmd = [sys.executable, str(ROOT / "bench.py"), "--impl", "reference", "--steps", "2", "--warmup", "1",
+           "--workload", "attn_fp16_b1_s1024_h8_d64_causal", "--ref-seconds", "2"]
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-3000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["config"]["workload"] == "attn_fp16_b1_s1024_h8_d64_causal" and line["config"]["causal"] is True
+    assert "attention" in line["metric"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_attention_row_sample_and_flop_count():
+    """The oracle samples' FLOP count is the visible-pair count of the rows."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", ROOT / "bench.py")
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    from dense_tiled_gemm_03_gb300.workloads import ATTN_WORKLOADS
+    w = ATTN_WORKLOADS["attn_fp16_b1_s1024_h8_d64_causal"]
+    rows = bench.attn_sample_rows(w, 1e18)
+    assert rows == list(range(w.seq))
+    assert bench.attn_rows_flops(w, rows) == w.flops
+    few = bench.attn_sample_rows(w, w.flops / 10)
+    assert 0 < len(few) < w.seq and few == sorted(set(few))
