@@ -43,10 +43,11 @@
 // old maximum (values up to 2^8, exact in fp16 and bf16 range). The result is
 // the same softmax -- the final division uses the same reference for the
 // numerator and the row sum -- with far fewer O rescales. After the first key
-// tile the probabilities are computed against the current reference at once,
-// with the tile's maximum taken in the same pass; only a warp in which a row's
-// maximum moved computes them again. That takes the separate pass over the
-// scores for their maximum off the path between the two products.
+// tile the probabilities are computed against the current reference at once;
+// since none of them can exceed 2^8 unless their sum does, the tile's maximum
+// is only taken when the row sum passes 2^8, and only a warp in which a row's
+// maximum moved computes them again. That keeps the pass over the scores for
+// their maximum off the path between the two products.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -397,21 +398,15 @@ __global__ void __launch_bounds__(C::kNumThreads) __maxnreg__(C::kMaxRegs)
         for (int e = 0; e < 128; ++e)
           if (key0 + e >= limit) sv[e] = -INFINITY;
       }
-      // probabilities against neg_m into the P columns; returns their sum and
-      // the scores' maximum
-      auto exp_pass = [&](float neg_m, float& mx) {
+      // probabilities against neg_m into the P columns; returns their sum
+      auto exp_pass = [&](float neg_m) {
         float sum0 = 0.0f, sum1 = 0.0f, sum2 = 0.0f, sum3 = 0.0f;
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];   // 32 scores -> 16 columns of P
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             const float* x = sv + 32 * c + e;
-            mx0 = fmaxf(mx0, x[0]);
-            mx1 = fmaxf(mx1, x[1]);
-            mx2 = fmaxf(mx2, x[2]);
-            mx3 = fmaxf(mx3, x[3]);
             const float p0 = ex2_approx(fmaf(x[0], c_log2, neg_m));
             const float p1 = ex2_approx(fmaf(x[1], c_log2, neg_m));
             const float p2 = ex2_approx(fmaf(x[2], c_log2, neg_m));
@@ -425,13 +420,9 @@ __global__ void __launch_bounds__(C::kNumThreads) __maxnreg__(C::kMaxRegs)
           }
           tmem_store_32x16(p_col(32 * c), pk);
         }
-        mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
         return (sum0 + sum1) + (sum2 + sum3);
       };
-      float alpha = 1.0f;
-      float sum;
-      if (j == 0) {
-        // first tile: the reference maximum is the tile's maximum
+      auto row_max = [&]() {
         float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
         for (int e = 4; e < 128; e += 4) {
@@ -440,25 +431,31 @@ __global__ void __launch_bounds__(C::kNumThreads) __maxnreg__(C::kMaxRegs)
           mx2 = fmaxf(mx2, sv[e + 2]);
           mx3 = fmaxf(mx3, sv[e + 3]);
         }
-        m_ref = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c_log2;
-        float unused;
-        sum = exp_pass(-m_ref, unused);
+        return fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      };
+      float alpha = 1.0f;
+      float sum;
+      if (j == 0) {
+        // first tile: the reference maximum is the tile's maximum
+        m_ref = row_max() * c_log2;
+        sum = exp_pass(-m_ref);
       } else {
-        // against the current reference; again only where a row's maximum
-        // moved past it by more than the threshold (every thread of the warp
-        // takes part: the P stores are warp-collective)
-        float mx;
-        sum = exp_pass(-m_ref, mx);
-        const float m_tile = mx * c_log2;
-        const bool move = m_tile > m_ref + fa::kRescaleThreshold;
-        if (__any_sync(0xffffffffu, move)) {
-          if (move) {
-            alpha = ex2_approx(m_ref - m_tile);
-            m_ref = m_tile;
+        // against the current reference at once. No probability exceeds 2^8
+        // unless the row sum does, so only then is the tile's maximum taken;
+        // where it moved past the threshold the warp computes the tile again
+        // (every thread takes part: the P stores are warp-collective)
+        sum = exp_pass(-m_ref);
+        if (__any_sync(0xffffffffu, !(sum <= 256.0f))) {
+          const float m_tile = row_max() * c_log2;
+          const bool move = m_tile > m_ref + fa::kRescaleThreshold;
+          if (__any_sync(0xffffffffu, move)) {
+            if (move) {
+              alpha = ex2_approx(m_ref - m_tile);
+              m_ref = m_tile;
+            }
+            tmem_store_wait();   // the first pass's stores land before they are overwritten
+            sum = exp_pass(-m_ref);
           }
-          tmem_store_wait();   // the first pass's stores land before they are overwritten
-          float unused;
-          sum = exp_pass(-m_ref, unused);
         }
       }
       l = l * alpha + sum;
