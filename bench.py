@@ -70,6 +70,9 @@ def parse_args():
     ap.add_argument("--config", default=None, help="force a kernel configuration (GEMM_TN_FORCE_CONFIG)")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="budget of the whole --impl reference run (oracle work)")
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="instead of the benchmark line: time the CPU oracle on every GEMM workload, with all "
+                         "host threads and with one thread (one JSON line per workload and thread count)")
     return ap.parse_args()
 
 
@@ -194,6 +197,45 @@ def cpu_oracle_rate(a, b, seconds: float):
         rows = target_rows
     flops = 2.0 * rows * n * k
     return flops / dt / 1e12, cores, f"first {rows} of {m} rows of C (all {n} columns, K={k}), {dt:.1f} s"
+
+
+def oracle_table():
+    """The CPU baseline per GEMM workload on this host: the fp64 oracle with
+    every host thread on a row sample of about 10 s, and with one thread on the
+    whole product for the two smallest workloads or on a 256-row slice (the
+    rate extrapolated to the whole product, labelled as such) for the others."""
+    import platform
+    import oracle
+    from dense_tiled_gemm_03_gb300.workloads import WORKLOADS, workload_operands
+    cpu = platform.processor() or platform.machine()
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                cpu = ln.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    for name, w in WORKLOADS.items():
+        a, b = workload_operands(w)
+        for threads in (oracle.host_threads(), 1):
+            if threads == 1 and w.m * w.n * w.k <= 4096 ** 3:
+                rows, how = w.m, "whole product"
+            elif threads == 1:
+                rows, how = min(w.m, 256), f"first {min(w.m, 256)} rows, rate extrapolated to the whole product"
+            else:
+                rows = max(1, min(w.m, threads))
+                t0 = time.perf_counter()
+                oracle.gemm_tn_reference(a[:rows], b, nthreads=threads)
+                per_row = (time.perf_counter() - t0) / rows
+                rows = int(min(w.m, max(rows, 10.0 / max(per_row, 1e-9))))
+                how = "whole product" if rows == w.m else f"first {rows} rows, rate extrapolated to the whole product"
+            t0 = time.perf_counter()
+            oracle.gemm_tn_reference(a[:rows], b, nthreads=threads)
+            dt = time.perf_counter() - t0
+            flops = 2.0 * rows * w.n * w.k
+            print(json.dumps({"oracle_table": name, "threads": threads, "cpu": cpu, "sample": how,
+                              "seconds": round(dt, 3), "gflops": round(flops / dt / 1e9, 3),
+                              "seconds_whole_product": round(dt * w.m / rows, 2)}), flush=True)
 
 
 # ------------------------------------------------------------------ native arm
@@ -575,6 +617,9 @@ def main():
         os.environ["GEMM_TN_FORCE_CONFIG"] = args.config
     if args.gpus < 1:
         raise SystemExit("--gpus must be >= 1")
+    if args.oracle_table:
+        oracle_table()
+        return
     dist = Dist()
     try:
         attn = args.workload.startswith("attn_")

@@ -202,3 +202,41 @@ def test_runs_on_the_callers_stream_and_in_a_graph():
     g.replay()
     torch.cuda.synchronize()
     assert_attn_parity(out.cpu(), q_cpu, k_cpu, v_cpu, True, label="graph replay")
+
+
+def test_long_sequence_sampled():
+    """seq = 32768 (256 key tiles, 128 query units per head), one head group;
+    checked on sampled rows, including the last ones (they walk every key)."""
+    b, s, h, d = 1, 32768, 2, 128
+    q, k, v = make_qkv(b, s, h, d, "bf16", seed=16)
+    o, st = run_flash(q, k, v, True)
+    assert st == 0
+    rows = sorted({0, 127, 128, 255, 256, 16383, 16384, s - 129, s - 128, s - 2, s - 1} |
+                  set(np.random.Generator(np.random.PCG64(16)).integers(0, s, size=12).tolist()))
+    assert_attn_parity(o, q, k, v, True, rows=rows, label="seq 32768")
+
+
+def test_concurrent_with_a_gemm_on_another_stream():
+    """Attention and a GEMM launched on two streams at once (both kernels use
+    all of an SM's tensor memory); both results are correct."""
+    from dense_tiled_gemm_03_gb300.workloads import make_operands
+    dev = torch.device("cuda", 0)
+    q_cpu, k_cpu, v_cpu = make_qkv(2, 2048, 4, 128, "bf16", seed=17)
+    a_cpu, b_cpu = make_operands(1536, 2560, 1024, "bf16", "uniform", seed=17)
+    q, k, v = q_cpu.to(dev), k_cpu.to(dev), v_cpu.to(dev)
+    a, b_ = a_cpu.to(dev), b_cpu.to(dev)
+    o = torch.full_like(q, float("nan"))
+    c = torch.full((1536, 2560), float("nan"), dtype=torch.bfloat16, device=dev)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            gt.flash_attn(q, k, v, causal=True, out=o)
+        with torch.cuda.stream(s2):
+            gt.mm_tn(a, b_, out=c)
+    torch.cuda.synchronize()
+    assert_attn_parity(o.cpu(), q_cpu, k_cpu, v_cpu, True,
+                       rows=list(range(0, 2048, 97)) + [2047], label="concurrent attention")
+    ref, bound = oracle.gemm_tn_reference(a_cpu, b_cpu)
+    rep = oracle.parity_report(c.cpu(), ref, bound)
+    assert rep.ok, rep
