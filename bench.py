@@ -209,11 +209,9 @@ def oracle_table():
     from dense_tiled_gemm_03_gb300.workloads import WORKLOADS, workload_operands
     cpu = platform.processor() or platform.machine()
     try:
-        for ln in open("/proc/cpuinfo"):
-            if ln.lower().startswith(("model name", "cpu part")):
-                cpu = ln.split(":", 1)[1].strip()
-                break
-    except OSError:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        cpu = next((ln.split(":", 1)[1].strip() for ln in out.splitlines() if ln.startswith("Model name")), cpu)
+    except (OSError, subprocess.SubprocessError):
         pass
     for name, w in WORKLOADS.items():
         a, b = workload_operands(w)
