@@ -70,6 +70,9 @@ def parse_args():
     ap.add_argument("--config", default=None, help="force a kernel configuration (GEMM_TN_FORCE_CONFIG)")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="budget of the whole --impl reference run (oracle work)")
+    ap.add_argument("--cublas-context", action="store_true",
+                    help="also time torch.matmul(a, b.T) (cuBLAS) on the same operands, the same way, and add it "
+                         "to the line as context (not part of the product)")
     ap.add_argument("--oracle-table", action="store_true",
                     help="instead of the benchmark line: time the CPU oracle on every GEMM workload, with all "
                          "host threads and with one thread (one JSON line per workload and thread count)")
@@ -362,6 +365,29 @@ def run_native(args, dist: Dist, peaks, peak_src):
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
     }
+    if args.cublas_context:
+        # the same operands through torch.matmul (cuBLAS), timed the same way
+        ref_c = torch.empty_like(c)
+        for _ in range(args.warmup):
+            if flush:
+                scratch.fill_(1)
+            torch.matmul(a, b.t(), out=ref_c)
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(args.steps):
+            if flush:
+                scratch.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            torch.matmul(a, b.t(), out=ref_c)
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        ms = sum(x.elapsed_time(y) for x, y in times) / len(times)
+        line["context"] = {"cublas_tflops": round(w.flops / (ms * 1e-3) / 1e12, 2),
+                           "ratio_to_cublas": round(roofline["achieved"] / (w.flops / (ms * 1e-3) / 1e12), 4)
+                           if roofline["unit"] == "TFLOP/s" else None,
+                           "what": "torch.matmul(a, b.T) on the same operands, per-launch CUDA events"}
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_rate(a_cpu, b_cpu, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
