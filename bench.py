@@ -285,9 +285,10 @@ def run_native(args, dist: Dist, peaks, peak_src):
     for i in range(args.steps):
         if flush:
             scratch.fill_(1)   # write a buffer larger than L2 between timed launches
-        starts[i].record(stream)
+            starts[i].record(stream)
         step()
-        ends[i].record(stream)
+        if flush:
+            ends[i].record(stream)
     region1.record(stream)
     torch.cuda.synchronize(dev)
     dist.barrier()
@@ -295,12 +296,14 @@ def run_native(args, dist: Dist, peaks, peak_src):
     if int(status.item()) != 0:
         raise RuntimeError(f"device watchdog fired: {gt.gemm_tn_status_string(int(status.item()))}")
 
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    avg_launch_ms = sum(launch_ms) / len(launch_ms)
     region_ms = region0.elapsed_time(region1)
-    # with an L2 flush between launches the region includes the flushes: take
-    # the step time from the launches themselves
-    step_ms = avg_launch_ms if flush else region_ms / args.steps
+    # With an L2 flush between launches the region includes the flushes: the
+    # step time comes from events around each launch. Otherwise the launches
+    # run back to back between the region's two events (events between
+    # launches would add their own gaps).
+    avg_launch_ms = (sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps if flush
+                     else region_ms / args.steps)
+    step_ms = avg_launch_ms
     step_ms = dist.max(step_ms)
     avg_launch_ms = dist.max(avg_launch_ms)
     value = dist.world * w.flops / (step_ms * 1e-3) / 1e12
@@ -374,20 +377,25 @@ def run_native(args, dist: Dist, peaks, peak_src):
             torch.matmul(a, b.t(), out=ref_c)
         torch.cuda.synchronize(dev)
         times = []
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
         for _ in range(args.steps):
             if flush:
                 scratch.fill_(1)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
             torch.matmul(a, b.t(), out=ref_c)
-            e1.record(stream)
-            times.append((e0, e1))
+            if flush:
+                e1.record(stream)
+                times.append((e0, e1))
+        r1.record(stream)
         torch.cuda.synchronize(dev)
-        ms = sum(x.elapsed_time(y) for x, y in times) / len(times)
-        line["context"] = {"cublas_tflops": round(w.flops / (ms * 1e-3) / 1e12, 2),
-                           "ratio_to_cublas": round(roofline["achieved"] / (w.flops / (ms * 1e-3) / 1e12), 4)
-                           if roofline["unit"] == "TFLOP/s" else None,
-                           "what": "torch.matmul(a, b.T) on the same operands, per-launch CUDA events"}
+        ms = (sum(x.elapsed_time(y) for x, y in times) / len(times) if flush
+              else r0.elapsed_time(r1) / args.steps)
+        cublas_tflops = w.flops / (ms * 1e-3) / 1e12
+        line["context"] = {"cublas_tflops": round(cublas_tflops, 2),
+                           "ratio_to_cublas": round(w.flops / (avg_launch_ms * 1e-3) / 1e12 / cublas_tflops, 4),
+                           "what": "torch.matmul(a, b.T) on the same operands, timed the same way"}
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_rate(a_cpu, b_cpu, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
@@ -472,17 +480,19 @@ def run_native_attn(args, dist: Dist, peaks, peak_src):
     for i in range(args.steps):
         if flush:
             scratch.fill_(1)
-        starts[i].record(stream)
+            starts[i].record(stream)
         step()
-        ends[i].record(stream)
+        if flush:
+            ends[i].record(stream)
     region1.record(stream)
     torch.cuda.synchronize(dev)
     dist.barrier()
     clocks = sampler.stop() if dist.rank == 0 else None
     if int(status.item()) != 0:
         raise RuntimeError(f"device watchdog fired: {gt.gemm_tn_status_string(int(status.item()))}")
-    avg_launch_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
-    step_ms = avg_launch_ms if flush else region0.elapsed_time(region1) / args.steps
+    avg_launch_ms = (sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps if flush
+                     else region0.elapsed_time(region1) / args.steps)
+    step_ms = avg_launch_ms
     step_ms = dist.max(step_ms)
     avg_launch_ms = dist.max(avg_launch_ms)
     value = dist.world * w.flops / (step_ms * 1e-3) / 1e12

@@ -377,6 +377,20 @@ int stream_k_mode() {
   return 0;
 }
 
+// K rotation and evict-first B loads for problems with one row of tiles.
+// There every tile streams its own rows of B once (an intensity of at most
+// ~M FLOP/B, under the ridge), and with all tiles at the same K offset the
+// concurrent reads, a row pitch apart, crowd few DRAM banks: bf16 128 x 16384
+// x 16384 measured 5.43 TB/s in the plain order and 5.94 TB/s rotated. With
+// several rows of tiles the grouped raster wants tiles to read shared rows of
+// A and B at the same time, so the order stays plain. GEMM_TN_K_ROTATE=0/1
+// overrides the choice (tests and experiments).
+bool k_rotation_on(int64_t num_m_tiles) {
+  const char* s = std::getenv("GEMM_TN_K_ROTATE");
+  if (s != nullptr && *s != '\0') return std::strcmp(s, "0") != 0;
+  return num_m_tiles == 1;
+}
+
 // Tile rows per rasterization group: tiles in flight together then share
 // about 2048 rows of A and the matching columns of B in L2.
 // GEMM_TN_GROUP_M overrides it (tuning experiments).
@@ -549,6 +563,9 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   args.split_log2 = split == 4 ? 2 : (split == 2 ? 1 : 0);
   args.split_begin = static_cast<int32_t>(split_begin);
   args.dp_units = static_cast<int32_t>(split_begin + (plan.dp_tiles - split_begin) * split);
+  // one row of tiles: B streams from HBM once and A is re-read from L2
+  args.k_rotate = k_rotation_on(num_m_tiles) ? 1 : 0;
+  args.b_evict_first = args.k_rotate;
   if (fused != nullptr) {
     args.alpha = fused->alpha;
     args.beta = fused->beta;

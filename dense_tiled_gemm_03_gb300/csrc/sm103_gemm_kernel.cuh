@@ -87,6 +87,12 @@ struct GemmArgs {
   int32_t out_f32;
   float* partials;        // per CTA: block_n / 32 chunks x 128 rows x 32 fp32 (stream-K only)
   int* flags;             // per CTA and epilogue warp: 1 once its partial rows are written (zeroed by the host)
+  // Memory-bound problems with one row of tiles (B streamed once, A re-read
+  // from L2): k_rotate != 0 starts every tile that covers all of K at its
+  // own k-block (k_start) and wraps around, and b_evict_first marks the B
+  // loads evict-first in L2.
+  int32_t k_rotate;
+  int32_t b_evict_first;
 };
 
 template <int kCtaGroup_, int kBlockN_, int kStages_, bool kBf16_, int kClusterPairs_ = 1, bool kBMnMajor_ = false,
@@ -251,6 +257,26 @@ struct WorkCursor {
   }
 };
 
+// First k-block of a rotated K walk for tile column `tile_col` (0 when the
+// item does not cover all of K or rotation is off). Tile columns are spread
+// over K by Fibonacci hashing (the fractional part of tile_col x 0.618...),
+// so the tiles streaming their rows of B at the same time read different K
+// offsets: rows of B lie a whole row pitch apart, and when every tile reads
+// the same offset the concurrent reads fall on few DRAM banks. Tiles of one
+// column (which share rows of B) start at the same k-block. The producer
+// loads k-block rotate_kb(i) as the i-th of the item and the MMA consumes the
+// ring in order, so C is the same sum up to the order of fp32 additions.
+__device__ __forceinline__ int k_start(const GemmArgs& a, const WorkItem& w, int tile_col) {
+  if (a.k_rotate == 0 || w.kb_begin != 0 || w.kb_end != a.num_k_blocks) return 0;
+  const uint32_t h = static_cast<uint32_t>(tile_col) * 0x9E3779B9u;
+  return static_cast<int>((static_cast<uint64_t>(h) * static_cast<uint32_t>(a.num_k_blocks)) >> 32);
+}
+
+__device__ __forceinline__ int rotate_kb(int kb, int start, int num_k_blocks) {
+  const int r = kb + start;
+  return r >= num_k_blocks ? r - num_k_blocks : r;
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -394,6 +420,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
   if (warp == kProducerWarp) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA producer
+      const uint64_t pol_b = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       int issued_phase_of[Cfg::kStages];
@@ -428,17 +455,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             }
           } else if constexpr (Cfg::kCtaGroup == 2) {
             tma_load_2d_pair(tmap_b, b_tile(stage_), bar, kb_ * Cfg::kBlockK, b_row);
+          } else if (args.b_evict_first) {
+            tma_load_2d_hint(tmap_b, b_tile(stage_), bar, kb_ * Cfg::kBlockK, b_row, pol_b);
           } else {
             tma_load_2d(tmap_b, b_tile(stage_), bar, kb_ * Cfg::kBlockK, b_row);
           }
         };
-        for (int kb = item.kb_begin; kb < item.kb_end; ++kb) {
+        const int kstart = k_start(args, item, tj);
+        for (int kb_i = item.kb_begin; kb_i < item.kb_end; ++kb_i) {
           if (!wd.wait(empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
           }
+          const int kb = rotate_kb(kb_i, kstart, args.num_k_blocks);
           const uint32_t fb = full_bar(stage);
-          const bool drop = item_index == 0 && kb == args.drop_load_kb;
+          const bool drop = item_index == 0 && kb_i == args.drop_load_kb;
           if constexpr (Cfg::kMulticastA) {
             // A: this CTA loads one 64-row half of its A block and multicasts
             // it to the CTA at the same position in the other pair; every

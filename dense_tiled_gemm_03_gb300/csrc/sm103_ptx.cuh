@@ -103,6 +103,24 @@ __device__ __forceinline__ void tma_prefetch_descriptor(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// L2 eviction policy "evict first" for a whole access (fraction 1.0): data
+// read once, which should not push re-read data out of L2.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_2d with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void tma_load_2d_hint(const void* tmap, uint32_t dst, uint32_t bar, int32_t x, int32_t y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // 2-D tile load global -> this CTA's shared memory, completion counted on a
 // barrier of this CTA. x is the inner (contiguous) coordinate in elements.
 __device__ __forceinline__ void tma_load_2d(const void* tmap, uint32_t dst, uint32_t bar, int32_t x, int32_t y) {

@@ -348,6 +348,28 @@ def test_stream_k_cut_tiles(mnk, config):
         assert_parity(c, a, b, f"{mnk} {config} streamk={sk}")
 
 
+@pytest.mark.parametrize("config", CONFIGS)
+@pytest.mark.parametrize("mnk", [(128, 4096, 4160), (100, 3000, 1000), (300, 1000, 3000), (8, 640, 64 * 37 + 5)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_k_rotation(mnk, config):
+    """Tiles that start their K walk at a hashed k-block and wrap around (the
+    default for one row of tiles, forced on here for every configuration and
+    shape, with and without the stream-K tail, whose partial items keep the
+    plain order): parity both ways, and repeated launches bit-identical."""
+    from _parity import env_var
+    m, n, k = mnk
+    a, b = make_operands(m, n, k, "bf16", "uniform", seed=m + 3 * n + k)
+    for sk in ("0", "1"):
+        outs = []
+        for rot in ("1", "0", "1"):
+            with env_var("GEMM_TN_K_ROTATE", rot), env_var("GEMM_TN_STREAMK", sk):
+                c, status = gpu_gemm(a, b, config)
+            assert status == 0
+            assert_parity(c, a, b, f"{mnk} {config} rotate={rot} streamk={sk}")
+            outs.append(c)
+        assert torch.equal(outs[0], outs[2]), "rotated launches differ"
+
+
 def test_stream_k_is_deterministic():
     m, n, k = 300, 1000, 3000
     dev = torch.device("cuda", 0)
