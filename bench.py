@@ -46,10 +46,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC_BYTES = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the current
     # kernels (profiles/gemm_tn_*.md)
-    ("bf16_8192x8192x8192", "2cta_n256"): 1_062_835_456 + 124_839_424,
-    ("fp16_4096x4096x4096", "2cta_n256_mc"): 81_862_912 + 14_420_736,
-    ("bf16_128x16384x16384", "1cta_n128"): 541_118_720 + 3_267_072,
-    ("fp16_3001x5003x4097", "2cta_n256_mc"): 82_356_480 + 13_108_992,
+    ("bf16_8192x8192x8192", "2cta_n256"): 1_157_012_992 + 127_281_152,
+    ("fp16_4096x4096x4096", "2cta_n256_mc"): 80_924_416 + 14_750_720,
+    ("bf16_128x16384x16384", "1cta_n128"): 542_159_872 + 2_949_120,
+    ("fp16_3001x5003x4097", "2cta_n256_mc"): 80_478_976 + 12_952_832,
 }
 # the same for the attention kernel, keyed by workload
 NCU_TRAFFIC_ATTN_BYTES: dict[str, int] = {
