@@ -681,6 +681,14 @@ int host_path(HostPath** out) {
 
 const ConfigInfo& config_info(int id) { return kConfigs[id]; }
 
+bool dependent_launch_enabled() {
+  static const bool on = [] {
+    const char* s = std::getenv("GEMM_TN_PDL");
+    return s == nullptr || std::strcmp(s, "0") != 0;
+  }();
+  return on;
+}
+
 }  // namespace gemm_tn_impl
 
 using namespace gemm_tn_impl;

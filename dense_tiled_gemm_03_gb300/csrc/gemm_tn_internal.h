@@ -78,6 +78,10 @@ int flash_attn_rows_per_cta();
 cudaError_t launch_flash_attn(int head_dim, bool bf16, const gemm_tn_dev::FlashArgs& args, unsigned grid,
                               cudaStream_t stream);
 
+// Whether the GEMM and repack kernels are launched as programmatic dependents
+// of the previous kernel in their stream (on unless GEMM_TN_PDL=0).
+bool dependent_launch_enabled();
+
 // One launch repacking up to two matrices (entries with rows <= 0 are skipped).
 cudaError_t launch_repack2(const RepackRequest* req, int num, int num_sms, cudaStream_t stream);
 

@@ -52,6 +52,11 @@ __device__ __forceinline__ uint4 extract16(const uint4& lo, const uint4& hi, uin
 }
 
 __global__ void __launch_bounds__(256) repack_rows_kernel(const __grid_constant__ RepackArgs args) {
+  // launched as a programmatic dependent: read the sources only once the
+  // previous kernel in the stream has completed; the GEMM that follows may
+  // then be scheduled (it waits for this grid before reading the copies)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t rows_a = args.job[0].rows;
   const int64_t total_rows = rows_a + (args.num_jobs > 1 ? args.job[1].rows : 0);
   for (int64_t gr = blockIdx.x; gr < total_rows; gr += gridDim.x) {
@@ -105,8 +110,17 @@ cudaError_t launch_repack2(const RepackRequest* req, int num, int num_sms, cudaS
   args.num_jobs = n;
   const int64_t max_grid = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
   const unsigned grid = static_cast<unsigned>(rows < max_grid ? rows : max_grid);
-  gemm_tn_dev::repack_rows_kernel<<<grid, 256, 0, stream>>>(args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent_launch_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_tn_dev::repack_rows_kernel, args);
 }
 
 }  // namespace gemm_tn_impl

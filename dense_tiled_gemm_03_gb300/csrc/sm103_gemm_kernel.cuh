@@ -413,6 +413,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
   }
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // The set-up above (barriers, TMEM, descriptor prefetch) may overlap the
+  // end of the previous kernel in the stream; global memory is touched only
+  // once that kernel has completed. The next kernel may then be scheduled: it
+  // takes an SM only when a CTA of this grid leaves it, and this grid is
+  // resident as a whole, so nothing here waits on it.
+  griddep_wait();
+  griddep_launch_dependents();
 
   const Watchdog<Cfg> wd{&args, abort_flag, smem_addr(const_cast<uint32_t*>(abort_flag))};
   const int worker = static_cast<int>(blockIdx.x) / Cfg::kClusterSize;

@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cstdint>
 
+#include "gemm_tn_internal.h"
 #include "sm103_gemm_kernel.cuh"
 
 namespace gemm_tn_impl {
@@ -27,7 +28,8 @@ struct Launcher {
     return e;
   }
 
-  static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int grid, cudaStream_t stream) {
+  static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int grid, cudaStream_t stream,
+                          bool dependent = false) {
     cfg = cudaLaunchConfig_t{};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(gemm_tn_dev::kNumThreads, 1, 1);
@@ -42,14 +44,21 @@ struct Launcher {
       attr[0].val.clusterDim.z = 1;
       cfg.numAttrs = 1;
     }
+    if (dependent) {
+      // programmatic dependent launch: the kernel's set-up may overlap the
+      // previous kernel in the stream (the kernel waits before touching memory)
+      attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+      ++cfg.numAttrs;
+    }
   }
 
   static cudaError_t launch(const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream) {
     cudaError_t e = ensure_smem_attr();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
-    fill_config(cfg, attr, grid, stream);
+    cudaLaunchAttribute attr[2];
+    fill_config(cfg, attr, grid, stream, dependent_launch_enabled());
     return cudaLaunchKernelEx(&cfg, gemm_tn_dev::gemm_tn_sm103_kernel<Cfg>, args);
   }
 
@@ -68,7 +77,7 @@ struct Launcher {
       return per_sm * sms;
     }
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     fill_config(cfg, attr, sms - sms % Cfg::kClusterSize, nullptr);
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_dev::gemm_tn_sm103_kernel<Cfg>, &cfg) != cudaSuccess) {

@@ -97,6 +97,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// ------------------------------------------------------------------ dependent launch
+
+// Programmatic dependent launch: block until the kernels this grid depends on
+// in its stream have completed and their memory is visible (returns at once
+// when the grid was launched without that dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel in the stream, if launched as a programmatic dependent,
+// be scheduled now; it still waits in griddep_wait() for this grid to finish.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_descriptor(const void* tmap) {

@@ -370,6 +370,41 @@ def test_k_rotation(mnk, config):
         assert torch.equal(outs[0], outs[2]), "rotated launches differ"
 
 
+@pytest.mark.parametrize("pad", [0, 1])
+def test_dependent_launch_chain(pad):
+    """Kernels are launched as programmatic dependents of the previous kernel
+    in the stream: their set-up may overlap it, their memory accesses may not.
+    Call 2 reads call 1's output (pre-filled with NaN just before call 1),
+    back to back with no synchronisation, 20 times; with pad = 1 that output
+    has an odd row pitch, so call 2 first repacks it (the repack kernel is a
+    dependent of call 1, and call 2's GEMM of the repack). Every result must
+    equal the one computed with a synchronisation between the calls."""
+    dev = torch.device("cuda", 0)
+    m, k1, k2, n2 = 1000, 640, 1536, 700
+    a_cpu, b_cpu = make_operands(m, k2, k1, "fp16", "normal_over_sqrt_k", seed=31)
+    _, d_cpu = make_operands(m, n2, k2, "fp16", "normal_over_sqrt_k", seed=32)
+    a, b, d = a_cpu.to(dev), b_cpu.to(dev), d_cpu.to(dev)
+    c1_big = torch.empty((m, k2 + pad), dtype=torch.float16, device=dev)
+    c1 = c1_big[:, :k2]
+    c2 = torch.empty((m, n2), dtype=torch.float16, device=dev)
+    gt.mm_tn(a, b, out=c1)
+    torch.cuda.synchronize()
+    gt.mm_tn(c1, d, out=c2)
+    torch.cuda.synchronize()
+    expected = c2.clone()
+    assert torch.isfinite(expected.float()).all()
+    outs = []
+    for _ in range(20):
+        c1_big.fill_(float("nan"))
+        c2.fill_(float("nan"))
+        gt.mm_tn(a, b, out=c1)
+        gt.mm_tn(c1, d, out=c2)
+        outs.append(c2.clone())
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        assert torch.equal(o, expected), f"iteration {i}: a dependent call read its input before the previous call finished"
+
+
 def test_stream_k_is_deterministic():
     m, n, k = 300, 1000, 3000
     dev = torch.device("cuda", 0)
