@@ -174,6 +174,33 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}: expected float16 or bfloat16")
 
 
+class _on_device:
+    """Make `device` current for the call (the library launches on the
+    current device), switching only when it is not current already; yields
+    the raw handle of the device's current torch stream. Cheaper than
+    torch.cuda.device() + torch.cuda.current_stream() on the common path."""
+
+    __slots__ = ("index", "prev")
+
+    def __init__(self, device):
+        self.index = device.index if device.index is not None else 0
+        self.prev = None
+
+    def __enter__(self) -> int:
+        import torch
+        cur = torch._C._cuda_getDevice()
+        if cur != self.index:
+            self.prev = cur
+            torch._C._cuda_setDevice(self.index)
+        return torch._C._cuda_getCurrentRawStream(self.index)
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            import torch
+            torch._C._cuda_setDevice(self.prev)
+        return False
+
+
 def _row_pitch(t, cols: int) -> int:
     if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
         raise ValueError("operands must be 2-D with unit stride along the last dimension")
@@ -200,11 +227,10 @@ def mm_tn(a, b, out=None, status=None):
     elif out.shape != (m, n) or out.dtype != a.dtype or out.device != a.device:
         raise ValueError("out must be [M, N] with the dtype and device of a")
     lda, ldb, ldc = _row_pitch(a, k), _row_pitch(b, k), _row_pitch(out, n)
-    stream = torch.cuda.current_stream(a.device).cuda_stream
     d_status = status.data_ptr() if status is not None else None
-    with torch.cuda.device(a.device):
-        rc = gemm_tn_ex(_dtype_code(a), m, n, k, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(), ldc,
-                        d_status, stream)
+    with _on_device(a.device) as stream:
+        rc = library().gemm_tn_ex(_dtype_code(a), m, n, k, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(),
+                                  ldc, d_status, stream)
     if rc != GEMM_TN_OK:
         raise GemmTnError(rc, "gemm_tn_ex")
     return out
@@ -236,9 +262,8 @@ def mm_tn_fused(a, b, out=None, alpha=1.0, beta=0.0, bias=None, activation="none
     ep = GemmTnEpilogue(float(alpha), float(beta), bias.data_ptr() if bias is not None else None,
                         _ACTIVATIONS[activation], GEMM_TN_OUT_F32 if out_fp32 else GEMM_TN_OUT_INPUT)
     lda, ldb, ldc = _row_pitch(a, k), _row_pitch(b, k), _row_pitch(out, n)
-    stream = torch.cuda.current_stream(a.device).cuda_stream
     d_status = status.data_ptr() if status is not None else None
-    with torch.cuda.device(a.device):
+    with _on_device(a.device) as stream:
         rc = gemm_tn_fused(_dtype_code(a), m, n, k, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(), ldc, ep,
                            d_status, stream)
     if rc != GEMM_TN_OK:
@@ -263,9 +288,8 @@ def mm_nn(a, b, out=None, status=None):
     elif out.shape != (m, n) or out.dtype != a.dtype or out.device != a.device:
         raise ValueError("out must be [M, N] with the dtype and device of a")
     lda, ldb, ldc = _row_pitch(a, k), _row_pitch(b, n), _row_pitch(out, n)
-    stream = torch.cuda.current_stream(a.device).cuda_stream
     d_status = status.data_ptr() if status is not None else None
-    with torch.cuda.device(a.device):
+    with _on_device(a.device) as stream:
         rc = gemm_nn(_dtype_code(a), m, n, k, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(), ldc,
                      d_status, stream)
     if rc != GEMM_TN_OK:
@@ -316,9 +340,8 @@ def flash_attn(q, k, v, causal=True, scale=None, out=None, status=None):
     elif out.shape != q.shape or out.dtype != q.dtype or out.device != q.device or not out.is_contiguous():
         raise ValueError("out must be a contiguous tensor with q's shape, dtype and device")
     b, s, h, d = q.shape
-    stream = torch.cuda.current_stream(q.device).cuda_stream
     d_status = status.data_ptr() if status is not None else None
-    with torch.cuda.device(q.device):
+    with _on_device(q.device) as stream:
         rc = flash_attn_fwd(_dtype_code(q), b, s, h, d, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                             0.0 if scale is None else float(scale), causal, d_status, stream)
     if rc != GEMM_TN_OK:

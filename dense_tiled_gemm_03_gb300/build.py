@@ -25,7 +25,7 @@ BUILD_DIR = ROOT / "_build" / "gemm_tn"
 LIBRARY = PKG / "libgemm_tn.so"
 
 SOURCES = ["gemm_tn_api.cu", "sm103_gemm_1cta.cu", "sm103_gemm_2cta.cu", "sm103_gemm_nn.cu", "sm103_gemm_fused.cu",
-           "sm103_flash_attn.cu", "repack.cu"]
+           "sm103_flash_attn.cu", "repack.cu", "sm103_gemm_splitk.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-I", str(INCLUDE), "-I", str(CSRC)]

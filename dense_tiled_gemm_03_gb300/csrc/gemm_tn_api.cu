@@ -36,6 +36,10 @@ int max_resident_2cta(int id, bool bf16);
 int smem_bytes_2cta(int id);
 cudaError_t launch_gemm_nn(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_fused(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_splitk(int splits, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid,
+                               cudaStream_t stream);
+int max_resident_splitk(int splits, bool bf16, int num_sms);
+constexpr int kGb300SplitKResidentDefault[3] = {76, 36, 15};
 cudaError_t launch_fused_k0(bool bf16, void* c, int64_t ldc, bool out_f32, int64_t m, int64_t n, float beta,
                             const float* bias, int activation, int num_sms, cudaStream_t stream);
 
@@ -51,6 +55,7 @@ const ConfigInfo kConfigs[kNumConfigs] = {
     {"2cta_n256", 2, 256, 256, 128, 6, 1, 128},
     {"2cta_n128", 2, 256, 128, 64, 8, 1, 128},
     {"2cta_n256_mc", 2, 256, 256, 128, 6, 2, 64},
+    {"1cta_n128_splitk", 1, 128, 128, 128, 6, 1, 128},
 };
 
 thread_local int t_last_cuda_error = 0;
@@ -73,6 +78,7 @@ struct DeviceFacts {
   bool valid = false;
   int cc_major = 0, cc_minor = 0, num_sms = 0;
   int max_clusters[kNumConfigs][2] = {};   // [config][bf16], 0 = not queried yet
+  int splitk_clusters[3][2] = {};           // split-K clusters of 2, 4, 8 CTAs [size][bf16]
 };
 
 std::mutex g_device_mutex;
@@ -108,10 +114,30 @@ int resident_clusters(DeviceFacts* f, int cfg, bool bf16) {
     std::lock_guard<std::mutex> lock(g_device_mutex);
     if (f->max_clusters[cfg][bf16] > 0) return f->max_clusters[cfg][bf16];
   }
-  const int n = kConfigs[cfg].cta_group == 2 ? max_resident_2cta(cfg, bf16) : max_resident_1cta(cfg, bf16);
+  // split-K clusters run one tile each (not persistent): one CTA per SM
+  const int n = cfg == kCfg1CtaSplitK       ? f->num_sms
+                : kConfigs[cfg].cta_group == 2 ? max_resident_2cta(cfg, bf16)
+                                               : max_resident_1cta(cfg, bf16);
   std::lock_guard<std::mutex> lock(g_device_mutex);
   f->max_clusters[cfg][bf16] = n;
   return n;
+}
+
+// Resident split-K clusters of 2, 4 and 8 CTAs on the current device (GB300's
+// when a query fails).
+void splitk_resident(DeviceFacts* f, bool bf16, int out[3]) {
+  for (int i = 0; i < 3; ++i) {
+    {
+      std::lock_guard<std::mutex> lock(g_device_mutex);
+      out[i] = f->splitk_clusters[i][bf16];
+    }
+    if (out[i] > 0) continue;
+    int n = max_resident_splitk(2 << i, bf16, f->num_sms);
+    if (n <= 0) n = kGb300SplitKResidentDefault[i];
+    std::lock_guard<std::mutex> lock(g_device_mutex);
+    f->splitk_clusters[i][bf16] = n;
+    out[i] = n;
+  }
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -245,9 +271,36 @@ int parse_forced_config() {
 //    per SM (fp16 4096^3: 1534 vs 1503 TFLOP/s; fp16 3001 x 5003 x 4097: 857 vs
 //    741), so it is chosen when its rounds of tiles, discounted by that 5%,
 //    are fewer than the pairs' rounds (bf16 8192^3: 15 rounds vs 14, so pairs).
-int choose_config(int64_t m, int64_t n, int64_t /*k*/, int resident_pairs = 76, int resident_quads = 36) {
+// K splits of the split-K configuration for an M x N x K problem (0: not
+// worth it). With fewer 128 x 128 tiles than half the SMs, each tile's K is
+// cut over a cluster of S CTAs, S the largest of 8, 4, 2 whose clusters are
+// all resident at once (resident[0..2]: clusters of 2, 4, 8 CTAs; GB300: 76,
+// 36, 15) and that leaves at least 4 k-blocks per CTA. Measured on GB300
+// (CUDA graphs, us per call, no split -> split): 128 x 1024 x 4096 19.8 ->
+// 6.9 (S = 8), 64 x 2048 x 8192 38.5 -> 12.2 (S = 4; 16 clusters of 8 do not
+// fit at once and took 17.2), 1024 x 1024 x 8192 39.5 -> 20.9 (S = 2); 256^3
+// (4 k-blocks) stays whole. GEMM_TN_SPLITK=<S> forces S (0 turns it off).
+int splitk_factor(int64_t m, int64_t n, int64_t k, int sms, const int resident[3]) {
+  const int64_t tiles = ((m + 127) / 128) * ((n + 127) / 128);
+  const int64_t kb = (k + 63) / 64;
+  const char* s = std::getenv("GEMM_TN_SPLITK");
+  if (s != nullptr && *s != '\0') {
+    const long v = std::strtol(s, nullptr, 10);
+    if (v == 0) return 0;
+    if ((v == 2 || v == 4 || v == 8) && v <= kb) return static_cast<int>(v);
+  }
+  if (tiles * 2 > sms) return 0;
+  const int splits_of[3] = {2, 4, 8};
+  for (int i = 2; i >= 0; --i)
+    if (tiles <= resident[i] && kb >= 4 * splits_of[i]) return splits_of[i];
+  return 0;
+}
+
+int choose_config(int64_t m, int64_t n, int64_t k, int resident_pairs = 76, int resident_quads = 36,
+                  const int* splitk_resident = kGb300SplitKResidentDefault) {
   const int forced = parse_forced_config();
   if (forced >= 0) return forced;
+  if (splitk_factor(m, n, k, 2 * resident_pairs, splitk_resident) > 1) return kCfg1CtaSplitK;
   if (m <= 128) return kCfg1CtaN128;
   const int64_t tile_rows = (m + 255) / 256;
   const int64_t pair_tiles = tile_rows * ((n + 255) / 256);
@@ -429,10 +482,23 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   }
   const bool bf16 = dtype == GEMM_TN_BF16;
 
+  int sk_resident[3];
+  splitk_resident(dev, bf16, sk_resident);
   int cfg_id = choose_config(m, n, k, resident_clusters(dev, kCfg2CtaN256, bf16),
-                             resident_clusters(dev, kCfg2CtaN256Mc, bf16));
+                             resident_clusters(dev, kCfg2CtaN256Mc, bf16), sk_resident);
   // the fused epilogue is built for the pair 256 x 256 and single-CTA 128 x 128 tiles
   if (fused != nullptr && cfg_id != kCfg1CtaN128) cfg_id = m <= 128 ? kCfg1CtaN128 : kCfg2CtaN256;
+  // split-K: K cut over a cluster of `splits` CTAs per 128 x 128 tile (plain
+  // K-major GEMM only; a forced split-K that cannot cut K runs whole tiles)
+  int splits = 0;
+  if (cfg_id == kCfg1CtaSplitK) {
+    if (!b_mn) {
+      splits = splitk_factor(m, n, k, dev->num_sms, sk_resident);
+      for (int s : {8, 4, 2})
+        if (splits == 0 && s <= (k + kBlockK - 1) / kBlockK) splits = s;
+    }
+    if (splits < 2) cfg_id = kCfg1CtaN128;
+  }
   const ConfigInfo& cfg = kConfigs[cfg_id];
   const int64_t num_m_tiles = (m + cfg.tile_m - 1) / cfg.tile_m;
   // columns per scheduled tile: a multicast cluster covers two pairs' tiles
@@ -445,7 +511,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   if (clusters <= 0) return fail(GEMM_TN_ERR_CUDA, "kernel cannot be resident on this device (occupancy query)");
   // The no-alloc path keeps to whole tiles: its fixed scratch is for repacks.
   WorkPlan plan = plan_work(tiles, num_k_blocks, clusters,
-                            fixed_scratch == nullptr && fused == nullptr ? stream_k_mode() : 0);
+                            fixed_scratch == nullptr && fused == nullptr && splits == 0 ? stream_k_mode() : 0);
   int64_t split_begin = tiles;
   // split-capable kernels exist for the two CTA-pair configurations of the plain GEMM
   const bool can_split = !b_mn && fused == nullptr && (cfg_id == kCfg2CtaN256 || cfg_id == kCfg2CtaN256Mc);
@@ -454,7 +520,10 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
     const int64_t units = split_begin + (tiles - split_begin) * split;
     plan.workers = static_cast<int>(std::min<int64_t>(units, clusters));
   }
-  const int grid_ctas = plan.workers * cfg.cta_group * cfg.cluster_pairs;
+  // split-K: one cluster of `splits` CTAs per tile
+  if (splits > 0 && tiles * splits > INT32_MAX) return fail(GEMM_TN_ERR_INVALID_VALUE, "too many output tiles");
+  const int grid_ctas =
+      splits > 0 ? static_cast<int>(tiles * splits) : plan.workers * cfg.cta_group * cfg.cluster_pairs;
 
   // Workspace: [repacked A][repacked B][stream-K partials][stream-K flags].
   // Operands the TMA cannot address directly are copied into padded rows.
@@ -574,7 +643,9 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
     args.out_f32 = out_f32 ? 1 : 0;
   }
 
-  if (fused != nullptr)
+  if (splits > 0)
+    e = launch_gemm_splitk(splits, bf16, args, grid_ctas, stream);
+  else if (fused != nullptr)
     e = launch_gemm_fused(cfg_id, bf16, args, grid_ctas, stream);
   else if (b_mn)
     e = launch_gemm_nn(cfg_id, bf16, args, grid_ctas, stream);
@@ -901,6 +972,7 @@ int gemm_tn_select_config(int dtype, int64_t m, int64_t n, int64_t k) {
   // resident cluster counts of the current device when it is a GB300,
   // otherwise GB300's (76 CTA pairs, 36 four-CTA clusters)
   int pairs = 76, quads = 36;
+  int sk[3] = {kGb300SplitKResidentDefault[0], kGb300SplitKResidentDefault[1], kGb300SplitKResidentDefault[2]};
   int dev = -1;
   if (cudaGetDevice(&dev) == cudaSuccess) {
     DeviceFacts* facts = nullptr;
@@ -912,11 +984,12 @@ int gemm_tn_select_config(int dtype, int64_t m, int64_t n, int64_t k) {
         pairs = p;
         quads = q;
       }
+      splitk_resident(facts, bf16, sk);
     }
   } else {
     cudaGetLastError();
   }
-  return choose_config(m, n, k, pairs, quads);
+  return choose_config(m, n, k, pairs, quads, sk);
 }
 
 int gemm_tn_num_configs(void) { return kNumConfigs; }

@@ -38,7 +38,8 @@ enum ConfigId : int {
   kCfg2CtaN256 = 2,   // CTA pair per 256 x 256 tile (cta_group::2), 6-stage ring
   kCfg2CtaN128 = 3,   // CTA pair per 256 x 128 tile (cta_group::2), 8-stage ring
   kCfg2CtaN256Mc = 4, // 4-CTA cluster: two pairs on 256 x 512, A shared by TMA multicast
-  kNumConfigs = 5
+  kCfg1CtaSplitK = 5, // 128 x 128 tiles, K split over a cluster of 2, 4 or 8 CTAs (few tiles, long K)
+  kNumConfigs = 6
 };
 
 struct ConfigInfo {

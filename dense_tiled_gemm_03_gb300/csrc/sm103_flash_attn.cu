@@ -236,6 +236,13 @@ __global__ void __launch_bounds__(C::kNumThreads) __maxnreg__(C::kMaxRegs)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // The set-up above may overlap the end of the previous kernel in the
+  // stream; global memory is touched only once that kernel has completed.
+  // The next kernel is scheduled only after every CTA of this grid has run
+  // this trigger (so after the last one has started), so it never holds an
+  // SM that a CTA of this grid still waits for.
+  griddep_wait();
+  griddep_launch_dependents();
   const fa::Watch wd{&args, abort_flag};
 
   if (warp == fa::kProducerWarp) {
@@ -525,8 +532,17 @@ cudaError_t launch_cfg(const gemm_tn_dev::FlashArgs& args, unsigned grid, cudaSt
     if (e != cudaSuccess) return e;
     done_mask.fetch_or(bit, std::memory_order_acq_rel);
   }
-  gemm_tn_dev::flash_attn_fwd_kernel<C><<<grid, C::kNumThreads, C::kSmemBytes, stream>>>(args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(C::kNumThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent_launch_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_tn_dev::flash_attn_fwd_kernel<C>, args);
 }
 
 }  // namespace

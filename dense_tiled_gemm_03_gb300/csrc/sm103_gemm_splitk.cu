@@ -1,0 +1,353 @@
+// sm103_gemm_splitk.cu -- C = A x B^T split along K across the CTAs of a
+// thread-block cluster, for problems with too few output tiles to occupy the
+// GPU ("Tiling a matmul", section "Where it breaks": small M leaves little
+// reuse and few tiles; split-K keeps all SMs busy).
+//
+// One cluster of S CTAs (S = 2, 4 or 8, on S SMs) owns one 128 x 128 output
+// tile. CTA r of the cluster runs the usual TMA -> shared-memory ring ->
+// tcgen05.mma pipeline over k-blocks [r * KB / S, (r + 1) * KB / S) into its
+// own TMEM accumulator. The partial sums are then exchanged through
+// distributed shared memory instead of global memory:
+//   1. each CTA moves its fp32 accumulator TMEM -> registers -> its own shared
+//      memory (the operand ring, idle once the last MMA has completed);
+//   2. a cluster barrier makes every partial visible to the whole cluster;
+//   3. CTA r adds, for rows [r * 128 / S, (r + 1) * 128 / S) of the tile, the
+//      S partials in CTA order (ld.shared::cluster), rounds once to the output
+//      type and stores those rows of C;
+//   4. a second cluster barrier keeps every CTA's shared memory alive until
+//      all peers have read it.
+// The fixed order of the additions makes repeated launches bit-identical,
+// and no global workspace, flag or atomic is involved.
+//
+// Every mbarrier wait is bounded (GEMM_TN_ERR_TIMEOUT through the status
+// word); the roles never leave early, so both cluster barriers are always
+// reached by every thread.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "gemm_tn_internal.h"
+#include "sm103_gemm_kernel.cuh"
+
+namespace gemm_tn_dev {
+namespace splitk {
+
+constexpr int kThreads = 192;           // warp 0 TMA, warp 1 MMA, warps 2-5 TMEM drain; all reduce
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+constexpr int kBlockK = 64;             // one 128-byte swizzle row of 16-bit data
+constexpr int kStages = 6;
+constexpr uint32_t kTileBytes = 128 * 64 * 2;                       // A or B box of one k-block
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kStages * kTileBytes;
+constexpr uint32_t kRingEnd = kOffB + kStages * kTileBytes;        // 192 KiB
+// fp32 partial tile, rows padded to 132 floats so that the 16-byte stores of
+// one warp (32 rows, same column) spread over all banks
+constexpr int kPartStride = kBlockN + 4;
+constexpr uint32_t kPartBytes = kBlockM * kPartStride * 4;
+constexpr uint32_t kOffBar = kRingEnd;                              // full[S], empty[S], acc_full, drain
+constexpr int kNumBars = 2 * kStages + 2;
+constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;                // + slack to align the base to 1024
+constexpr uint32_t kTmemCols = 128;
+static_assert(kPartBytes <= kRingEnd, "the partial tile fits in the idle operand ring");
+static_assert(kSmemBytes <= 232448, "fits the opt-in shared memory of one CTA");
+
+// What Watchdog needs to know of the launch.
+template <int S>
+struct ClusterOf {
+  static constexpr int kClusterSize = S;
+};
+
+__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (kBf16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+}  // namespace splitk
+
+template <int S, bool kBf16>
+__global__ void __launch_bounds__(splitk::kThreads, 1) gemm_tn_splitk_kernel(const __grid_constant__ GemmArgs args) {
+  using namespace splitk;
+  static_assert(S == 2 || S == 4 || S == 8, "cluster of 2, 4 or 8 CTAs");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t base = smem_addr(smem);
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const uint32_t rank = cluster_ctarank();          // this CTA's slice of K
+  const int tile = static_cast<int>(blockIdx.x) / S;
+  const int tm = tile % args.num_m_tiles;
+  const int tn = tile / args.num_m_tiles;
+  const int kb0 = static_cast<int>(static_cast<int64_t>(rank) * args.num_k_blocks / S);
+  const int kb1 = static_cast<int>(static_cast<int64_t>(rank + 1) * args.num_k_blocks / S);
+
+  auto a_tile = [&](int s) { return base + kOffA + s * kTileBytes; };
+  auto b_tile = [&](int s) { return base + kOffB + s * kTileBytes; };
+  auto full_bar = [&](int s) { return base + kOffBar + 8u * s; };
+  auto empty_bar = [&](int s) { return base + kOffBar + 8u * (kStages + s); };
+  const uint32_t acc_full_bar = base + kOffBar + 8u * (2 * kStages);
+  const uint32_t drain_bar = acc_full_bar + 8u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + kOffAbort);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(acc_full_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_descriptor(&args.tmap_a);
+    tma_prefetch_descriptor(&args.tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc<1>(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before_sync();
+  cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  // set-up may overlap the previous kernel in the stream; memory waits for it
+  griddep_wait();
+  griddep_launch_dependents();
+  const Watchdog<ClusterOf<S>> wd{&args, abort_flag, smem_addr(const_cast<uint32_t*>(abort_flag))};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_phase_of[kStages];
+      for (int s = 0; s < kStages; ++s) issued_phase_of[s] = -1;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wd.wait(empty_bar(stage), phase ^ 1u)) break;
+        const uint32_t fb = full_bar(stage);
+        mbar_arrive_expect_tx(fb, 2 * kTileBytes);
+        if (kb - kb0 != args.drop_load_kb) {
+          tma_load_2d(&args.tmap_a, a_tile(stage), fb, kb * kBlockK, tm * kBlockM);
+          tma_load_2d(&args.tmap_b, b_tile(stage), fb, kb * kBlockK, tn * kBlockN);
+        }
+        issued_phase_of[stage] = static_cast<int>(phase);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      // loads still landing after another role gave up finish before exit
+      for (int s = 0; s < kStages; ++s)
+        if (issued_phase_of[s] >= 0) wd.drain(full_bar(s), static_cast<uint32_t>(issued_phase_of[s]));
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t kIdesc = mma_idesc_f16(kBf16, kBlockM, kBlockN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wd.wait(full_bar(stage), phase)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage));
+        const uint64_t b_desc = sw128_kmajor_desc(b_tile(stage));
+#pragma unroll
+        for (int kk = 0; kk < kBlockK / 16; ++kk)
+          mma_f16<1>(tmem_base, a_desc + 2u * kk, b_desc + 2u * kk, kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+        mma_commit(empty_bar(stage));
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) mma_commit(acc_full_bar);
+      // every MMA issued here completes before TMEM is freed
+      mma_commit(drain_bar);
+      wd.drain(drain_bar, 0);
+    }
+  } else {
+    // -------------------------------------------------------------- TMEM -> own shared memory
+    const uint32_t quarter = warp & 3u;          // TMEM lanes this warp may read
+    const bool ok = __all_sync(0xffffffffu, wd.wait(acc_full_bar, 0));
+    if (ok) {
+      tc_fence_after_sync();
+      const uint32_t row = quarter * 32u + lane;
+      const uint32_t t_row = tmem_base + ((quarter * 32u) << 16);
+#pragma unroll 1
+      for (int chunk = 0; chunk < kBlockN / 32; ++chunk) {
+        uint32_t r[32];
+        tmem_load_32x32(t_row + static_cast<uint32_t>(chunk * 32), r);
+        tmem_load_wait();
+        const uint32_t dst = base + (row * kPartStride + chunk * 32) * 4u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) st_shared_v4(dst + 16u * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+      }
+    }
+  }
+  __syncwarp();
+
+  // ---------------------------------------------------------------- cluster reduction
+  // every CTA's partial is in its shared memory: make them visible cluster-wide
+  tc_fence_before_sync();
+  cluster_sync_all();
+  {
+    constexpr int kRows = kBlockM / S;           // rows of the tile this CTA finishes
+    const int r0 = static_cast<int>(rank) * kRows;
+    uint16_t* cbase = static_cast<uint16_t*>(args.c);
+    for (int idx = threadIdx.x; idx < kRows * (kBlockN / 4); idx += kThreads) {
+      const int row = r0 + (idx >> 5);
+      const int col = (idx & 31) * 4;
+      const uint32_t off = base + static_cast<uint32_t>(row * kPartStride + col) * 4u;
+      float4 v[S];
+#pragma unroll
+      for (int s = 0; s < S; ++s) v[s] = ld_shared_cluster_f4(map_to_cta(off, static_cast<uint32_t>(s)));
+      float4 acc = v[0];
+#pragma unroll
+      for (int s = 1; s < S; ++s) {   // CTA order: the same sum on every launch
+        acc.x += v[s].x;
+        acc.y += v[s].y;
+        acc.z += v[s].z;
+        acc.w += v[s].w;
+      }
+      const int grow = tm * kBlockM + row;
+      const int gcol = tn * kBlockN + col;
+      if (grow >= args.m || gcol >= args.n) continue;
+      uint16_t* dst = cbase + static_cast<int64_t>(grow) * args.ldc + gcol;
+      const uint32_t lo = pack2<kBf16>(acc.x, acc.y), hi = pack2<kBf16>(acc.z, acc.w);
+      if (gcol + 4 <= args.n && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+      } else {
+        const uint16_t e[4] = {static_cast<uint16_t>(lo & 0xFFFFu), static_cast<uint16_t>(lo >> 16),
+                               static_cast<uint16_t>(hi & 0xFFFFu), static_cast<uint16_t>(hi >> 16)};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (gcol + j < args.n) dst[j] = e[j];
+      }
+    }
+  }
+  // peers may still be reading this CTA's partial
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc<1>(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace gemm_tn_dev
+
+namespace gemm_tn_impl {
+namespace {
+
+template <int S, bool kBf16>
+struct SplitKLauncher {
+  static cudaError_t ensure_smem_attr() {
+    static std::atomic<uint64_t> done_mask{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done_mask.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(gemm_tn_dev::gemm_tn_splitk_kernel<S, kBf16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(gemm_tn_dev::splitk::kSmemBytes));
+    if (e == cudaSuccess) done_mask.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+  }
+
+  static void fill(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int grid, cudaStream_t stream, bool dep) {
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(gemm_tn_dev::splitk::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = gemm_tn_dev::splitk::kSmemBytes;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (dep) {
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
+      cfg.numAttrs = 2;
+    }
+  }
+
+  static cudaError_t launch(const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream) {
+    cudaError_t e = ensure_smem_attr();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fill(cfg, attr, grid, stream, dependent_launch_enabled());
+    return cudaLaunchKernelEx(&cfg, gemm_tn_dev::gemm_tn_splitk_kernel<S, kBf16>, args);
+  }
+
+  static int max_clusters(int num_sms) {
+    if (ensure_smem_attr() != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fill(cfg, attr, num_sms - num_sms % S, nullptr, false);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_dev::gemm_tn_splitk_kernel<S, kBf16>, &cfg) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return clusters;
+  }
+};
+
+}  // namespace
+
+cudaError_t launch_gemm_splitk(int splits, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid,
+                               cudaStream_t stream) {
+  switch (splits) {
+    case 2: return bf16 ? SplitKLauncher<2, true>::launch(args, grid, stream)
+                        : SplitKLauncher<2, false>::launch(args, grid, stream);
+    case 4: return bf16 ? SplitKLauncher<4, true>::launch(args, grid, stream)
+                        : SplitKLauncher<4, false>::launch(args, grid, stream);
+    case 8: return bf16 ? SplitKLauncher<8, true>::launch(args, grid, stream)
+                        : SplitKLauncher<8, false>::launch(args, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int max_resident_splitk(int splits, bool bf16, int num_sms) {
+  switch (splits) {
+    case 2: return bf16 ? SplitKLauncher<2, true>::max_clusters(num_sms) : SplitKLauncher<2, false>::max_clusters(num_sms);
+    case 4: return bf16 ? SplitKLauncher<4, true>::max_clusters(num_sms) : SplitKLauncher<4, false>::max_clusters(num_sms);
+    case 8: return bf16 ? SplitKLauncher<8, true>::max_clusters(num_sms) : SplitKLauncher<8, false>::max_clusters(num_sms);
+    default: return 0;
+  }
+}
+
+}  // namespace gemm_tn_impl

@@ -47,7 +47,7 @@ def test_version_status_strings_and_configs(lib):
     assert gt.gemm_tn_status_string(gt.GEMM_TN_ERR_TIMEOUT) == "GEMM_TN_ERR_TIMEOUT"
     assert gt.gemm_tn_status_string(99) == "GEMM_TN_ERR_UNKNOWN"
     names = [gt.gemm_tn_config_name(i) for i in range(gt.gemm_tn_num_configs())]
-    assert names == ["1cta_n256", "1cta_n128", "2cta_n256", "2cta_n128", "2cta_n256_mc"]
+    assert names == ["1cta_n256", "1cta_n128", "2cta_n256", "2cta_n128", "2cta_n256_mc", "1cta_n128_splitk"]
     assert gt.gemm_tn_config_name(-1) == "invalid"
 
 
@@ -55,6 +55,12 @@ def test_config_table(lib, monkeypatch):
     monkeypatch.delenv("GEMM_TN_FORCE_CONFIG", raising=False)
     sel = lambda m, n, k: gt.gemm_tn_config_name(gt.gemm_tn_select_config(gt.GEMM_TN_BF16, m, n, k))
     assert sel(128, 16384, 16384) == "1cta_n128"   # skinny: one 128-row block of outputs
+    # few 128 x 128 tiles and a long K: K split over a cluster
+    assert sel(128, 1024, 4096) == "1cta_n128_splitk"     # 8 tiles x 8 splits
+    assert sel(128, 4096, 4096) == "1cta_n128_splitk"     # 32 tiles x 4 splits
+    assert sel(64, 2048, 8192) == "1cta_n128_splitk"      # 16 tiles: 4 splits (15 clusters of 8 fit at once)
+    assert sel(256, 256, 256) == "2cta_n256_mc"           # 4 k-blocks: too short to split
+    assert sel(1024, 2048, 4096) == "2cta_n256_mc"        # 128 tiles: more than half the SMs
     # with GB300's resident clusters (76 pairs, 36 four-CTA clusters):
     assert sel(8192, 8192, 8192) == "2cta_n256"      # 14 rounds of pair tiles vs 15 of multicast tiles
     assert sel(4096, 4096, 4096) == "2cta_n256_mc"   # 4 rounds either way: multicast streams more per SM

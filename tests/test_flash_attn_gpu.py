@@ -240,3 +240,42 @@ def test_concurrent_with_a_gemm_on_another_stream():
     ref, bound = oracle.gemm_tn_reference(a_cpu, b_cpu)
     rep = oracle.parity_report(c.cpu(), ref, bound)
     assert rep.ok, rep
+
+
+def test_dependent_launch_chain():
+    """The attention kernel is launched as a programmatic dependent of the
+    previous kernel in its stream. A pass whose queries are the previous
+    pass's output (pre-filled with NaN just before it), then a GEMM reading
+    that output, all back to back with no synchronisation, 10 times: every
+    result equals the one computed with synchronisations in between."""
+    dev = torch.device("cuda", 0)
+    q_cpu, k_cpu, v_cpu = make_qkv(2, 700, 4, 64, "bf16", seed=21)
+    q, k, v = q_cpu.to(dev), k_cpu.to(dev), v_cpu.to(dev)
+    o1 = torch.empty_like(q)
+    o2 = torch.empty_like(q)
+    w = torch.randn(320, 4 * 64, device=dev).to(torch.bfloat16)
+    g = torch.empty((2 * 700, 320), dtype=torch.bfloat16, device=dev)
+
+    def chain(sync):
+        gt.flash_attn(q, k, v, causal=True, out=o1)
+        if sync:
+            torch.cuda.synchronize()
+        gt.flash_attn(o1, k, v, causal=True, out=o2)
+        if sync:
+            torch.cuda.synchronize()
+        gt.mm_tn(o2.view(2 * 700, 4 * 64), w, out=g)
+
+    chain(True)
+    torch.cuda.synchronize()
+    expected_o2, expected_g = o2.clone(), g.clone()
+    assert torch.isfinite(expected_g.float()).all()
+    outs = []
+    for _ in range(10):
+        o1.fill_(float("nan"))
+        o2.fill_(float("nan"))
+        chain(False)
+        outs.append((o2.clone(), g.clone()))
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(outs):
+        assert torch.equal(a, expected_o2), f"iteration {i}: attention read its input early"
+        assert torch.equal(b, expected_g), f"iteration {i}: the GEMM read the attention output early"

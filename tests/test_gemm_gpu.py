@@ -20,7 +20,7 @@ from _parity import (assert_parity, assert_sampled_parity, edge_indices, epilogu
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = ["1cta_n256", "1cta_n128", "2cta_n128", "2cta_n256", "2cta_n256_mc"]
+CONFIGS = ["1cta_n256", "1cta_n128", "2cta_n128", "2cta_n256", "2cta_n256_mc", "1cta_n128_splitk"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -301,7 +301,7 @@ def test_plain_entry_point_and_host_entry_point_agree():
 
 # ------------------------------------------------------------ device watchdog
 
-@pytest.mark.parametrize("config", ["1cta_n256", "2cta_n256"])
+@pytest.mark.parametrize("config", ["1cta_n256", "2cta_n256", "1cta_n128_splitk"])
 def test_watchdog_reports_timeout_and_context_survives(config):
     """A wait that can never complete (the producer skips one k-block's loads
     through the test hook) must end within the watchdog budget with
@@ -403,6 +403,48 @@ def test_dependent_launch_chain(pad):
     torch.cuda.synchronize()
     for i, o in enumerate(outs):
         assert torch.equal(o, expected), f"iteration {i}: a dependent call read its input before the previous call finished"
+
+
+@pytest.mark.parametrize("splits", ["2", "4", "8"])
+@pytest.mark.parametrize("mnk", [(128, 1024, 4096), (16, 4096, 2048), (300, 700, 1000), (129, 257, 513),
+                                 (1, 1, 1024), (200, 390, 4097)], ids=lambda s: "x".join(map(str, s)))
+def test_split_k_over_a_cluster(mnk, splits):
+    """K cut over a cluster of 2, 4 or 8 CTAs per 128 x 128 tile, the fp32
+    partials added through distributed shared memory in CTA order: parity for
+    ragged M, N, K (K = 4097 also repacks A and B), an odd C pitch written
+    only inside N, and bit-identical results on repeated launches."""
+    from _parity import env_var
+    m, n, k = mnk
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "bf16", "normal_over_sqrt_k", seed=m + n + k + int(splits))
+    a, b = a_cpu.to(dev), b_cpu.to(dev)
+    ldc = n + 3
+    outs = []
+    for _ in range(2):
+        c_big = torch.full((m, ldc), float("nan"), dtype=torch.bfloat16, device=dev)
+        c = c_big[:, :n]
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        with forced_config("1cta_n128_splitk"), env_var("GEMM_TN_SPLITK", splits):
+            gt.mm_tn(a, b, out=c, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.isnan(c_big[:, n:].float()).all(), "wrote past N"
+        outs.append(c.cpu())
+    assert_parity(outs[0], a_cpu, b_cpu, f"{mnk} split {splits}")
+    assert torch.equal(outs[0], outs[1]), "split-K launches differ"
+
+
+def test_split_k_is_chosen_for_few_tiles_and_matches_whole_tiles():
+    """The default choice for 128 x 4096 x 4096 is the split-K cluster; its
+    result is within the criterion of the whole-K single-CTA tiles'."""
+    m, n, k = 128, 4096, 4096
+    a, b = make_operands(m, n, k, "fp16", "normal_over_sqrt_k", seed=5)
+    assert gt.gemm_tn_config_name(gt.gemm_tn_select_config(gt.GEMM_TN_F16, m, n, k)) == "1cta_n128_splitk"
+    c_split, st1 = gpu_gemm(a, b)
+    c_whole, st2 = gpu_gemm(a, b, "1cta_n128")
+    assert st1 == 0 and st2 == 0
+    assert_parity(c_split, a, b, "split-K default")
+    assert_parity(c_whole, a, b, "whole tiles")
 
 
 def test_stream_k_is_deterministic():
