@@ -404,6 +404,7 @@ int tail_split(const ConfigInfo& cfg, int64_t tiles, int clusters, int64_t* spli
   *split_begin = tiles;
   const char* env = std::getenv("GEMM_TN_TAIL_SPLIT");
   if (env != nullptr && std::strcmp(env, "0") == 0) return 1;
+  const bool force = env != nullptr && std::strcmp(env, "force") == 0;   // any number of full waves (tests)
   const int64_t full = tiles >= clusters ? tiles - tiles % clusters : 0;
   const int64_t last = tiles - full;
   if (last == 0) return 1;
@@ -411,7 +412,7 @@ int tail_split(const ConfigInfo& cfg, int64_t tiles, int clusters, int64_t* spli
   // pays only when it is a large share of the work: at most 4 full waves
   // before it (bf16 8192^3, 13 full waves: -1.2% with the cut; fp16
   // 3001 x 5003 x 4097, 3: +4.4%).
-  if (full / clusters > 4) return 1;
+  if (full / clusters > 4 && !force) return 1;
   for (int s : {4, 2}) {
     if (cfg.block_n / s >= 64 && (cfg.b_rows / s) % (b_mn ? 64 : 8) == 0 && last * s <= clusters) {
       *split_begin = full;

@@ -51,6 +51,8 @@ WORKLOADS = {
         Workload("bf16_8192x8192x8192", "bf16", 8192, 8192, 8192, "uniform", 1003),
         Workload("fp16_3001x5003x4097", "fp16", 3001, 5003, 4097, "uniform", 1004),
         Workload("bf16_128x16384x16384", "bf16", 128, 16384, 16384, "normal_over_sqrt_k", 1005),
+        # decode-like: a few rows against a square weight (few output tiles, long K)
+        Workload("bf16_8x4096x4096", "bf16", 8, 4096, 4096, "normal_over_sqrt_k", 1006),
     ]
 }
 

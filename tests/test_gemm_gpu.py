@@ -72,7 +72,7 @@ def test_ragged_output_with_aligned_pitch(mn, config):
 # ------------------------------------------------------------ the five workloads
 
 @pytest.mark.parametrize("name", ["fp16_256x256x256", "fp16_4096x4096x4096", "fp16_3001x5003x4097",
-                                  "bf16_128x16384x16384"])
+                                  "bf16_128x16384x16384", "bf16_8x4096x4096"])
 def test_workload_full_parity(name):
     """Element-by-element parity over the whole output, default configuration."""
     a, b = workload_operands(name)
