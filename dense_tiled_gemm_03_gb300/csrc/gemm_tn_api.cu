@@ -538,7 +538,8 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   const size_t b_bytes = repack_b ? static_cast<size_t>(round_up(b_rows_mem * ldb_pad * 2, 256)) : 0;
   const size_t partial_bytes =
       plan.sk_iters > 0 ? static_cast<size_t>(grid_ctas) * 128 * static_cast<size_t>(cfg.block_n) * 4 : 0;
-  const size_t flag_bytes = plan.sk_iters > 0 ? static_cast<size_t>(grid_ctas) * 4 * sizeof(int) : 0;
+  const size_t flag_bytes =
+      plan.sk_iters > 0 ? static_cast<size_t>(grid_ctas) * gemm_tn_dev::kNumEpilogueWarps * sizeof(int) : 0;
   const size_t ws_bytes = a_bytes + b_bytes + partial_bytes + flag_bytes;
   void* workspace = nullptr;
   void* owned_workspace = nullptr;   // what this call allocated and must free

@@ -42,11 +42,15 @@
 
 namespace gemm_tn_dev {
 
-constexpr int kNumThreads = 192;       // 6 warps
+constexpr int kNumThreads = 320;       // 10 warps
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kFirstEpilogueWarp = 2;
-constexpr int kNumEpilogueWarps = 4;
+// two epilogue warps per 32-lane quarter of TMEM, on alternate 32-column
+// chunks: a chunk is a chain of short dependent steps (TMEM load, convert,
+// staging stores, proxy fence, TMA store), so two chains per quarter halve
+// the epilogue that is left exposed after a CTA's last tile
+constexpr int kNumEpilogueWarps = 8;
 constexpr int kStatusTimeout = 6;      // == GEMM_TN_ERR_TIMEOUT
 
 // Kernel arguments. Tensor maps first: they must be 64-byte aligned.
@@ -601,6 +605,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
     // ------------------------------------------------------------------ epilogue
     const uint32_t quarter = warp & 3u;           // TMEM lanes this warp may read
     const uint32_t epi_warp = warp - kFirstEpilogueWarp;
+    const int half = static_cast<int>(epi_warp >> 2);   // this warp takes chunks half, half + 2, ...
     uint8_t* warp_stage = smem + Cfg::kOffEpi + epi_warp * Cfg::kEpiWarpBytes;
     uint32_t* stg = reinterpret_cast<uint32_t*>(warp_stage);
     const uint32_t stage_addr = smem_addr(warp_stage);
@@ -651,7 +656,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         last_contrib = sk_worker_of(args, (t_local + 1) * args.num_k_blocks - 1);
         for (int w = first_contrib; w <= last_contrib && ok; ++w) {
           const int cta = w * Cfg::kClusterSize + static_cast<int>(cluster_rank);
-          ok = __all_sync(0xffffffffu, wd.wait_flag(args.flags + cta * kNumEpilogueWarps + quarter));
+          ok = __all_sync(0xffffffffu, wd.wait_flag(args.flags + cta * kNumEpilogueWarps + epi_warp));
         }
         if (!ok) break;
       }
@@ -663,28 +668,33 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         return reinterpret_cast<const float4*>(
             args.partials + ((static_cast<int64_t>(cta) * kChunks + chunk) * 128 + part_row) * 32);
       };
+      // this warp's last chunk (-1: none), after whose TMEM load it hands
+      // the accumulator back to the MMA warp (every epilogue warp arrives once)
+      const int my_last = chunks > half ? half + (((chunks - 1 - half) >> 1) << 1) : -1;
+      auto hand_back = [&]() {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (Cfg::kCtaGroup == 2) {
+            mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
+          } else {
+            mbar_arrive(acc_empty_bar(acc));
+          }
+        }
+      };
+      if (my_last < 0) hand_back();
       float4 pre[8];
-      if (finisher) {
+      if (finisher && half < chunks) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) pre[j] = __ldcg(partial_src(first_contrib, 0) + j);
+        for (int j = 0; j < 8; ++j) pre[j] = __ldcg(partial_src(first_contrib, half) + j);
       }
-      for (int chunk = 0; chunk < chunks; ++chunk) {
+      for (int chunk = half; chunk < chunks; chunk += 2) {
         const int col0 = col_tile + chunk * 32;
         uint32_t r[32];
         tmem_load_32x32(t_row + static_cast<uint32_t>(chunk * 32), r);
         tmem_load_wait();
-        if (chunk == chunks - 1) {
-          // the accumulator is in registers now: hand it back to the MMA warp
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) {
-            if constexpr (Cfg::kCtaGroup == 2) {
-              mbar_arrive_cluster(acc_empty_leader0 + 8u * acc);
-            } else {
-              mbar_arrive(acc_empty_bar(acc));
-            }
-          }
-        }
+        // the accumulator is in registers now: hand it back to the MMA warp
+        if (chunk == my_last) hand_back();
         if (contributor) {
           float4* dst = reinterpret_cast<float4*>(
               args.partials + ((static_cast<int64_t>(blockIdx.x) * kChunks + chunk) * 128 + row_in_cta) * 32);
@@ -702,9 +712,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             if (w == first_contrib) {
 #pragma unroll
               for (int j = 0; j < 8; ++j) v[j] = pre[j];
-              if (chunk + 1 < chunks) {
+              if (chunk + 2 < chunks) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) pre[j] = __ldcg(partial_src(first_contrib, chunk + 1) + j);
+                for (int j = 0; j < 8; ++j) pre[j] = __ldcg(partial_src(first_contrib, chunk + 2) + j);
               }
             } else {
 #pragma unroll
@@ -871,7 +881,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         // visible at GPU scope before lane 0 raises the flag
         __threadfence();
         __syncwarp();
-        if (lane == 0) st_release_gpu(args.flags + blockIdx.x * kNumEpilogueWarps + quarter, 1);
+        if (lane == 0) st_release_gpu(args.flags + blockIdx.x * kNumEpilogueWarps + epi_warp, 1);
       }
       if (++acc == Cfg::kNumAcc) {
         acc = 0;
