@@ -10,7 +10,8 @@
 //    "TileLang: a tile language one level below Triton", section "What it
 //    generated": 3 full + 3 empty barriers around a TMA producer).
 //  * Warp specialization: warp 0 is the TMA producer, one thread of warp 1
-//    issues every tcgen05.mma, warps 2..5 are the epilogue.
+//    issues every tcgen05.mma, warps 2..9 are the epilogue (two per 32-lane
+//    quarter of TMEM, on alternate 32-column chunks).
 //  * Accumulators live in tensor memory (TMEM), double-buffered so the
 //    epilogue of one tile overlaps the main loop of the next. The operand
 //    round trip through registers that the Hopper V0 kernel pays ("0. A
