@@ -281,6 +281,7 @@ def run_native(args, dist: Dist, peaks, peak_src):
         sampler.start()
     dist.barrier()
     torch.cuda.synchronize(dev)
+    launches0 = gt.gemm_tn_launch_count()
     region0.record(stream)
     for i in range(args.steps):
         if flush:
@@ -290,6 +291,7 @@ def run_native(args, dist: Dist, peaks, peak_src):
         if flush:
             ends[i].record(stream)
     region1.record(stream)
+    launches = gt.gemm_tn_launch_count() - launches0   # this library's kernels in the timed region
     torch.cuda.synchronize(dev)
     dist.barrier()
     clocks = sampler.stop() if dist.rank == 0 else None
@@ -341,9 +343,6 @@ def run_native(args, dist: Dist, peaks, peak_src):
            "h2d_bytes_per_step": op_bytes, "d2h_bytes_per_step": w.m * w.n * 2 + 4,
            "steps": args.e2e_steps, "entry_point": "gemm_tn_host (pinned host buffers)"}
 
-    # one GEMM kernel per step, plus one repack kernel when the operands' row
-    # pitch (K here: the operands are contiguous) is not a multiple of 8
-    launches_per_step = 1 + (1 if w.k % 8 else 0)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -365,7 +364,7 @@ def run_native(args, dist: Dist, peaks, peak_src):
         "pct_of_peak": round(100 * w.flops / (avg_launch_ms * 1e-3) / 1e12 / tensor_peak, 2),
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": args.steps * launches_per_step,
+        "gpu_launches": launches,
         "clocks": clocks,
     }
     if args.cublas_context:
@@ -476,6 +475,7 @@ def run_native_attn(args, dist: Dist, peaks, peak_src):
         sampler.start()
     dist.barrier()
     torch.cuda.synchronize(dev)
+    launches0 = gt.gemm_tn_launch_count()
     region0.record(stream)
     for i in range(args.steps):
         if flush:
@@ -485,6 +485,7 @@ def run_native_attn(args, dist: Dist, peaks, peak_src):
         if flush:
             ends[i].record(stream)
     region1.record(stream)
+    launches = gt.gemm_tn_launch_count() - launches0   # this library's kernels in the timed region
     torch.cuda.synchronize(dev)
     dist.barrier()
     clocks = sampler.stop() if dist.rank == 0 else None
@@ -548,7 +549,7 @@ def run_native_attn(args, dist: Dist, peaks, peak_src):
         "pct_of_peak": round(100 * achieved / tensor_peak, 2),
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": launches,
         "clocks": clocks,
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

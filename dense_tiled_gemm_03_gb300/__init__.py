@@ -36,6 +36,7 @@ from ._native import (  # noqa: F401
     gemm_tn_select_config,
     gemm_tn_status_string,
     gemm_tn_version,
+    gemm_tn_launch_count,
     library,
     mm_nn,
     mm_tn_fused,

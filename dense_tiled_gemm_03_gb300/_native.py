@@ -60,6 +60,7 @@ _SIGNATURES = {
     "gemm_tn_last_cuda_error": (_int, []),
     "gemm_tn_last_error_message": (ctypes.c_char_p, []),
     "gemm_tn_version": (_int, []),
+    "gemm_tn_launch_count": (ctypes.c_uint64, []),
     "flash_attn_fwd": (_int, [_int, _i64, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr, ctypes.c_float, _int, _ptr,
                               _ptr]),
 }
@@ -161,6 +162,11 @@ def gemm_tn_last_error_message() -> str:
 
 def gemm_tn_version() -> int:
     return library().gemm_tn_version()
+
+
+def gemm_tn_launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return library().gemm_tn_launch_count()
 
 
 # ---------------------------------------------------------------- torch helpers

@@ -19,6 +19,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/flash_attn.h"
@@ -59,6 +60,13 @@ const ConfigInfo kConfigs[kNumConfigs] = {
 };
 
 thread_local int t_last_cuda_error = 0;
+std::atomic<uint64_t> g_launch_count{0};
+
+// Count one kernel launch that the runtime accepted.
+cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) g_launch_count.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
 thread_local char t_last_message[256] = "";
 
 int fail(int status, const char* what) {
@@ -400,19 +408,22 @@ WorkPlan plan_work(int64_t tiles, int64_t k_blocks, int clusters, int stream_k) 
 // that wave has up to `split` times as many, shorter units for the same
 // workers. Returns the split factor (1: none) and the first cut tile.
 // GEMM_TN_TAIL_SPLIT=0 turns it off.
+
 int tail_split(const ConfigInfo& cfg, int64_t tiles, int clusters, int64_t* split_begin, bool b_mn) {
   *split_begin = tiles;
   const char* env = std::getenv("GEMM_TN_TAIL_SPLIT");
   if (env != nullptr && std::strcmp(env, "0") == 0) return 1;
-  const bool force = env != nullptr && std::strcmp(env, "force") == 0;   // any number of full waves (tests)
   const int64_t full = tiles >= clusters ? tiles - tiles % clusters : 0;
   const int64_t last = tiles - full;
   if (last == 0) return 1;
   // The split-capable kernel runs every round ~1% slower, so a cut last wave
   // pays only when it is a large share of the work: at most 4 full waves
-  // before it (bf16 8192^3, 13 full waves: -1.2% with the cut; fp16
-  // 3001 x 5003 x 4097, 3: +4.4%).
-  if (full / clusters > 4 && !force) return 1;
+  // before it (bf16 8192^3, 13 full waves: -1.3 to -1.8% with the cut; fp16
+  // 3001 x 5003 x 4097, 3: +4.4%). Running the cut tiles as a second launch
+  // after the full waves, with the plain kernel for those, measured worse
+  // still (fp16 3001 x 5003 x 4097: 120 against 112 us; bf16 8192^3: +2-3%):
+  // the second launch waits for the whole first grid and starts cold.
+  if (full / clusters > 4) return 1;
   for (int s : {4, 2}) {
     if (cfg.block_n / s >= 64 && (cfg.b_rows / s) % (b_mn ? 64 : 8) == 0 && last * s <= clusters) {
       *split_begin = full;
@@ -473,8 +484,8 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   const bool out_f32 = fused != nullptr && fused->out_dtype == GEMM_TN_OUT_F32;
   if (k == 0) {  // the empty sum
     if (fused != nullptr) {
-      cudaError_t e = launch_fused_k0(dtype == GEMM_TN_BF16, c, ldc, out_f32, m, n, fused->beta, fused->bias,
-                                      fused->activation, dev->num_sms, stream);
+      cudaError_t e = counted(launch_fused_k0(dtype == GEMM_TN_BF16, c, ldc, out_f32, m, n, fused->beta,
+                                              fused->bias, fused->activation, dev->num_sms, stream));
       return e == cudaSuccess ? GEMM_TN_OK : fail_cuda(e, "fused epilogue (K = 0)");
     }
     cudaError_t e = cudaMemset2DAsync(c, static_cast<size_t>(ldc) * 2, 0, static_cast<size_t>(n) * 2,
@@ -567,7 +578,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   if (repack_a || repack_b) {
     RepackRequest req[2] = {{a, lda, ws, ld_pad, repack_a ? m : 0, k},
                             {b, ldb, ws + a_bytes, ldb_pad, repack_b ? b_rows_mem : 0, b_cols_mem}};
-    e = launch_repack2(req, 2, dev->num_sms, stream);
+    e = counted(launch_repack2(req, 2, dev->num_sms, stream));
     if (repack_a) {
       a_use = ws;
       lda_use = ld_pad;
@@ -646,14 +657,14 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   }
 
   if (splits > 0)
-    e = launch_gemm_splitk(splits, bf16, args, grid_ctas, stream);
+    e = counted(launch_gemm_splitk(splits, bf16, args, grid_ctas, stream));
   else if (fused != nullptr)
-    e = launch_gemm_fused(cfg_id, bf16, args, grid_ctas, stream);
+    e = counted(launch_gemm_fused(cfg_id, bf16, args, grid_ctas, stream));
   else if (b_mn)
-    e = launch_gemm_nn(cfg_id, bf16, args, grid_ctas, stream);
+    e = counted(launch_gemm_nn(cfg_id, bf16, args, grid_ctas, stream));
   else
-    e = cfg.cta_group == 2 ? launch_gemm_2cta(cfg_id, bf16, args, grid_ctas, stream)
-                           : launch_gemm_1cta(cfg_id, bf16, args, grid_ctas, stream);
+    e = counted(cfg.cta_group == 2 ? launch_gemm_2cta(cfg_id, bf16, args, grid_ctas, stream)
+                                   : launch_gemm_1cta(cfg_id, bf16, args, grid_ctas, stream));
   if (owned_workspace) {
     cudaError_t e2 = cudaFreeAsync(owned_workspace, stream);
     if (e == cudaSuccess) e = e2;
@@ -962,8 +973,8 @@ int flash_attn_fwd(int dtype, int64_t batch, int64_t seq, int64_t heads, int64_t
   const int64_t kv_bytes = 2 * seq * head_dim * 2;
   args.head_group = static_cast<int>(std::min<int64_t>(batch * heads, std::max<int64_t>(1, (48ll << 20) / kv_bytes)));
   const unsigned grid = static_cast<unsigned>(q_tiles * batch * heads);
-  const cudaError_t e = launch_flash_attn(static_cast<int>(head_dim), bf16, args, grid,
-                                          reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e = counted(launch_flash_attn(static_cast<int>(head_dim), bf16, args, grid,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
   if (e != cudaSuccess) return fail_cuda(e, "flash attention launch");
   return GEMM_TN_OK;
 }
@@ -1019,5 +1030,7 @@ int gemm_tn_last_cuda_error(void) { return t_last_cuda_error; }
 const char* gemm_tn_last_error_message(void) { return t_last_message; }
 
 int gemm_tn_version(void) { return kAbiVersion; }
+
+uint64_t gemm_tn_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
 
 }  // extern "C"

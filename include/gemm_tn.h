@@ -196,6 +196,13 @@ GEMM_TN_API const char* gemm_tn_last_error_message(void);
 /* ABI version: major * 100 + minor. */
 GEMM_TN_API int gemm_tn_version(void);
 
+/* Number of kernels this library has launched in this process so far, over
+ * every thread and device: GEMM kernels (one per call), repack
+ * kernels for misaligned operands, the K = 0 epilogue kernel and attention
+ * kernels. Diagnostics: read it before and after a region of work to count
+ * that region's launches. Never fails. */
+GEMM_TN_API uint64_t gemm_tn_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

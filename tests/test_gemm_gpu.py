@@ -447,6 +447,26 @@ def test_split_k_is_chosen_for_few_tiles_and_matches_whole_tiles():
     assert_parity(c_whole, a, b, "whole tiles")
 
 
+def test_launch_counter():
+    """gemm_tn_launch_count counts this library's kernel launches: one for an
+    aligned GEMM without a cut tail, one more for a repack of misaligned
+    operands, one per attention pass, none for the K = 0 memset."""
+    dev = torch.device("cuda", 0)
+    a, b = (t.to(dev) for t in make_operands(512, 512, 512, "fp16", "uniform", seed=3))
+    n0 = gt.gemm_tn_launch_count()
+    gt.mm_tn(a, b)
+    assert gt.gemm_tn_launch_count() - n0 == 1
+    ar, br = (t.to(dev) for t in make_operands(300, 200, 100, "fp16", "uniform", seed=4))   # K = 100: repack
+    n0 = gt.gemm_tn_launch_count()
+    gt.mm_tn(ar, br)
+    assert gt.gemm_tn_launch_count() - n0 == 2
+    az, bz = torch.empty((64, 0), dtype=torch.float16, device=dev), torch.empty((32, 0), dtype=torch.float16, device=dev)
+    n0 = gt.gemm_tn_launch_count()
+    gt.mm_tn(az, bz)
+    assert gt.gemm_tn_launch_count() - n0 == 0
+    torch.cuda.synchronize()
+
+
 def test_stream_k_is_deterministic():
     m, n, k = 300, 1000, 3000
     dev = torch.device("cuda", 0)
