@@ -46,14 +46,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC_BYTES = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the current
     # kernels (profiles/gemm_tn_*.md)
-    ("bf16_8192x8192x8192", "2cta_n256"): 1_157_012_992 + 127_281_152,
-    ("fp16_4096x4096x4096", "2cta_n256_mc"): 80_924_416 + 14_750_720,
-    ("bf16_128x16384x16384", "1cta_n128"): 542_159_872 + 2_949_120,
-    ("fp16_3001x5003x4097", "2cta_n256_mc"): 80_478_976 + 12_952_832,
+    ("bf16_8192x8192x8192", "2cta_n256"): 1_074_012_416 + 125_360_896,
+    ("fp16_4096x4096x4096", "2cta_n256_mc"): 81_974_528 + 15_100_928,
+    ("bf16_128x16384x16384", "1cta_n128"): 542_159_872 + 2_915_584,
+    ("fp16_3001x5003x4097", "2cta_n256_mc"): 82_883_328 + 14_531_328,
+    ("bf16_8x4096x4096", "1cta_n128_splitk"): 33_637_888 + 0,
 }
 # the same for the attention kernel, keyed by workload
 NCU_TRAFFIC_ATTN_BYTES: dict[str, int] = {
-    "attn_bf16_b2_s8192_h32_d128_causal": 448_981_760 + 113_403_904,
+    "attn_bf16_b2_s8192_h32_d128_causal": 450_154_496 + 113_367_552,
 }
 
 
@@ -328,7 +329,8 @@ def run_native(args, dist: Dist, peaks, peak_src):
     roofline["traffic"] = NCU_TRAFFIC_BYTES.get((w.name, cfg_name))
     roofline["algorithmic_bytes"] = compulsory
     roofline["peak_source"] = f"{peak_src} ({'hbm_gbs' if hbm_bound else 'bf16_tflops'} burst; kernel timed alone)"
-    roofline["kernel"] = f"gemm_tn_sm103_kernel<{cfg_name}>"
+    roofline["kernel"] = ("gemm_tn_splitk_kernel" if cfg_name.endswith("splitk")
+                          else f"gemm_tn_sm103_kernel<{cfg_name}>")
 
     # end to end through the host-buffer entry point
     pin_a, pin_b = a_cpu.pin_memory(), b_cpu.pin_memory()
