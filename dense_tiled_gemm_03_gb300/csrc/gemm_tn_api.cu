@@ -39,6 +39,9 @@ cudaError_t launch_gemm_nn(int id, bool bf16, const gemm_tn_dev::GemmArgs& args,
 cudaError_t launch_gemm_fused(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_splitk(int splits, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid,
                                cudaStream_t stream);
+cudaError_t launch_gemm_decode(int splits, int rows, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid,
+                               cudaStream_t stream);
+int decode_rows(int64_t m);
 int max_resident_splitk(int splits, bool bf16, int num_sms);
 constexpr int kGb300SplitKResidentDefault[3] = {76, 36, 15};
 cudaError_t launch_fused_k0(bool bf16, void* c, int64_t ldc, bool out_f32, int64_t m, int64_t n, float beta,
@@ -57,6 +60,7 @@ const ConfigInfo kConfigs[kNumConfigs] = {
     {"2cta_n128", 2, 256, 128, 64, 8, 1, 128},
     {"2cta_n256_mc", 2, 256, 256, 128, 6, 2, 64},
     {"1cta_n128_splitk", 1, 128, 128, 128, 6, 1, 128},
+    {"1cta_decode_splitk", 1, 128, 128, 128, 11, 1, 16},
 };
 
 thread_local int t_last_cuda_error = 0;
@@ -123,7 +127,7 @@ int resident_clusters(DeviceFacts* f, int cfg, bool bf16) {
     if (f->max_clusters[cfg][bf16] > 0) return f->max_clusters[cfg][bf16];
   }
   // split-K clusters run one tile each (not persistent): one CTA per SM
-  const int n = cfg == kCfg1CtaSplitK       ? f->num_sms
+  const int n = cfg == kCfg1CtaSplitK || cfg == kCfgDecodeSplitK ? f->num_sms
                 : kConfigs[cfg].cta_group == 2 ? max_resident_2cta(cfg, bf16)
                                                : max_resident_1cta(cfg, bf16);
   std::lock_guard<std::mutex> lock(g_device_mutex);
@@ -308,7 +312,10 @@ int choose_config(int64_t m, int64_t n, int64_t k, int resident_pairs = 76, int 
                   const int* splitk_resident = kGb300SplitKResidentDefault) {
   const int forced = parse_forced_config();
   if (forced >= 0) return forced;
-  if (splitk_factor(m, n, k, 2 * resident_pairs, splitk_resident) > 1) return kCfg1CtaSplitK;
+  // few output tiles: split K over a cluster (with at most 32 rows of A, B's
+  // rows take the MMA's M side)
+  if (splitk_factor(m, n, k, 2 * resident_pairs, splitk_resident) > 1)
+    return m <= 32 ? kCfgDecodeSplitK : kCfg1CtaSplitK;
   if (m <= 128) return kCfg1CtaN128;
   const int64_t tile_rows = (m + 255) / 256;
   const int64_t pair_tiles = tile_rows * ((n + 255) / 256);
@@ -503,13 +510,21 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   // split-K: K cut over a cluster of `splits` CTAs per 128 x 128 tile (plain
   // K-major GEMM only; a forced split-K that cannot cut K runs whole tiles)
   int splits = 0;
-  if (cfg_id == kCfg1CtaSplitK) {
+  int decode = 0;   // rows of A per MMA of the decode kernel (0: not that kernel)
+  if (cfg_id == kCfgDecodeSplitK) {
+    decode = b_mn ? 0 : decode_rows(m);
+    cfg_id = decode > 0 ? kCfgDecodeSplitK : kCfg1CtaSplitK;
+  }
+  if (cfg_id == kCfg1CtaSplitK || cfg_id == kCfgDecodeSplitK) {
     if (!b_mn) {
       splits = splitk_factor(m, n, k, dev->num_sms, sk_resident);
       for (int s : {8, 4, 2})
         if (splits == 0 && s <= (k + kBlockK - 1) / kBlockK) splits = s;
     }
-    if (splits < 2) cfg_id = kCfg1CtaN128;
+    if (splits < 2) {
+      cfg_id = kCfg1CtaN128;
+      decode = 0;
+    }
   }
   const ConfigInfo& cfg = kConfigs[cfg_id];
   const int64_t num_m_tiles = (m + cfg.tile_m - 1) / cfg.tile_m;
@@ -604,7 +619,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
 
   alignas(64) gemm_tn_dev::GemmArgs args;
   std::memset(&args, 0, sizeof(args));
-  st = encode_matrix_map(&args.tmap_a, bf16, a_use, m, k, lda_use, kBlockK, cfg.a_box_rows,
+  st = encode_matrix_map(&args.tmap_a, bf16, a_use, m, k, lda_use, kBlockK, decode > 0 ? decode : cfg.a_box_rows,
                          CU_TENSOR_MAP_SWIZZLE_128B);
   if (st == GEMM_TN_OK && b_mn)   // [K, N]: 64 N x 64 K boxes
     st = encode_matrix_map(&args.tmap_b, bf16, b_use, k, n, ldb_use, 64, kBlockK, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -656,7 +671,9 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
     args.out_f32 = out_f32 ? 1 : 0;
   }
 
-  if (splits > 0)
+  if (decode > 0)
+    e = counted(launch_gemm_decode(splits, decode, bf16, args, grid_ctas, stream));
+  else if (splits > 0)
     e = counted(launch_gemm_splitk(splits, bf16, args, grid_ctas, stream));
   else if (fused != nullptr)
     e = counted(launch_gemm_fused(cfg_id, bf16, args, grid_ctas, stream));

@@ -39,7 +39,8 @@ enum ConfigId : int {
   kCfg2CtaN128 = 3,   // CTA pair per 256 x 128 tile (cta_group::2), 8-stage ring
   kCfg2CtaN256Mc = 4, // 4-CTA cluster: two pairs on 256 x 512, A shared by TMA multicast
   kCfg1CtaSplitK = 5, // 128 x 128 tiles, K split over a cluster of 2, 4 or 8 CTAs (few tiles, long K)
-  kNumConfigs = 6
+  kCfgDecodeSplitK = 6, // M <= 32: B's rows on the MMA's M side, K split over a cluster (decode-like)
+  kNumConfigs = 7
 };
 
 struct ConfigInfo {

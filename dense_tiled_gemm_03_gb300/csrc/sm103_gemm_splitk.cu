@@ -264,6 +264,216 @@ __global__ void __launch_bounds__(splitk::kThreads, 1) gemm_tn_splitk_kernel(con
 
 }  // namespace gemm_tn_dev
 
+namespace gemm_tn_dev {
+namespace decode {
+
+// Few rows of A (decode-like M <= 32): the roles swap. 128 rows of B are the
+// MMA's M side and A's kN rows (zero-filled past M) its N side, so the
+// accumulator holds C^T for 128 columns of C. A stage then carries 16 KiB of B
+// and only kN * 128 bytes of A, and about twice the B bytes of the 128 x 128
+// split-K kernel are in flight per SM.
+constexpr int kThreads = 192;
+constexpr uint32_t kBTileBytes = 128 * 64 * 2;
+constexpr uint32_t kRingBudget = 200 * 1024;
+
+template <int kN>
+struct Layout {
+  static constexpr uint32_t kATileBytes = kN * 64 * 2;
+  static constexpr int kStages = static_cast<int>(kRingBudget / (kBTileBytes + kATileBytes));
+  static constexpr uint32_t kOffB = 0;
+  static constexpr uint32_t kOffA = kOffB + kStages * kBTileBytes;
+  static constexpr uint32_t kRingEnd = kOffA + kStages * kATileBytes;
+  static constexpr int kPartStride = kN + 4;                            // floats per partial row (n)
+  static constexpr uint32_t kPartBytes = 128 * kPartStride * 4;
+  static constexpr uint32_t kOffBar = kRingEnd;                          // full[S], empty[S], acc_full, drain
+  static constexpr int kNumBars = 2 * kStages + 2;
+  static constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+  static constexpr uint32_t kSmemBytes = kOffAbort + 4 + 1024;
+  static constexpr uint32_t kTmemCols = kN < 32 ? 32 : kN;
+  static_assert(kN == 16 || kN == 32, "A rows per MMA: 16 or 32");
+  static_assert(kATileBytes % 1024 == 0 && kBTileBytes % 1024 == 0, "swizzle atoms stay 1024-aligned");
+  static_assert(kPartBytes <= kRingEnd, "the partial tile fits in the idle ring");
+  static_assert(kSmemBytes <= 214 * 1024 + 256, "no more shared memory than the other GEMM kernels");
+};
+
+}  // namespace decode
+
+template <int S, int kN, bool kBf16>
+__global__ void __launch_bounds__(decode::kThreads, 1) gemm_tn_decode_kernel(const __grid_constant__ GemmArgs args) {
+  using L = decode::Layout<kN>;
+  static_assert(S == 2 || S == 4 || S == 8, "cluster of 2, 4 or 8 CTAs");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t base = smem_addr(smem);
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const uint32_t rank = cluster_ctarank();          // this CTA's slice of K
+  const int tn = static_cast<int>(blockIdx.x) / S;  // 128 columns of C (rows of B)
+  const int kb0 = static_cast<int>(static_cast<int64_t>(rank) * args.num_k_blocks / S);
+  const int kb1 = static_cast<int>(static_cast<int64_t>(rank + 1) * args.num_k_blocks / S);
+
+  auto b_tile = [&](int s) { return base + L::kOffB + s * decode::kBTileBytes; };
+  auto a_tile = [&](int s) { return base + L::kOffA + s * L::kATileBytes; };
+  auto full_bar = [&](int s) { return base + L::kOffBar + 8u * s; };
+  auto empty_bar = [&](int s) { return base + L::kOffBar + 8u * (L::kStages + s); };
+  const uint32_t acc_full_bar = base + L::kOffBar + 8u * (2 * L::kStages);
+  const uint32_t drain_bar = acc_full_bar + 8u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmemSlot);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kOffAbort);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(acc_full_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_descriptor(&args.tmap_a);
+    tma_prefetch_descriptor(&args.tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc<1>(smem_addr(tmem_slot), L::kTmemCols);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before_sync();
+  cluster_sync_all();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  // set-up may overlap the previous kernel in the stream; memory waits for it
+  griddep_wait();
+  griddep_launch_dependents();
+  const Watchdog<splitk::ClusterOf<S>> wd{&args, abort_flag, smem_addr(const_cast<uint32_t*>(abort_flag))};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued_phase_of[L::kStages];
+      for (int s = 0; s < L::kStages; ++s) issued_phase_of[s] = -1;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wd.wait(empty_bar(stage), phase ^ 1u)) break;
+        const uint32_t fb = full_bar(stage);
+        mbar_arrive_expect_tx(fb, decode::kBTileBytes + L::kATileBytes);
+        if (kb - kb0 != args.drop_load_kb) {
+          tma_load_2d(&args.tmap_b, b_tile(stage), fb, kb * 64, tn * 128);
+          tma_load_2d(&args.tmap_a, a_tile(stage), fb, kb * 64, 0);   // rows past M read as zero
+        }
+        issued_phase_of[stage] = static_cast<int>(phase);
+        if (++stage == L::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      for (int s = 0; s < L::kStages; ++s)
+        if (issued_phase_of[s] >= 0) wd.drain(full_bar(s), static_cast<uint32_t>(issued_phase_of[s]));
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer: D[n][m] += B[n][k] A[m][k]
+      constexpr uint32_t kIdesc = mma_idesc_f16(kBf16, 128, kN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wd.wait(full_bar(stage), phase)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t b_desc = sw128_kmajor_desc(b_tile(stage));
+        const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16<1>(tmem_base, b_desc + 2u * kk, a_desc + 2u * kk, kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+        mma_commit(empty_bar(stage));
+        if (++stage == L::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) mma_commit(acc_full_bar);
+      mma_commit(drain_bar);
+      wd.drain(drain_bar, 0);
+    }
+  } else {
+    // -------------------------------------------------------------- TMEM -> own shared memory
+    const uint32_t quarter = warp & 3u;
+    const bool ok = __all_sync(0xffffffffu, wd.wait(acc_full_bar, 0));
+    if (ok) {
+      tc_fence_after_sync();
+      const uint32_t row = quarter * 32u + lane;   // column n of this 128-column block
+      const uint32_t t_row = tmem_base + ((quarter * 32u) << 16);
+      const uint32_t dst = base + row * L::kPartStride * 4u;
+      if constexpr (kN == 16) {
+        uint32_t r[16];
+        tmem_load_32x16(t_row, r);
+        tmem_load_wait();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_shared_v4(dst + 16u * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+      } else {
+#pragma unroll 1
+        for (int chunk = 0; chunk < kN / 32; ++chunk) {
+          uint32_t r[32];
+          tmem_load_32x32(t_row + static_cast<uint32_t>(chunk * 32), r);
+          tmem_load_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(dst + 128u * chunk + 16u * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        }
+      }
+    }
+  }
+  __syncwarp();
+
+  // ---------------------------------------------------------------- cluster reduction
+  tc_fence_before_sync();
+  cluster_sync_all();
+  {
+    constexpr int kRows = 128 / S;          // columns of C (rows of the partial) this CTA finishes
+    const int r0 = static_cast<int>(rank) * kRows;
+    uint16_t* cbase = static_cast<uint16_t*>(args.c);
+    for (int idx = threadIdx.x; idx < kRows * (kN / 4); idx += decode::kThreads) {
+      const int nl = r0 + idx % kRows;       // consecutive threads: consecutive columns of C
+      const int m0 = (idx / kRows) * 4;
+      const int gn = tn * 128 + nl;
+      if (gn >= args.n || m0 >= args.m) continue;
+      const uint32_t off = base + static_cast<uint32_t>(nl * L::kPartStride + m0) * 4u;
+      float4 v[S];
+#pragma unroll
+      for (int s = 0; s < S; ++s) v[s] = splitk::ld_shared_cluster_f4(map_to_cta(off, static_cast<uint32_t>(s)));
+      float4 acc = v[0];
+#pragma unroll
+      for (int s = 1; s < S; ++s) {   // CTA order: the same sum on every launch
+        acc.x += v[s].x;
+        acc.y += v[s].y;
+        acc.z += v[s].z;
+        acc.w += v[s].w;
+      }
+      const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (m0 + j < args.m)
+          cbase[static_cast<int64_t>(m0 + j) * args.ldc + gn] =
+              static_cast<uint16_t>(splitk::pack2<kBf16>(vals[j], 0.0f) & 0xFFFFu);
+    }
+  }
+  // peers may still be reading this CTA's partial
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc<1>(tmem_base, L::kTmemCols);
+  }
+}
+
+}  // namespace gemm_tn_dev
 namespace gemm_tn_impl {
 namespace {
 
@@ -326,7 +536,69 @@ struct SplitKLauncher {
   }
 };
 
+template <int S, int kN, bool kBf16>
+struct DecodeLauncher {
+  static cudaError_t launch(const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream) {
+    using L = gemm_tn_dev::decode::Layout<kN>;
+    static std::atomic<uint64_t> done_mask{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(done_mask.load(std::memory_order_acquire) & bit)) {
+      e = cudaFuncSetAttribute(gemm_tn_dev::gemm_tn_decode_kernel<S, kN, kBf16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L::kSmemBytes));
+      if (e != cudaSuccess) return e;
+      done_mask.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(gemm_tn_dev::decode::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (dependent_launch_enabled()) {
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
+      cfg.numAttrs = 2;
+    }
+    return cudaLaunchKernelEx(&cfg, gemm_tn_dev::gemm_tn_decode_kernel<S, kN, kBf16>, args);
+  }
+};
+
+template <int kN, bool kBf16>
+cudaError_t launch_decode_rows(int splits, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream) {
+  switch (splits) {
+    case 2: return DecodeLauncher<2, kN, kBf16>::launch(args, grid, stream);
+    case 4: return DecodeLauncher<4, kN, kBf16>::launch(args, grid, stream);
+    case 8: return DecodeLauncher<8, kN, kBf16>::launch(args, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
+
+// Rows of A per MMA of the decode kernel for an M-row problem (0: M > 32).
+// With 33-64 rows the 128 x 128 split-K kernel measured as fast or faster
+// (64 x 2048 x 8192: 12.1 against 12.6 us): C's column-wise stores cost more.
+int decode_rows(int64_t m) { return m <= 16 ? 16 : m <= 32 ? 32 : 0; }
+
+cudaError_t launch_gemm_decode(int splits, int rows, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid,
+                               cudaStream_t stream) {
+  switch (rows) {
+    case 16: return bf16 ? launch_decode_rows<16, true>(splits, args, grid, stream)
+                         : launch_decode_rows<16, false>(splits, args, grid, stream);
+    case 32: return bf16 ? launch_decode_rows<32, true>(splits, args, grid, stream)
+                         : launch_decode_rows<32, false>(splits, args, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_gemm_splitk(int splits, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid,
                                cudaStream_t stream) {

@@ -47,7 +47,8 @@ def test_version_status_strings_and_configs(lib):
     assert gt.gemm_tn_status_string(gt.GEMM_TN_ERR_TIMEOUT) == "GEMM_TN_ERR_TIMEOUT"
     assert gt.gemm_tn_status_string(99) == "GEMM_TN_ERR_UNKNOWN"
     names = [gt.gemm_tn_config_name(i) for i in range(gt.gemm_tn_num_configs())]
-    assert names == ["1cta_n256", "1cta_n128", "2cta_n256", "2cta_n128", "2cta_n256_mc", "1cta_n128_splitk"]
+    assert names == ["1cta_n256", "1cta_n128", "2cta_n256", "2cta_n128", "2cta_n256_mc", "1cta_n128_splitk",
+                     "1cta_decode_splitk"]
     assert gt.gemm_tn_config_name(-1) == "invalid"
 
 
@@ -59,6 +60,8 @@ def test_config_table(lib, monkeypatch):
     assert sel(128, 1024, 4096) == "1cta_n128_splitk"     # 8 tiles x 8 splits
     assert sel(128, 4096, 4096) == "1cta_n128_splitk"     # 32 tiles x 4 splits
     assert sel(64, 2048, 8192) == "1cta_n128_splitk"      # 16 tiles: 4 splits (15 clusters of 8 fit at once)
+    assert sel(8, 4096, 4096) == "1cta_decode_splitk"     # <= 32 rows: B on the MMA's M side
+    assert sel(33, 4096, 4096) == "1cta_n128_splitk"
     assert sel(256, 256, 256) == "2cta_n256_mc"           # 4 k-blocks: too short to split
     assert sel(1024, 2048, 4096) == "2cta_n256_mc"        # 128 tiles: more than half the SMs
     # with GB300's resident clusters (76 pairs, 36 four-CTA clusters):

@@ -20,7 +20,8 @@ from _parity import (assert_parity, assert_sampled_parity, edge_indices, epilogu
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = ["1cta_n256", "1cta_n128", "2cta_n128", "2cta_n256", "2cta_n256_mc", "1cta_n128_splitk"]
+CONFIGS = ["1cta_n256", "1cta_n128", "2cta_n128", "2cta_n256", "2cta_n256_mc", "1cta_n128_splitk",
+           "1cta_decode_splitk"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -301,7 +302,7 @@ def test_plain_entry_point_and_host_entry_point_agree():
 
 # ------------------------------------------------------------ device watchdog
 
-@pytest.mark.parametrize("config", ["1cta_n256", "2cta_n256", "1cta_n128_splitk"])
+@pytest.mark.parametrize("config", ["1cta_n256", "2cta_n256", "1cta_n128_splitk", "1cta_decode_splitk"])
 def test_watchdog_reports_timeout_and_context_survives(config):
     """A wait that can never complete (the producer skips one k-block's loads
     through the test hook) must end within the watchdog budget with
@@ -432,6 +433,36 @@ def test_split_k_over_a_cluster(mnk, splits):
         outs.append(c.cpu())
     assert_parity(outs[0], a_cpu, b_cpu, f"{mnk} split {splits}")
     assert torch.equal(outs[0], outs[1]), "split-K launches differ"
+
+
+@pytest.mark.parametrize("splits", ["2", "4", "8"])
+@pytest.mark.parametrize("mnk", [(1, 4096, 4096), (8, 1000, 2048), (16, 300, 1000), (17, 640, 4097), (32, 129, 512),
+                                 (33, 4000, 8192), (64, 2048, 1024)], ids=lambda s: "x".join(map(str, s)))
+def test_decode_split_k(mnk, splits):
+    """At most 32 rows of A: B's rows on the MMA's M side and A's rows
+    (zero-filled to 16 or 32) on its N side (a forced decode configuration
+    with more rows runs the 128 x 128 split-K kernel), K split over a cluster, C
+    stored column by column: parity, nothing written past N into C's padded
+    pitch, and bit-identical results on repeated launches."""
+    from _parity import env_var
+    m, n, k = mnk
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "fp16", "normal_over_sqrt_k", seed=m * 7 + n + k + int(splits))
+    a, b = a_cpu.to(dev), b_cpu.to(dev)
+    ldc = n + 5
+    outs = []
+    for _ in range(2):
+        c_big = torch.full((m, ldc), float("nan"), dtype=torch.float16, device=dev)
+        c = c_big[:, :n]
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        with forced_config("1cta_decode_splitk"), env_var("GEMM_TN_SPLITK", splits):
+            gt.mm_tn(a, b, out=c, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.isnan(c_big[:, n:].float()).all(), "wrote past N"
+        outs.append(c.cpu())
+    assert_parity(outs[0], a_cpu, b_cpu, f"{mnk} decode split {splits}")
+    assert torch.equal(outs[0], outs[1]), "decode launches differ"
 
 
 def test_split_k_is_chosen_for_few_tiles_and_matches_whole_tiles():
