@@ -38,7 +38,17 @@
  *     The environment variable GEMM_TN_TEST_DROP_LOAD=<k-block> is a test
  *     hook of gemm_tn_ex: the kernel skips that k-block's loads of its first
  *     tiles so that a wait expires and the watchdog path runs.
- *   - Thread-safe: the only shared state is a per-device cache of attributes.
+ *   - Kernels are launched as programmatic dependents of the previous kernel
+ *     in `stream`: their set-up may overlap its end, but they touch memory
+ *     only once it has completed, so stream order holds as for any launch
+ *     (GEMM_TN_PDL=0 launches them plainly).
+ *   - The kernel configuration is chosen per call (gemm_tn_select_config).
+ *     Problems with few output tiles split K over a thread-block cluster and
+ *     add the fp32 partials in a fixed order; problems with one row of tiles
+ *     start each tile's K walk at a hashed k-block. Each configuration gives
+ *     bit-identical results on repeated calls.
+ *   - Thread-safe: the shared state is a per-device cache of attributes and
+ *     the launch counter (atomic).
  *   - Only compute capability 10.3 (GB300) devices are supported.
  */
 #ifndef GEMM_TN_H_
