@@ -406,27 +406,35 @@ __global__ void __launch_bounds__(C::kNumThreads) __maxnreg__(C::kMaxRegs)
           if (key0 + e >= limit) sv[e] = -INFINITY;
       }
       // probabilities against neg_m into the P columns; returns their sum
+      // The scaling and the four running sums use packed fp32 pairs (one
+      // instruction for two values, the same fp32 arithmetic per value): the
+      // pass is bound by issue slots as much as by the exponential unit.
       auto exp_pass = [&](float neg_m) {
-        float sum0 = 0.0f, sum1 = 0.0f, sum2 = 0.0f, sum3 = 0.0f;
+        const uint64_t cc = f32x2_pack(c_log2, c_log2), mm = f32x2_pack(neg_m, neg_m);
+        uint64_t s01 = f32x2_pack(0.0f, 0.0f), s23 = f32x2_pack(0.0f, 0.0f);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];   // 32 scores -> 16 columns of P
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             const float* x = sv + 32 * c + e;
-            const float p0 = ex2_approx(fmaf(x[0], c_log2, neg_m));
-            const float p1 = ex2_approx(fmaf(x[1], c_log2, neg_m));
-            const float p2 = ex2_approx(fmaf(x[2], c_log2, neg_m));
-            const float p3 = ex2_approx(fmaf(x[3], c_log2, neg_m));
-            sum0 += p0;
-            sum1 += p1;
-            sum2 += p2;
-            sum3 += p3;
+            float a0, a1, a2, a3;
+            f32x2_unpack(f32x2_fma(f32x2_pack(x[0], x[1]), cc, mm), a0, a1);
+            f32x2_unpack(f32x2_fma(f32x2_pack(x[2], x[3]), cc, mm), a2, a3);
+            const float p0 = ex2_approx(a0);
+            const float p1 = ex2_approx(a1);
+            const float p2 = ex2_approx(a2);
+            const float p3 = ex2_approx(a3);
+            s01 = f32x2_add(s01, f32x2_pack(p0, p1));
+            s23 = f32x2_add(s23, f32x2_pack(p2, p3));
             pk[e / 2] = fa::pack2<C::kBf16>(p0, p1);
             pk[e / 2 + 1] = fa::pack2<C::kBf16>(p2, p3);
           }
           tmem_store_32x16(p_col(32 * c), pk);
         }
+        float sum0, sum1, sum2, sum3;
+        f32x2_unpack(s01, sum0, sum1);
+        f32x2_unpack(s23, sum2, sum3);
         return (sum0 + sum1) + (sum2 + sum3);
       };
       auto row_max = [&]() {
