@@ -50,11 +50,11 @@ NCU_TRAFFIC_BYTES = {
     ("fp16_4096x4096x4096", "2cta_n256_mc"): 81_974_528 + 15_100_928,
     ("bf16_128x16384x16384", "1cta_n128"): 542_159_872 + 2_915_584,
     ("fp16_3001x5003x4097", "2cta_n256_mc"): 82_883_328 + 14_531_328,
-    ("bf16_8x4096x4096", "1cta_n128_splitk"): 33_637_888 + 0,
+    ("bf16_8x4096x4096", "1cta_decode_splitk"): 33_638_144 + 0,
 }
 # the same for the attention kernel, keyed by workload
 NCU_TRAFFIC_ATTN_BYTES: dict[str, int] = {
-    "attn_bf16_b2_s8192_h32_d128_causal": 450_154_496 + 113_367_552,
+    "attn_bf16_b2_s8192_h32_d128_causal": 453_134_336 + 116_694_016,
 }
 
 
@@ -329,7 +329,8 @@ def run_native(args, dist: Dist, peaks, peak_src):
     roofline["traffic"] = NCU_TRAFFIC_BYTES.get((w.name, cfg_name))
     roofline["algorithmic_bytes"] = compulsory
     roofline["peak_source"] = f"{peak_src} ({'hbm_gbs' if hbm_bound else 'bf16_tflops'} burst; kernel timed alone)"
-    roofline["kernel"] = ("gemm_tn_splitk_kernel" if cfg_name.endswith("splitk")
+    roofline["kernel"] = ("gemm_tn_decode_kernel" if cfg_name == "1cta_decode_splitk"
+                          else "gemm_tn_splitk_kernel" if cfg_name.endswith("splitk")
                           else f"gemm_tn_sm103_kernel<{cfg_name}>")
 
     # end to end through the host-buffer entry point
