@@ -154,18 +154,6 @@ __device__ __forceinline__ void tma_load_3d(const void* tmap, uint32_t dst, uint
       : "memory");
 }
 
-// 2-D tile load multicast to every CTA of `cta_mask` in this cluster: the box
-// lands at offset `dst` of each destination CTA's shared memory and each
-// destination's barrier at offset `bar` counts the bytes it received.
-__device__ __forceinline__ void tma_load_2d_multicast(const void* tmap, uint32_t dst, uint32_t bar, int32_t x,
-                                                      int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 // Multicast inside CTA pairs: the box lands at offset `dst` of every CTA in
 // `cta_mask`, and each destination pair's leader (even) CTA counts the bytes
 // on its barrier at the offset of `pair_bar` (a barrier address whose CTA
@@ -353,11 +341,6 @@ __device__ __forceinline__ void tmem_store_32x16(uint32_t taddr, const uint32_t 
       :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
-}
-
-// Named barrier `id` (1-15) over `count` threads (a multiple of 32).
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void tmem_store_wait() {
