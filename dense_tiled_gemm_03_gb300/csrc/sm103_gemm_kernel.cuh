@@ -811,17 +811,33 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
           if (args.out_f32) {
-            // fp32 output: each thread writes its row's 32 values (128 bytes)
-            if (row_ok) {
-              float* dst = static_cast<float*>(args.c) + rbase;
-              if (full && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+            // fp32 output: the warp's 32 rows x 32 values go through its 4 KiB
+            // staging block (16-byte units XOR-swizzled by row), then each
+            // store instruction writes 128 contiguous bytes of four rows
+            // instead of 16 bytes of 32 rows
+            __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  reinterpret_cast<float4*>(dst)[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            for (int u = 0; u < 8; ++u)
+              st_shared_v4(stage_addr + lane * 128u + ((static_cast<uint32_t>(u) ^ (lane & 7u)) * 16u),
+                           __float_as_uint(v[4 * u]), __float_as_uint(v[4 * u + 1]), __float_as_uint(v[4 * u + 2]),
+                           __float_as_uint(v[4 * u + 3]));
+            __syncwarp();
+            const uint32_t unit = lane & 7u;
+            const int col = col0 + static_cast<int>(unit) * 4;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t rr = static_cast<uint32_t>(i) * 4u + (lane >> 3);
+              const int row = row0 + static_cast<int>(rr);
+              const float4 val = *reinterpret_cast<const float4*>(warp_stage + rr * 128u + ((unit ^ (rr & 7u)) * 16u));
+              if (row >= args.m || col >= args.n) continue;
+              float* dst = static_cast<float*>(args.c) + static_cast<int64_t>(row) * args.ldc + col;
+              if (col + 4 <= args.n && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+                *reinterpret_cast<float4*>(dst) = val;
               } else {
+                const float e[4] = {val.x, val.y, val.z, val.w};
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (col0 + j < args.n) dst[j] = v[j];
+                for (int q = 0; q < 4; ++q)
+                  if (col + q < args.n) dst[q] = e[q];
               }
             }
             continue;
