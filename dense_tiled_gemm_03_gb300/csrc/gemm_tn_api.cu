@@ -317,6 +317,12 @@ int choose_config(int64_t m, int64_t n, int64_t k, int resident_pairs = 76, int 
   if (splitk_factor(m, n, k, 2 * resident_pairs, splitk_resident) > 1)
     return m <= 32 ? kCfgDecodeSplitK : kCfg1CtaSplitK;
   if (m <= 128) return kCfg1CtaN128;
+  // One round of single-CTA 128 x 128 tiles: every SM gets at most one tile,
+  // and a 128 x 128 tile is half the work of a pair's 256 x 256 (GB300, us
+  // per call in CUDA graphs, 1cta_n128 vs the pair / cluster choice: 256^3
+  // 4.31 vs 4.52, 1536 x 1536 x 256 4.52 vs 6.58, 1536 x 1536 x 2048 12.4 vs
+  // 14.5, 1024 x 2048 x 4096 20.9 vs 23.0).
+  if (((m + 127) / 128) * ((n + 127) / 128) <= 2 * static_cast<int64_t>(resident_pairs)) return kCfg1CtaN128;
   const int64_t tile_rows = (m + 255) / 256;
   const int64_t pair_tiles = tile_rows * ((n + 255) / 256);
   const int64_t quad_tiles = tile_rows * ((n + 511) / 512);

@@ -62,8 +62,9 @@ def test_config_table(lib, monkeypatch):
     assert sel(64, 2048, 8192) == "1cta_n128_splitk"      # 16 tiles: 4 splits (15 clusters of 8 fit at once)
     assert sel(8, 4096, 4096) == "1cta_decode_splitk"     # <= 32 rows: B on the MMA's M side
     assert sel(33, 4096, 4096) == "1cta_n128_splitk"
-    assert sel(256, 256, 256) == "2cta_n256_mc"           # 4 k-blocks: too short to split
-    assert sel(1024, 2048, 4096) == "2cta_n256_mc"        # 128 tiles: more than half the SMs
+    assert sel(256, 256, 256) == "1cta_n128"              # 4 k-blocks: too short to split; one round
+    assert sel(1024, 2048, 4096) == "1cta_n128"           # 128 tiles: one round of single-CTA tiles
+    assert sel(1280, 2048, 4096) == "2cta_n256_mc"        # 160 tiles: more than one round
     # with GB300's resident clusters (76 pairs, 36 four-CTA clusters):
     assert sel(8192, 8192, 8192) == "2cta_n256"      # 14 rounds of pair tiles vs 15 of multicast tiles
     assert sel(4096, 4096, 4096) == "2cta_n256_mc"   # 4 rounds either way: multicast streams more per SM
