@@ -323,6 +323,13 @@ int choose_config(int64_t m, int64_t n, int64_t k, int resident_pairs = 76, int 
   // 4.31 vs 4.52, 1536 x 1536 x 256 4.52 vs 6.58, 1536 x 1536 x 2048 12.4 vs
   // 14.5, 1024 x 2048 x 4096 20.9 vs 23.0).
   if (((m + 127) / 128) * ((n + 127) / 128) <= 2 * static_cast<int64_t>(resident_pairs)) return kCfg1CtaN128;
+  // One round of single-CTA 128 x 256 tiles, K up to 4096: the same work per
+  // SM as pair tiles without the pairs' cross-CTA hand-offs (2048^2 x 512 6.8
+  // vs 8.5 us, 2048^3 14.1 vs 15.5, 2304 x 2048 x 4096 22.9 vs 24.7). Longer K
+  // favours the pairs, whose CTAs stream 32 KiB per k-block against 48 KiB
+  // (2048^2 x 8192: 50.4 vs 41.9).
+  if (((m + 127) / 128) * ((n + 255) / 256) <= 2 * static_cast<int64_t>(resident_pairs) && k <= 4096)
+    return kCfg1CtaN256;
   const int64_t tile_rows = (m + 255) / 256;
   const int64_t pair_tiles = tile_rows * ((n + 255) / 256);
   const int64_t quad_tiles = tile_rows * ((n + 511) / 512);

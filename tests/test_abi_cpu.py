@@ -64,7 +64,10 @@ def test_config_table(lib, monkeypatch):
     assert sel(33, 4096, 4096) == "1cta_n128_splitk"
     assert sel(256, 256, 256) == "1cta_n128"              # 4 k-blocks: too short to split; one round
     assert sel(1024, 2048, 4096) == "1cta_n128"           # 128 tiles: one round of single-CTA tiles
-    assert sel(1280, 2048, 4096) == "2cta_n256_mc"        # 160 tiles: more than one round
+    assert sel(1280, 2048, 4096) == "1cta_n256"           # 160 tiles of 128 x 128, 80 of 128 x 256: one round
+    assert sel(2048, 2048, 2048) == "1cta_n256"
+    assert sel(2048, 2048, 8192) == "2cta_n256_mc"        # long K: pair tiles stream less per SM
+    assert sel(2560, 2560, 1024) == "2cta_n256_mc"        # 200 tiles of 128 x 256: more than one round
     # with GB300's resident clusters (76 pairs, 36 four-CTA clusters):
     assert sel(8192, 8192, 8192) == "2cta_n256"      # 14 rounds of pair tiles vs 15 of multicast tiles
     assert sel(4096, 4096, 4096) == "2cta_n256_mc"   # 4 rounds either way: multicast streams more per SM
