@@ -543,6 +543,40 @@ def test_cuda_graph_capture_and_replay():
     assert_parity(out.cpu(), a.cpu(), b_cpu, "graph replay after operand update")
 
 
+@pytest.mark.parametrize("mnk", [(128, 4096, 4096), (8, 4096, 4096), (256, 256, 256), (2048, 2048, 2048)],
+                         ids=["splitk", "decode", "one_round_128", "one_round_128x256"])
+def test_cuda_graph_chain_of_each_kernel_kind(mnk):
+    """Three dependent calls of one kernel kind (cluster split-K, decode,
+    single-CTA tiles) captured into a CUDA graph, where their programmatic
+    dependent launches become graph edges: C1 = A B^T, C2 = C1' ..., replayed
+    twice with the intermediate pre-filled with NaN; the results equal the
+    ones computed call by call with synchronisations."""
+    m, n, k = mnk
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "bf16", "normal_over_sqrt_k", seed=m + n)
+    a, b = a_cpu.to(dev), b_cpu.to(dev)
+    w = torch.randn(n, n, device=dev).to(torch.bfloat16) / n ** 0.5     # second GEMM: C2 = C1 W^T
+    c1 = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    c2 = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    gt.mm_tn(a, b, out=c1)
+    torch.cuda.synchronize()
+    gt.mm_tn(c1, w, out=c2)
+    torch.cuda.synchronize()
+    expected = c2.clone()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        c1.fill_(float("nan"))
+        gt.mm_tn(a, b, out=c1)
+        gt.mm_tn(c1, w, out=c2)
+    for _ in range(2):
+        c2.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(c2, expected), f"{mnk}: graph replay differs"
+
+
 def test_concurrent_calls_from_two_threads_on_two_streams():
     import threading
     dev = torch.device("cuda", 0)
