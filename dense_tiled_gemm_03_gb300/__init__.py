@@ -17,6 +17,9 @@ from ._native import (  # noqa: F401
     GEMM_TN_ERR_UNSUPPORTED_DTYPE,
     GEMM_TN_F16,
     GEMM_TN_OK,
+    GEMM_TN_OUT_E4M3,
+    GEMM_TN_OUT_F32,
+    GEMM_TN_OUT_INPUT,
     LIBRARY_PATH,
     GemmTnEpilogue,
     GemmTnError,

@@ -29,7 +29,7 @@ GEMM_TN_ERR_CUDA = 5
 GEMM_TN_ERR_TIMEOUT = 6
 
 GEMM_TN_ACT_NONE, GEMM_TN_ACT_RELU, GEMM_TN_ACT_GELU = 0, 1, 2
-GEMM_TN_OUT_INPUT, GEMM_TN_OUT_F32 = 0, 1
+GEMM_TN_OUT_INPUT, GEMM_TN_OUT_F32, GEMM_TN_OUT_E4M3 = 0, 1, 2
 
 
 class GemmTnEpilogue(ctypes.Structure):
@@ -245,10 +245,13 @@ def mm_tn(a, b, out=None, status=None):
 _ACTIVATIONS = {"none": GEMM_TN_ACT_NONE, "relu": GEMM_TN_ACT_RELU, "gelu": GEMM_TN_ACT_GELU}
 
 
-def mm_tn_fused(a, b, out=None, alpha=1.0, beta=0.0, bias=None, activation="none", out_fp32=False, status=None):
+def mm_tn_fused(a, b, out=None, alpha=1.0, beta=0.0, bias=None, activation="none", out_fp32=False, status=None,
+                out_dtype=None):
     """act(alpha * A x B^T + beta * out + bias) through gemm_tn_fused. a: [M, K],
-    b: [N, K] CUDA fp16/bf16; bias: optional fp32 CUDA [N]; out: [M, N] in
-    a's dtype, or fp32 with out_fp32 (its contents are read when beta != 0)."""
+    b: [N, K] CUDA fp16/bf16; bias: optional fp32 CUDA [N]; out: [M, N] of
+    out_dtype (its contents are read when beta != 0). out_dtype: None for a's
+    dtype, torch.float32 (or out_fp32=True), or torch.float8_e4m3fn for the
+    saturating fp8 output (alpha then carries the quantisation scale)."""
     import torch
     if a.device.type != "cuda" or b.device != a.device:
         raise ValueError("a and b must be CUDA tensors on one device")
@@ -258,15 +261,21 @@ def mm_tn_fused(a, b, out=None, alpha=1.0, beta=0.0, bias=None, activation="none
     n, kb = b.shape
     if kb != k:
         raise ValueError(f"inner dimensions differ: {tuple(a.shape)} x {tuple(b.shape)}^T")
-    out_dtype = torch.float32 if out_fp32 else a.dtype
+    if out_dtype is None:
+        out_dtype = torch.float32 if out_fp32 else a.dtype
+    elif out_fp32 and out_dtype != torch.float32:
+        raise ValueError("out_fp32 contradicts out_dtype")
+    codes = {a.dtype: GEMM_TN_OUT_INPUT, torch.float32: GEMM_TN_OUT_F32, torch.float8_e4m3fn: GEMM_TN_OUT_E4M3}
+    if out_dtype not in codes:
+        raise TypeError(f"unsupported output dtype {out_dtype}")
     if out is None:
         out = torch.zeros((m, n), dtype=out_dtype, device=a.device)
     elif out.shape != (m, n) or out.dtype != out_dtype or out.device != a.device:
-        raise ValueError("out must be [M, N] on a's device, fp32 with out_fp32 else a's dtype")
+        raise ValueError(f"out must be [M, N] of {out_dtype} on a's device")
     if bias is not None and (bias.dtype != torch.float32 or bias.shape != (n,) or bias.device != a.device):
         raise ValueError("bias must be a CUDA fp32 [N] tensor")
     ep = GemmTnEpilogue(float(alpha), float(beta), bias.data_ptr() if bias is not None else None,
-                        _ACTIVATIONS[activation], GEMM_TN_OUT_F32 if out_fp32 else GEMM_TN_OUT_INPUT)
+                        _ACTIVATIONS[activation], codes[out_dtype])
     lda, ldb, ldc = _row_pitch(a, k), _row_pitch(b, k), _row_pitch(out, n)
     d_status = status.data_ptr() if status is not None else None
     with _on_device(a.device) as stream:

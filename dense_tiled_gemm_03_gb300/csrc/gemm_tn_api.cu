@@ -44,7 +44,7 @@ cudaError_t launch_gemm_decode(int splits, int rows, bool bf16, const gemm_tn_de
 int decode_rows(int64_t m);
 int max_resident_splitk(int splits, bool bf16, int num_sms);
 constexpr int kGb300SplitKResidentDefault[3] = {76, 36, 15};
-cudaError_t launch_fused_k0(bool bf16, void* c, int64_t ldc, bool out_f32, int64_t m, int64_t n, float beta,
+cudaError_t launch_fused_k0(bool bf16, void* c, int64_t ldc, int out_kind, int64_t m, int64_t n, float beta,
                             const float* bias, int activation, int num_sms, cudaStream_t stream);
 
 namespace {
@@ -225,27 +225,34 @@ int encode_bshd_map(CUtensorMap* map, bool bf16, const void* ptr, int64_t batch,
 bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
 
 // Bytes spanned by a [rows, cols] matrix with pitch ld (16-bit elements).
-uintptr_t span_bytes(int64_t rows, int64_t cols, int64_t ld) {
-  return static_cast<uintptr_t>(((rows - 1) * ld + cols) * 2);
+uintptr_t span_bytes(int64_t rows, int64_t cols, int64_t ld, int64_t elem_bytes = 2) {
+  return static_cast<uintptr_t>(((rows - 1) * ld + cols) * elem_bytes);
+}
+
+// Bytes per element of C: the input dtype's 2, or the fused epilogue's
+// fp32 / e4m3 output.
+int64_t c_elem_bytes(const gemm_tn_epilogue* fused) {
+  if (fused == nullptr) return 2;
+  return fused->out_dtype == GEMM_TN_OUT_F32 ? 4 : (fused->out_dtype == GEMM_TN_OUT_E4M3 ? 1 : 2);
 }
 
 // b_mn: B is [K, N] (N contiguous, ldb >= n) instead of [N, K].
 int validate(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b, int64_t ldb,
-             const void* c, int64_t ldc, bool b_mn = false) {
+             const void* c, int64_t ldc, bool b_mn = false, int64_t c_elem = 2) {
   if (dtype != GEMM_TN_F16 && dtype != GEMM_TN_BF16) return fail(GEMM_TN_ERR_UNSUPPORTED_DTYPE, "dtype");
   if (m < 0 || n < 0 || k < 0 || m > kMaxDim || n > kMaxDim || k > kMaxDim)
     return fail(GEMM_TN_ERR_INVALID_VALUE, "sizes must be in [0, 2^31)");
   if (m == 0 || n == 0) return GEMM_TN_OK;
   if (c == nullptr) return fail(GEMM_TN_ERR_INVALID_VALUE, "C is NULL");
   if (ldc < n || ldc > kMaxDim * 2) return fail(GEMM_TN_ERR_INVALID_VALUE, "ldc < n");
-  if (reinterpret_cast<uintptr_t>(c) % 2) return fail(GEMM_TN_ERR_MISALIGNED, "C is not 2-byte aligned");
+  if (reinterpret_cast<uintptr_t>(c) % c_elem) return fail(GEMM_TN_ERR_MISALIGNED, "C is not aligned to its element");
   if (k == 0) return GEMM_TN_OK;
   if (a == nullptr || b == nullptr) return fail(GEMM_TN_ERR_INVALID_VALUE, "A or B is NULL");
   if (lda < k || ldb < (b_mn ? n : k) || lda > kMaxDim * 2 || ldb > kMaxDim * 2)
     return fail(GEMM_TN_ERR_INVALID_VALUE, b_mn ? "lda < k or ldb < n" : "lda or ldb < k");
   if (reinterpret_cast<uintptr_t>(a) % 2 || reinterpret_cast<uintptr_t>(b) % 2)
     return fail(GEMM_TN_ERR_MISALIGNED, "A or B is not 2-byte aligned");
-  const uintptr_t c0 = reinterpret_cast<uintptr_t>(c), c1 = c0 + span_bytes(m, n, ldc);
+  const uintptr_t c0 = reinterpret_cast<uintptr_t>(c), c1 = c0 + span_bytes(m, n, ldc, c_elem);
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), a1 = a0 + span_bytes(m, k, lda);
   const uintptr_t b0 = reinterpret_cast<uintptr_t>(b), b1 = b0 + (b_mn ? span_bytes(k, n, ldb) : span_bytes(n, k, ldb));
   if (ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1))
@@ -494,17 +501,18 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
              const gemm_tn_epilogue* fused = nullptr) {
   t_last_cuda_error = 0;
   t_last_message[0] = '\0';
-  int st = validate(dtype, m, n, k, a, lda, b, ldb, c, ldc, b_mn);
+  int st = validate(dtype, m, n, k, a, lda, b, ldb, c, ldc, b_mn, c_elem_bytes(fused));
   if (st != GEMM_TN_OK) return st;
   if (m == 0 || n == 0) return GEMM_TN_OK;
   DeviceFacts* dev = nullptr;
   st = current_device(&dev);
   if (st != GEMM_TN_OK) return st;
 
-  const bool out_f32 = fused != nullptr && fused->out_dtype == GEMM_TN_OUT_F32;
+  // C's element type in the fused epilogue: 0 the input dtype, 1 fp32, 2 e4m3
+  const int out_kind = fused == nullptr ? 0 : fused->out_dtype;
   if (k == 0) {  // the empty sum
     if (fused != nullptr) {
-      cudaError_t e = counted(launch_fused_k0(dtype == GEMM_TN_BF16, c, ldc, out_f32, m, n, fused->beta,
+      cudaError_t e = counted(launch_fused_k0(dtype == GEMM_TN_BF16, c, ldc, out_kind, m, n, fused->beta,
                                               fused->bias, fused->activation, dev->num_sms, stream));
       return e == cudaSuccess ? GEMM_TN_OK : fail_cuda(e, "fused epilogue (K = 0)");
     }
@@ -643,7 +651,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
                            CU_TENSOR_MAP_SWIZZLE_128B);
   // C goes out through the TMA when its base and pitch allow; otherwise the
   // epilogue's predicated element stores handle any 2-byte-aligned layout.
-  const bool c_tma = !out_f32 && tma_compatible(c, ldc) && !force_direct_epilogue();
+  const bool c_tma = out_kind == 0 && tma_compatible(c, ldc) && !force_direct_epilogue();
   if (st == GEMM_TN_OK && c_tma)
     st = encode_matrix_map(&args.tmap_c, bf16, c, m, n, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (st != GEMM_TN_OK) {
@@ -681,7 +689,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
     args.beta = fused->beta;
     args.bias = fused->bias;
     args.activation = fused->activation;
-    args.out_f32 = out_f32 ? 1 : 0;
+    args.out_kind = out_kind;
   }
 
   if (decode > 0)
@@ -827,22 +835,13 @@ int gemm_tn_fused(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int
   if (epilogue == nullptr) return fail(GEMM_TN_ERR_INVALID_VALUE, "epilogue is NULL");
   if (epilogue->activation < GEMM_TN_ACT_NONE || epilogue->activation > GEMM_TN_ACT_GELU)
     return fail(GEMM_TN_ERR_INVALID_VALUE, "unknown activation");
-  if (epilogue->out_dtype != GEMM_TN_OUT_INPUT && epilogue->out_dtype != GEMM_TN_OUT_F32)
+  if (epilogue->out_dtype != GEMM_TN_OUT_INPUT && epilogue->out_dtype != GEMM_TN_OUT_F32 &&
+      epilogue->out_dtype != GEMM_TN_OUT_E4M3)
     return fail(GEMM_TN_ERR_INVALID_VALUE, "unknown output dtype");
-  int st = validate(dtype, m, n, k, a, lda, b, ldb, c, ldc);
-  if (st != GEMM_TN_OK || m == 0 || n == 0) return st;
-  const int64_t out_elem = epilogue->out_dtype == GEMM_TN_OUT_F32 ? 4 : 2;
-  if (reinterpret_cast<uintptr_t>(c) % out_elem) return fail(GEMM_TN_ERR_MISALIGNED, "C is not aligned to its element");
   if (epilogue->bias != nullptr && reinterpret_cast<uintptr_t>(epilogue->bias) % 4)
     return fail(GEMM_TN_ERR_MISALIGNED, "bias is not 4-byte aligned");
-  if (k > 0) {  // an fp32 C spans twice the bytes the 16-bit overlap check assumed
-    const uintptr_t c0 = reinterpret_cast<uintptr_t>(c);
-    const uintptr_t c1 = c0 + static_cast<uintptr_t>(((m - 1) * ldc + n) * out_elem);
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), a1 = a0 + span_bytes(m, k, lda);
-    const uintptr_t b0 = reinterpret_cast<uintptr_t>(b), b1 = b0 + span_bytes(n, k, ldb);
-    if (ranges_overlap(c0, c1, a0, a1) || ranges_overlap(c0, c1, b0, b1))
-      return fail(GEMM_TN_ERR_INVALID_VALUE, "C overlaps A or B");
-  }
+  // C's alignment and its overlap with A and B are checked for C's own
+  // element size by run_gemm's validation
   return run_gemm(dtype, m, n, k, a, lda, b, ldb, c, ldc, d_status, reinterpret_cast<cudaStream_t>(stream),
                   test_drop_load_kb(), nullptr, 0, false, epilogue);
 }

@@ -85,11 +85,12 @@ struct GemmArgs {
   int32_t split_begin;
   int32_t dp_units;       // split_begin + (dp_tiles - split_begin) * split
   // Fused epilogue (kFused kernels): D = act(alpha * acc + beta * C + bias[j]),
-  // stored in the input dtype or (out_f32) as fp32.
+  // stored in C's element type out_kind: 0 the input dtype, 1 fp32, 2 fp8
+  // e4m3 (round to nearest even, saturating at +-448).
   float alpha, beta;
   const float* bias;      // nullable [N]
   int32_t activation;     // 0 none, 1 relu, 2 gelu
-  int32_t out_f32;
+  int32_t out_kind;
   float* partials;        // per CTA: block_n / 32 chunks x 128 rows x 32 fp32 (stream-K only)
   int* flags;             // per CTA and epilogue warp: 1 once its partial rows are written (zeroed by the host)
   // Memory-bound problems with one row of tiles (B streamed once, A re-read
@@ -758,7 +759,36 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             }
           }
           if (args.beta != 0.0f && row_ok) {
-            if (args.out_f32) {
+            if (args.out_kind == 2) {
+              // C's previous contents as e4m3 bytes, widened exactly
+              const uint8_t* src = static_cast<const uint8_t*>(args.c) + rbase;
+              if (full && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                  const uint4 t = reinterpret_cast<const uint4*>(src)[j];
+                  const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) {
+                    float f0, f1, f2, f3;
+                    e4m3x2_to_f32(w4[q] & 0xFFFFu, f0, f1);
+                    e4m3x2_to_f32(w4[q] >> 16, f2, f3);
+                    v[16 * j + 4 * q] += args.beta * f0;
+                    v[16 * j + 4 * q + 1] += args.beta * f1;
+                    v[16 * j + 4 * q + 2] += args.beta * f2;
+                    v[16 * j + 4 * q + 3] += args.beta * f3;
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  if (col0 + j < args.n) {
+                    float f, unused;
+                    e4m3x2_to_f32(src[j], f, unused);
+                    v[j] += args.beta * f;
+                  }
+                }
+              }
+            } else if (args.out_kind == 1) {
               const float* src = static_cast<const float*>(args.c) + rbase;
               if (full && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
 #pragma unroll
@@ -810,7 +840,42 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
           }
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);
-          if (args.out_f32) {
+          if (args.out_kind == 2) {
+            // e4m3 output: each row's 32 bytes go through the warp's staging
+            // block (two 16-byte halves, swapped on every other group of four
+            // rows so the writes spread over all banks), then each store
+            // instruction writes the full 32 bytes of 16 rows
+            uint32_t q8[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              q8[j] = cvt_e4m3x2(v[4 * j], v[4 * j + 1]) | (cvt_e4m3x2(v[4 * j + 2], v[4 * j + 3]) << 16);
+            __syncwarp();
+            const uint32_t flip = (lane >> 2) & 1u;
+            st_shared_v4(stage_addr + lane * 32u + (flip * 16u), q8[0], q8[1], q8[2], q8[3]);
+            st_shared_v4(stage_addr + lane * 32u + ((flip ^ 1u) * 16u), q8[4], q8[5], q8[6], q8[7]);
+            __syncwarp();
+            const uint32_t half16 = lane & 1u;
+            const int col = col0 + static_cast<int>(half16) * 16;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const uint32_t rr = static_cast<uint32_t>(i) * 16u + (lane >> 1);
+              const int row = row0 + static_cast<int>(rr);
+              const uint4 val =
+                  *reinterpret_cast<const uint4*>(warp_stage + rr * 32u + ((half16 ^ ((rr >> 2) & 1u)) * 16u));
+              if (row >= args.m || col >= args.n) continue;
+              uint8_t* dst = static_cast<uint8_t*>(args.c) + static_cast<int64_t>(row) * args.ldc + col;
+              if (col + 16 <= args.n && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+                *reinterpret_cast<uint4*>(dst) = val;
+              } else {
+                const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                  if (col + q < args.n) dst[q] = static_cast<uint8_t>(w[q >> 2] >> ((q & 3) * 8));
+              }
+            }
+            continue;
+          }
+          if (args.out_kind == 1) {
             // fp32 output: the warp's 32 rows x 32 values go through its 4 KiB
             // staging block (16-byte units XOR-swizzled by row), then each
             // store instruction writes 128 contiguous bytes of four rows

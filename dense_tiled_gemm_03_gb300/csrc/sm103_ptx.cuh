@@ -11,6 +11,8 @@
 // have completed. TMA copies decrement the byte count as they land.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include <cstdint>
 
 namespace gemm_tn_dev {
@@ -371,6 +373,26 @@ __device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
+}
+
+// ------------------------------------------------------------------ fp8 (e4m3) conversions
+
+// Two fp32 values rounded to nearest-even e4m3 with saturation (magnitudes
+// past the largest finite value 448 become +-448; NaN stays NaN). The result
+// holds `lo` in bits 0-7 and `hi` in bits 8-15, i.e. lo at the lower address
+// once stored.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Two e4m3 values (bits 0-7 and 8-15) widened exactly to fp32.
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t bits16, float& lo, float& hi) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(bits16)));
+  lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+  hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
 }
 
 // ------------------------------------------------------------------ special functions

@@ -106,22 +106,31 @@ GEMM_TN_API int gemm_tn_ex(int dtype, int64_t m, int64_t n, int64_t k, const voi
 
 /* Fused epilogue of gemm_tn_fused. */
 enum gemm_tn_activation { GEMM_TN_ACT_NONE = 0, GEMM_TN_ACT_RELU = 1, GEMM_TN_ACT_GELU = 2 };
-enum gemm_tn_out_dtype { GEMM_TN_OUT_INPUT = 0, GEMM_TN_OUT_F32 = 1 };
+enum gemm_tn_out_dtype { GEMM_TN_OUT_INPUT = 0, GEMM_TN_OUT_F32 = 1, GEMM_TN_OUT_E4M3 = 2 };
 typedef struct gemm_tn_epilogue {
   float alpha;        /* scale of A x B^T */
   float beta;         /* scale of C's previous contents; 0: C is not read */
   const float* bias;  /* nullable device fp32 [n], added to every row */
   int activation;     /* GEMM_TN_ACT_*: none, max(x, 0), or x * Phi(x) (erf form) */
-  int out_dtype;      /* GEMM_TN_OUT_INPUT: C has A's dtype; GEMM_TN_OUT_F32: C is fp32 */
+  int out_dtype;      /* GEMM_TN_OUT_INPUT: C has A's dtype; GEMM_TN_OUT_F32: C is fp32;
+                         GEMM_TN_OUT_E4M3: C is fp8 e4m3 (1 sign, 4 exponent bits with bias 7,
+                         3 mantissa bits; largest finite 448, no infinities) */
 } gemm_tn_epilogue;
 
 /*
  * gemm_tn_fused -- D = act(alpha * (A x B^T) + beta * C + bias[j]) written
  * over C, all in fp32 in the GEMM's epilogue before the one rounding to C's
  * dtype: the step after the GEMM done without another pass over C. A and B
- * as in gemm_tn_ex; C has ldc >= n elements per row of out_dtype (4-byte
- * aligned for fp32). K == 0 gives act(beta * C + bias). Same errors, watchdog
- * and workspace behaviour as gemm_tn_ex; the stream-K tail is not used.
+ * as in gemm_tn_ex; C has ldc >= n elements per row of out_dtype and is
+ * aligned to that element (4 bytes for fp32, 2 for fp16/bf16, none for e4m3).
+ * The e4m3 output is the fused form of a quantising pass after the GEMM:
+ * alpha carries the caller's quantisation scale, D rounds to nearest even
+ * with saturation (|D| past 448 stores +-448, NaN stays NaN), and with
+ * beta != 0 C's previous e4m3 contents are read back exactly. ("TileLang: a
+ * tile language one level below Triton", exercise 4: a quantisation to FP8
+ * is bandwidth-bound, so it belongs fused with the operator that produces
+ * its input.) K == 0 gives act(beta * C + bias). Same errors, watchdog and
+ * workspace behaviour as gemm_tn_ex; the stream-K tail is not used.
  */
 GEMM_TN_API int gemm_tn_fused(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b,
                               int64_t ldb, void* c, int64_t ldc, const gemm_tn_epilogue* epilogue, int* d_status,

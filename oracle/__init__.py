@@ -12,6 +12,10 @@ Contents:
     with NaN/Inf anywhere in c counted as a failure.
   * ``tiling_model``       -- the traffic / shared-memory model and the counted
     tiled loop of "Tiling a matmul" (pure Python).
+  * ``fused_reference``    -- the fused epilogue act(alpha * A x B^T + beta * C
+    + bias) written out element by element on top of gemm_tn_reference, with
+    ``fused_parity_report`` / ``fused_e4m3_parity_report`` carrying the
+    criterion through it (the latter for the fp8 e4m3 output, ``fp8``).
   * ``attention_reference`` -- the attention forward pass that consumes the
     GEMM (C, ``attention_oracle.c``): O = softmax(scale * Q K^T, causal mask) V
     per batch and head, with bound = sum_j p_j |V_j|; checked with the same
@@ -31,8 +35,9 @@ from dataclasses import dataclass
 import numpy as np
 
 from . import build as _build
+from . import fp8
 
-__all__ = ["attention_reference", "gemm_tn_reference", "gemm_nn_reference", "fused_reference", "fused_parity_report", "parity_report", "ParityReport", "ALLOW_REL", "ALLOW_ABS",
+__all__ = ["attention_reference", "gemm_tn_reference", "gemm_nn_reference", "fused_reference", "fused_parity_report", "fused_e4m3_parity_report", "fp8", "parity_report", "ParityReport", "ALLOW_REL", "ALLOW_ABS",
            "host_threads", "load_library"]
 
 #: The pass criterion's two constants: |c - ref| <= ALLOW_REL * bound + ALLOW_ABS.
@@ -203,6 +208,21 @@ def fused_parity_report(d, d_ref: np.ndarray, pre_bound: np.ndarray, activation=
         else parity_report(d, d_ref, pre_bound)
 
 
+def fused_e4m3_parity_report(codes, d_ref: np.ndarray, pre_bound: np.ndarray, activation=ACT_NONE) -> "ParityReport":
+    """The fused criterion for an e4m3 output (``codes``: the stored bytes).
+    Before its one rounding the kernel's fp32 value v is within
+    E = L * (1e-2 * pre_bound + 1e-3) of d_ref (fused_parity_report), and
+    clamping to [-448, 448] moves neither side apart. Rounding v to nearest
+    e4m3 then moves it by at most half a step: 2^-4 * |v| for normal values
+    (3 mantissa bits) and 2^-10 below 2^-6 (subnormal step 2^-9). So
+        |decode(codes) - clamp(d_ref)| <= E + 2^-4 * (|clamp(d_ref)| + E) + 2^-10."""
+    lip = ACT_LIPSCHITZ[activation]
+    e = lip * (ALLOW_REL * pre_bound + ALLOW_ABS)
+    target = np.clip(d_ref, -fp8.E4M3_MAX, fp8.E4M3_MAX)
+    allow = e + 2.0 ** -4 * (np.abs(target) + e) + 2.0 ** -10
+    return _report(fp8.e4m3_decode(codes), target, allow)
+
+
 @dataclass
 class ParityReport:
     ok: bool
@@ -223,14 +243,17 @@ def parity_report(c, ref: np.ndarray, bound: np.ndarray) -> ParityReport:
     c is the result under test (any dtype, widened to fp64); NaN or Inf in c
     fails (the inputs of every workload are finite and in range).
     """
-    C = _as_f64(c)
+    return _report(_as_f64(c), ref, ALLOW_REL * bound + ALLOW_ABS)
+
+
+def _report(C: np.ndarray, ref: np.ndarray, allow: np.ndarray) -> ParityReport:
+    """|C - ref| <= allow element-wise; non-finite entries of C fail."""
     if C.shape != ref.shape:
         raise ValueError(f"shape mismatch {C.shape} vs {ref.shape}")
     if C.size == 0:
         return ParityReport(True, 0.0, (), 0, 0, 0.0)
     finite = np.isfinite(C)
     err = np.abs(C - ref)
-    allow = ALLOW_REL * bound + ALLOW_ABS
     ratio = np.where(finite, err / allow, np.inf)
     flat = int(np.argmax(ratio))
     idx = tuple(int(v) for v in np.unravel_index(flat, ratio.shape))

@@ -140,6 +140,15 @@ def test_fused_entry_validation(lib):
     ep = gt.GemmTnEpilogue(1.0, 0.0, None, 0, 1)
     assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, B - 40, 4, ep, None, None) == gt.GEMM_TN_ERR_INVALID_VALUE
     assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, C, 4, None, None, None) == gt.GEMM_TN_ERR_INVALID_VALUE
+    # an e4m3 C (1-byte elements, any alignment) of 4 x 4 spans 16 bytes:
+    # starting 15 bytes before B overlaps it; out_dtype 3 does not exist
+    ep = gt.GemmTnEpilogue(1.0, 0.0, None, 0, gt.GEMM_TN_OUT_E4M3)
+    assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, B - 15, 4, ep, None, None) == gt.GEMM_TN_ERR_INVALID_VALUE
+    assert "overlaps" in gt.gemm_tn_last_error_message()
+    assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, C + 1, 3, ep, None, None) == gt.GEMM_TN_ERR_INVALID_VALUE
+    ep = gt.GemmTnEpilogue(1.0, 0.0, None, 0, 3)
+    assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, C, 4, ep, None, None) == gt.GEMM_TN_ERR_INVALID_VALUE
+    assert "output dtype" in gt.gemm_tn_last_error_message()
 
 
 # flash_attn_fwd (include/flash_attn.h): every argument error is reported

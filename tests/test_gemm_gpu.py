@@ -753,6 +753,79 @@ def test_fused_epilogue_k_zero(out_fp32):
     _fused_case(100, 70, 0, "fp16", "gelu", out_fp32, alpha=2.0, beta=0.5, with_bias=True, seed=3)
 
 
+def _fused_e4m3_case(m, n, k, dtype, activation, alpha, beta, with_bias, seed, ldc_pad=0):
+    """gemm_tn_fused with the fp8 e4m3 output, against the oracle's fp64 D and
+    the e4m3 criterion (rounding and saturation carried through)."""
+    import oracle
+    from oracle import fp8
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, dtype, "uniform", seed=seed)
+    g = torch.Generator().manual_seed(seed)
+    bias = (torch.rand(n, generator=g) * 8 - 4).float() if with_bias else None
+    # C's previous contents: random finite e4m3 codes; the padding holds NaN (0x7F)
+    codes_in = torch.randint(0, 256, (m, n), generator=g, dtype=torch.int32).to(torch.uint8)
+    codes_in[(codes_in & 0x7F) == 0x7F] = 0x3A
+    c_big = torch.full((m, n + ldc_pad), 0x7F, dtype=torch.uint8)
+    c_big[:, :n] = codes_in
+    c_big = c_big.to(dev).view(torch.float8_e4m3fn)
+    c = c_big[:, :n]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    gt.mm_tn_fused(a_cpu.to(dev), b_cpu.to(dev), out=c, alpha=alpha, beta=beta,
+                   bias=bias.to(dev) if bias is not None else None, activation=activation,
+                   out_dtype=torch.float8_e4m3fn, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    act = {"none": oracle.ACT_NONE, "relu": oracle.ACT_RELU, "gelu": oracle.ACT_GELU}[activation]
+    d_ref, pre_bound = oracle.fused_reference(a_cpu, b_cpu, alpha, beta, fp8.e4m3_decode(codes_in), bias, act)
+    rep = oracle.fused_e4m3_parity_report(c.cpu(), d_ref, pre_bound, act)
+    assert rep.ok, f"fused e4m3 {m}x{n}x{k} {dtype} {activation} a={alpha} b={beta}: {rep}"
+    if ldc_pad:
+        assert (c_big[:, n:].cpu().view(torch.uint8) == 0x7F).all(), "wrote outside C"
+
+
+@pytest.mark.parametrize("activation", ["none", "gelu"])
+@pytest.mark.parametrize("mnk,ldc_pad", [((129, 257, 65), 3), ((64, 640, 512), 0), ((1000, 1003, 200), 0),
+                                         ((300, 1024, 640), 0), ((77, 333, 128), 5)],
+                         ids=lambda s: "x".join(map(str, s)) if isinstance(s, tuple) else f"pad{s}")
+def test_fused_e4m3_parity(mnk, ldc_pad, activation):
+    m, n, k = mnk
+    # alpha as the quantisation scale: |D| reaches the top binades of e4m3
+    _fused_e4m3_case(m, n, k, "bf16", activation, alpha=8.0, beta=0.25, with_bias=True, seed=m * n + k,
+                     ldc_pad=ldc_pad)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_fused_e4m3_saturates(dtype):
+    """alpha far above the range: most outputs clamp to +-448 exactly."""
+    _fused_e4m3_case(260, 300, 256, dtype, "none", alpha=500.0, beta=0.0, with_bias=False, seed=4)
+
+
+def test_fused_e4m3_k_zero():
+    _fused_e4m3_case(100, 70, 0, "fp16", "relu", alpha=2.0, beta=0.5, with_bias=True, seed=3)
+
+
+@pytest.mark.parametrize("m", [100, 300])
+def test_fused_e4m3_exact_integers(m):
+    """Entries in {-1, 0, 1} and K = 16: every product sum is an integer in
+    [-16, 16], and times alpha = 16 still exact in e4m3 (at most 3 mantissa
+    bits), so the stored codes equal the oracle's encoding bit for bit (zero's
+    sign aside: +0 and -0 are the same value)."""
+    import oracle
+    from oracle import fp8
+    dev = torch.device("cuda", 0)
+    n, k = 520, 16
+    g = torch.Generator().manual_seed(m)
+    a_cpu = torch.randint(-1, 2, (m, k), generator=g).to(torch.bfloat16)
+    b_cpu = torch.randint(-1, 2, (n, k), generator=g).to(torch.bfloat16)
+    c = gt.mm_tn_fused(a_cpu.to(dev), b_cpu.to(dev), alpha=16.0, out_dtype=torch.float8_e4m3fn)
+    torch.cuda.synchronize()
+    d_ref, _ = oracle.fused_reference(a_cpu, b_cpu, alpha=16.0)
+    want = fp8.e4m3_encode(d_ref)
+    got = c.cpu().view(torch.uint8).numpy()
+    zero_sign = np.uint8(0x80)
+    assert np.array_equal(np.where(got == zero_sign, 0, got), np.where(want == zero_sign, 0, want))
+
+
 def test_fused_headline_shape_sampled():
     """bf16 8192^3 with bias + GELU and fp32 output: sampled rows and columns."""
     import oracle

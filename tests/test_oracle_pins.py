@@ -252,3 +252,84 @@ def test_fused_tolerance_scales_with_the_activation_slope():
     d = ref + 1.05 * (oracle.ALLOW_REL * 1.0 + oracle.ALLOW_ABS)   # 5% over the plain allowance
     assert not oracle.fused_parity_report(d, ref, pb, oracle.ACT_NONE).ok
     assert oracle.fused_parity_report(d, ref, pb, oracle.ACT_GELU).ok    # GELU allows 13% more
+
+
+# ------------------------------------------------------------ fp8 e4m3 output
+
+from oracle import fp8  # noqa: E402
+
+
+def test_e4m3_decode_landmarks():
+    """Codes whose values the format's definition fixes (sign, 4 exponent
+    bits with bias 7, 3 mantissa bits; e = 15 with m = 7 is NaN)."""
+    landmarks = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+                 0x39: 1.125, 0x40: 2.0, 0x77: 240.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    for code, value in landmarks.items():
+        assert fp8.e4m3_decode(np.array([code]))[0] == value, hex(code)
+    assert np.isnan(fp8.e4m3_decode(np.array([0x7F, 0xFF]))).all()
+    assert np.signbit(fp8.e4m3_decode(np.array([0x80]))[0])
+    vals = fp8.e4m3_decode(np.arange(256))
+    assert np.isnan(vals).sum() == 2
+    assert len(np.unique(vals[~np.isnan(vals)])) == 253          # +0 and -0 compare equal
+
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    """torch's float8_e4m3fn widening (a library routine) of all 256 codes."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    want = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = fp8.e4m3_decode(codes.numpy())
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    fin = ~np.isnan(want)
+    assert np.array_equal(got[fin], want[fin])
+    assert np.array_equal(np.signbit(got[fin]), np.signbit(want[fin]))
+
+
+def test_e4m3_round_trip_and_ties_to_even():
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    assert np.array_equal(fp8.e4m3_encode(fp8.e4m3_decode(finite)), finite.astype(np.uint8))
+    pos = fp8.e4m3_decode(np.arange(127))
+    mid = (pos[:-1] + pos[1:]) / 2                                 # exact in fp64
+    got = fp8.e4m3_encode(mid).astype(np.int64)
+    lower = np.arange(126)
+    assert np.array_equal(got, np.where(lower % 2 == 0, lower, lower + 1))
+    assert fp8.e4m3_encode(np.array([1.0 + 1 / 16]))[0] == 0x38   # tie: 1.0 (m = 000), not 1.125
+    assert fp8.e4m3_encode(np.array([1.0 + 3 / 16]))[0] == 0x3A   # tie: 1.25 (m = 010), not 1.125
+    # just off a midpoint, the nearer neighbour wins whatever its parity
+    assert fp8.e4m3_encode(np.array([1.0 + 1 / 16 + 1e-9]))[0] == 0x39
+
+
+def test_e4m3_saturation_and_special_values():
+    enc = fp8.e4m3_encode(np.array([448.0, 463.9, 464.0, 1e6, np.inf, -1e6, -np.inf, np.nan, -0.0, -1e-9, 2.0 ** -10]))
+    assert enc.tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE, 0x7F, 0x80, 0x80, 0x00]
+    # 3 * 2^-10 lies halfway between 2^-9 (0x01) and 2^-8 (0x02): the even code
+    assert fp8.e4m3_encode(np.array([3 * 2.0 ** -10]))[0] == 0x02
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    """torch's float8_e4m3fn rounding (a library routine) of fp32 values in the
+    finite range, where it and the saturating encoder agree by definition."""
+    g = np.random.Generator(np.random.PCG64(88))
+    x = np.concatenate([g.uniform(-448, 448, 20000), g.standard_normal(20000) * 4,
+                        g.uniform(-2.0 ** -5, 2.0 ** -5, 20000)]).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(fp8.e4m3_encode(x.astype(np.float64)), want)
+
+
+def test_e4m3_parity_allowance():
+    """The e4m3 criterion accepts the oracle's own rounding of d (and of the
+    saturated values) and rejects a code one step off where the step is larger
+    than the fp32 allowance."""
+    g = np.random.Generator(np.random.PCG64(5))
+    d = np.concatenate([g.uniform(-600, 600, 4000), g.uniform(-1, 1, 4000)]).reshape(80, 100)
+    pre_bound = np.abs(d)
+    rep = oracle.fused_e4m3_parity_report(fp8.e4m3_encode(d), d, pre_bound)
+    assert rep.ok, rep
+    codes = fp8.e4m3_encode(d)
+    bumped = codes.copy()
+    big = int(np.argmax(np.where(np.abs(d) < 300, np.abs(d), 0)))      # code <= 0x7A: +2 stays finite
+    bumped.flat[big] = codes.flat[big] + 2                              # two steps: over 2^-3 relative
+    assert np.isfinite(fp8.e4m3_decode(bumped.flat[big:big + 1]))[0]
+    assert not oracle.fused_e4m3_parity_report(bumped, d, np.zeros_like(d)).ok
+    nan = codes.copy()
+    nan.flat[7] = 0x7F
+    assert not oracle.fused_e4m3_parity_report(nan, d, pre_bound).ok
