@@ -37,6 +37,7 @@ from ._native import (  # noqa: F401
     gemm_tn_last_error_message,
     gemm_tn_num_configs,
     gemm_tn_select_config,
+    gemm_tn_select_splits,
     gemm_tn_status_string,
     gemm_tn_version,
     gemm_tn_launch_count,

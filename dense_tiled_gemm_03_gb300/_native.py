@@ -54,6 +54,7 @@ _SIGNATURES = {
     "gemm_tn_ex_noalloc": (_int, [_int, _i64, _i64, _i64, _ptr, _i64, _ptr, _i64, _ptr, _i64, _ptr, _ptr]),
     "gemm_tn_host": (_int, [_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr]),
     "gemm_tn_select_config": (_int, [_int, _i64, _i64, _i64]),
+    "gemm_tn_select_splits": (_int, [_int, _i64, _i64, _i64]),
     "gemm_tn_num_configs": (_int, []),
     "gemm_tn_config_name": (ctypes.c_char_p, [_int]),
     "gemm_tn_status_string": (ctypes.c_char_p, [_int]),
@@ -138,6 +139,10 @@ def flash_attn_fwd(dtype, batch, seq, heads, head_dim, q, k, v, o, softmax_scale
 
 def gemm_tn_select_config(dtype, m, n, k) -> int:
     return library().gemm_tn_select_config(dtype, m, n, k)
+
+
+def gemm_tn_select_splits(dtype, m, n, k) -> int:
+    return library().gemm_tn_select_splits(dtype, m, n, k)
 
 
 def gemm_tn_num_configs() -> int:

@@ -294,11 +294,15 @@ int parse_forced_config() {
 // worth it). With fewer 128 x 128 tiles than half the SMs, each tile's K is
 // cut over a cluster of S CTAs, S the largest of 8, 4, 2 whose clusters are
 // all resident at once (resident[0..2]: clusters of 2, 4, 8 CTAs; GB300: 76,
-// 36, 15) and that leaves at least 4 k-blocks per CTA. Measured on GB300
-// (CUDA graphs, us per call, no split -> split): 128 x 1024 x 4096 19.8 ->
-// 6.9 (S = 8), 64 x 2048 x 8192 38.5 -> 12.2 (S = 4; 16 clusters of 8 do not
-// fit at once and took 17.2), 1024 x 1024 x 8192 39.5 -> 20.9 (S = 2); 256^3
-// (4 k-blocks) stays whole. GEMM_TN_SPLITK=<S> forces S (0 turns it off).
+// 36, 15) and that leaves enough k-blocks per CTA: 4 for S = 2 and 8, 2 for
+// S = 4. Measured on GB300 (CUDA graphs, us per call, no split -> split):
+// 128 x 1024 x 4096 19.8 -> 6.9 (S = 8), 64 x 2048 x 8192 38.5 -> 12.2 (S = 4;
+// 16 clusters of 8 do not fit at once and took 17.2), 1024 x 1024 x 8192 39.5
+// -> 20.9 (S = 2); 256^3 (4 k-blocks) stays whole. With 8 to 15 k-blocks S = 4
+// beat S = 2 on every shape tried (S = 2 -> 4: 256 x 256 x 512 5.64 -> 4.85,
+// 512 x 512 x 896 6.67 -> 5.43, 768^3 6.36 -> 5.95, 640 x 640 x 512 5.74 ->
+// 5.33), and S = 2 was at times slower than no split (5.34 and 5.43 there).
+// GEMM_TN_SPLITK=<S> forces S (0 turns it off).
 int splitk_factor(int64_t m, int64_t n, int64_t k, int sms, const int resident[3]) {
   const int64_t tiles = ((m + 127) / 128) * ((n + 127) / 128);
   const int64_t kb = (k + 63) / 64;
@@ -310,9 +314,21 @@ int splitk_factor(int64_t m, int64_t n, int64_t k, int sms, const int resident[3
   }
   if (tiles * 2 > sms) return 0;
   const int splits_of[3] = {2, 4, 8};
+  const int min_kb_per_cta[3] = {4, 2, 4};
   for (int i = 2; i >= 0; --i)
-    if (tiles <= resident[i] && kb >= 4 * splits_of[i]) return splits_of[i];
+    if (tiles <= resident[i] && kb >= min_kb_per_cta[i] * splits_of[i]) return splits_of[i];
   return 0;
+}
+
+// The K split a split-K configuration runs with: splitk_factor's choice, or
+// for a forced split-K configuration the largest split that K allows; 0 when
+// K cannot be cut (the call then runs whole 128 x 128 tiles) or B is [K, N].
+int resolve_splits(int64_t m, int64_t n, int64_t k, bool b_mn, int sms, const int resident[3]) {
+  if (b_mn) return 0;
+  int splits = splitk_factor(m, n, k, sms, resident);
+  for (int s : {8, 4, 2})
+    if (splits == 0 && s <= (k + kBlockK - 1) / kBlockK) splits = s;
+  return splits >= 2 ? splits : 0;
 }
 
 int choose_config(int64_t m, int64_t n, int64_t k, int resident_pairs = 76, int resident_quads = 36,
@@ -537,11 +553,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
     cfg_id = decode > 0 ? kCfgDecodeSplitK : kCfg1CtaSplitK;
   }
   if (cfg_id == kCfg1CtaSplitK || cfg_id == kCfgDecodeSplitK) {
-    if (!b_mn) {
-      splits = splitk_factor(m, n, k, dev->num_sms, sk_resident);
-      for (int s : {8, 4, 2})
-        if (splits == 0 && s <= (k + kBlockK - 1) / kBlockK) splits = s;
-    }
+    splits = resolve_splits(m, n, k, b_mn, dev->num_sms, sk_resident);
     if (splits < 2) {
       cfg_id = kCfg1CtaN128;
       decode = 0;
@@ -1008,30 +1020,55 @@ int flash_attn_fwd(int dtype, int64_t batch, int64_t seq, int64_t heads, int64_t
   return GEMM_TN_OK;
 }
 
-int gemm_tn_select_config(int dtype, int64_t m, int64_t n, int64_t k) {
-  if (dtype != GEMM_TN_F16 && dtype != GEMM_TN_BF16) return -1;
-  if (m <= 0 || n <= 0 || k <= 0 || m > kMaxDim || n > kMaxDim || k > kMaxDim) return -1;
-  // resident cluster counts of the current device when it is a GB300,
-  // otherwise GB300's (76 CTA pairs, 36 four-CTA clusters)
-  int pairs = 76, quads = 36;
-  int sk[3] = {kGb300SplitKResidentDefault[0], kGb300SplitKResidentDefault[1], kGb300SplitKResidentDefault[2]};
+namespace {
+
+// What the selection sees for a dtype on the current device: resident CTA
+// pairs, 4-CTA clusters, split-K clusters of 2, 4, 8 CTAs, and SMs; GB300's
+// when there is no usable device.
+void selection_facts(int dtype, int* pairs, int* quads, int sk[3], int* sms) {
+  *pairs = 76;
+  *quads = 36;
+  *sms = 152;
+  for (int i = 0; i < 3; ++i) sk[i] = kGb300SplitKResidentDefault[i];
   int dev = -1;
-  if (cudaGetDevice(&dev) == cudaSuccess) {
-    DeviceFacts* facts = nullptr;
-    if (current_device(&facts) == GEMM_TN_OK) {
-      const bool bf16 = dtype == GEMM_TN_BF16;
-      const int p = resident_clusters(facts, kCfg2CtaN256, bf16);
-      const int q = resident_clusters(facts, kCfg2CtaN256Mc, bf16);
-      if (p > 0 && q > 0) {
-        pairs = p;
-        quads = q;
-      }
-      splitk_resident(facts, bf16, sk);
-    }
-  } else {
+  if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
+    return;
   }
+  DeviceFacts* facts = nullptr;
+  if (current_device(&facts) != GEMM_TN_OK) return;
+  const bool bf16 = dtype == GEMM_TN_BF16;
+  const int p = resident_clusters(facts, kCfg2CtaN256, bf16);
+  const int q = resident_clusters(facts, kCfg2CtaN256Mc, bf16);
+  if (p > 0 && q > 0) {
+    *pairs = p;
+    *quads = q;
+  }
+  splitk_resident(facts, bf16, sk);
+  *sms = facts->num_sms;
+}
+
+bool selectable(int dtype, int64_t m, int64_t n, int64_t k) {
+  return (dtype == GEMM_TN_F16 || dtype == GEMM_TN_BF16) && m > 0 && n > 0 && k > 0 && m <= kMaxDim &&
+         n <= kMaxDim && k <= kMaxDim;
+}
+
+}  // namespace
+
+int gemm_tn_select_config(int dtype, int64_t m, int64_t n, int64_t k) {
+  if (!selectable(dtype, m, n, k)) return -1;
+  int pairs, quads, sms, sk[3];
+  selection_facts(dtype, &pairs, &quads, sk, &sms);
   return choose_config(m, n, k, pairs, quads, sk);
+}
+
+int gemm_tn_select_splits(int dtype, int64_t m, int64_t n, int64_t k) {
+  if (!selectable(dtype, m, n, k)) return 0;
+  int pairs, quads, sms, sk[3];
+  selection_facts(dtype, &pairs, &quads, sk, &sms);
+  const int cfg = choose_config(m, n, k, pairs, quads, sk);
+  if (cfg != kCfg1CtaSplitK && cfg != kCfgDecodeSplitK) return 0;
+  return resolve_splits(m, n, k, false, sms, sk);
 }
 
 int gemm_tn_num_configs(void) { return kNumConfigs; }

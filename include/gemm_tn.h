@@ -198,6 +198,14 @@ GEMM_TN_API int gemm_tn_host(int dtype, int64_t m, int64_t n, int64_t k, const v
  * overrides the table. */
 GEMM_TN_API int gemm_tn_select_config(int dtype, int64_t m, int64_t n, int64_t k);
 
+/* K split gemm_tn_ex would run for this problem on the current device when
+ * the chosen configuration is a split-K one (1cta_n128_splitk or
+ * 1cta_decode_splitk): the number of CTAs of a cluster that share one
+ * output tile's K (2, 4 or 8). 0 for every other configuration, or for a
+ * no-op / invalid size. GEMM_TN_FORCE_CONFIG and GEMM_TN_SPLITK apply as in
+ * gemm_tn_ex. Host-only: launches nothing. */
+GEMM_TN_API int gemm_tn_select_splits(int dtype, int64_t m, int64_t n, int64_t k);
+
 /* Number of kernel configurations, and the name of one ("1cta_n256", ...,
  * "1cta_n128_splitk": K split over a cluster of 2, 4 or 8 CTAs per 128 x 128
  * tile, chosen when the tiles fill less than half the SMs; "1cta_decode_splitk":

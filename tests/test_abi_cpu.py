@@ -63,6 +63,15 @@ def test_config_table(lib, monkeypatch):
     assert sel(8, 4096, 4096) == "1cta_decode_splitk"     # <= 32 rows: B on the MMA's M side
     assert sel(33, 4096, 4096) == "1cta_n128_splitk"
     assert sel(256, 256, 256) == "1cta_n128"              # 4 k-blocks: too short to split; one round
+    splits = lambda m, n, k: gt.gemm_tn_select_splits(gt.GEMM_TN_F16, m, n, k)
+    assert splits(128, 1024, 4096) == 8                   # 8 tiles, 64 k-blocks
+    assert splits(64, 2048, 8192) == 4                    # 16 tiles: more than 15 clusters of 8
+    assert splits(1024, 1024, 8192) == 2                  # 64 tiles: more than 36 clusters of 4
+    assert splits(512, 512, 512) == 4                     # 8 k-blocks: 2 per CTA of a 4-CTA cluster
+    assert splits(256, 256, 960) == 4
+    assert splits(256, 256, 1024) == 4                    # 16 k-blocks: 8 splits would leave 2 per CTA
+    assert splits(8, 4096, 4096) == 4                     # the decode kernel's split
+    assert splits(256, 256, 256) == 0 and splits(8192, 8192, 8192) == 0 and splits(0, 5, 5) == 0
     assert sel(1024, 2048, 4096) == "1cta_n128"           # 128 tiles: one round of single-CTA tiles
     assert sel(1280, 2048, 4096) == "1cta_n256"           # 160 tiles of 128 x 128, 80 of 128 x 256: one round
     assert sel(2048, 2048, 2048) == "1cta_n256"
