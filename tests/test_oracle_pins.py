@@ -233,6 +233,30 @@ def test_fused_reference_closed_forms():
     np.testing.assert_array_equal(d, np.maximum(exact, 0.0))
 
 
+def test_fused_reference_all_terms_and_bound():
+    """Every term at once with exactly representable scales: D = 2 A B^T +
+    0.5 C_in + bias and pre_bound = 2 sum|a b| + |0.5 C_in| + |bias|, both
+    exact (integer operands, dyadic scales); B given [K, N] (b_kn) gives the
+    same D."""
+    a = _rand((8, 16), torch.float16, 502, kind="int")
+    b = _rand((6, 16), torch.float16, 503, kind="int")
+    exact = (a.long() @ b.long().T).double().numpy()
+    abs_sum = (a.long().abs() @ b.long().abs().T).double().numpy()
+    c_in = (torch.arange(48, dtype=torch.float32).reshape(8, 6) - 20) / 4
+    bias = torch.tensor([0.5, -1.0, 2.0, 0.0, -0.25, 4.0])
+    d, pb = oracle.fused_reference(a, b, alpha=2.0, beta=0.5, c_in=c_in, bias=bias)
+    cin, bb = c_in.double().numpy(), bias.double().numpy()[None, :]
+    np.testing.assert_array_equal(d, 2.0 * exact + 0.5 * cin + bb)
+    np.testing.assert_array_equal(pb, 2.0 * abs_sum + np.abs(0.5 * cin) + np.abs(bb))
+    d_kn, pb_kn = oracle.fused_reference(a, b.T.contiguous(), alpha=2.0, beta=0.5, c_in=c_in, bias=bias, b_kn=True)
+    np.testing.assert_array_equal(d_kn, d)
+    np.testing.assert_array_equal(pb_kn, pb)
+    # a negative alpha flips D but not the bound
+    d_neg, pb_neg = oracle.fused_reference(a, b, alpha=-2.0)
+    np.testing.assert_array_equal(d_neg, -2.0 * exact)
+    np.testing.assert_array_equal(pb_neg, 2.0 * abs_sum)
+
+
 def test_gelu_reference_properties():
     """GELU(x) = x * Phi(x): GELU(0) = 0, GELU(x) - GELU(-x) = x, Phi(1) and
     Phi(2) from the normal CDF's tabulated values, and GELU(x) ~ x for large x."""
