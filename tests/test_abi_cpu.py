@@ -135,6 +135,46 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 
 
+def test_split_choice_invariants(lib, monkeypatch):
+    """Over a grid of shapes, a split-K choice always has every cluster
+    resident at once (GB300 without a device: 76 clusters of 2, 36 of 4, 15 of
+    8), at most half the SMs' worth of tiles, and enough k-blocks per CTA (4,
+    or 2 in a 4-way split); any other configuration reports no split."""
+    monkeypatch.delenv("GEMM_TN_FORCE_CONFIG", raising=False)
+    monkeypatch.delenv("GEMM_TN_SPLITK", raising=False)
+    resident = {2: 76, 4: 36, 8: 15}
+    min_kb = {2: 4, 4: 2, 8: 4}
+    split_cfgs = {"1cta_n128_splitk", "1cta_decode_splitk"}
+    seen = set()
+    for m in (1, 8, 32, 33, 128, 200, 256, 512, 1024, 2048):
+        for n in (64, 256, 512, 1000, 2048, 4096, 8192):
+            for k in (64, 256, 512, 960, 1024, 4096, 16384):
+                s = gt.gemm_tn_select_splits(gt.GEMM_TN_BF16, m, n, k)
+                cfg = gt.gemm_tn_config_name(gt.gemm_tn_select_config(gt.GEMM_TN_BF16, m, n, k))
+                if cfg not in split_cfgs:
+                    assert s == 0, (m, n, k, cfg, s)
+                    continue
+                tiles = -(-m // 128) * -(-n // 128)
+                kb = -(-k // 64)
+                assert s in resident, (m, n, k, s)
+                assert tiles <= resident[s] and 2 * tiles <= 152, (m, n, k, s, tiles)
+                assert kb >= min_kb[s] * s, (m, n, k, s, kb)
+                seen.add(s)
+    assert seen == {2, 4, 8}
+
+
+def test_split_override_is_reported(lib, monkeypatch):
+    monkeypatch.delenv("GEMM_TN_FORCE_CONFIG", raising=False)
+    monkeypatch.setenv("GEMM_TN_SPLITK", "2")
+    assert gt.gemm_tn_select_splits(gt.GEMM_TN_F16, 128, 1024, 4096) == 2
+    monkeypatch.setenv("GEMM_TN_SPLITK", "0")           # off: whole tiles, no split
+    assert gt.gemm_tn_select_splits(gt.GEMM_TN_F16, 128, 1024, 4096) == 0
+    monkeypatch.delenv("GEMM_TN_SPLITK")
+    monkeypatch.setenv("GEMM_TN_FORCE_CONFIG", "1cta_n128_splitk")   # forced: the largest split K allows
+    assert gt.gemm_tn_select_splits(gt.GEMM_TN_F16, 4096, 4096, 256) == 4
+    assert gt.gemm_tn_select_splits(gt.GEMM_TN_F16, 4096, 4096, 64) == 0
+
+
 def test_fused_entry_validation(lib):
     ep = gt.GemmTnEpilogue(1.0, 0.0, None, 7, 0)
     assert gt.gemm_tn_fused(0, 4, 4, 4, A, 4, B, 4, C, 4, ep, None, None) == gt.GEMM_TN_ERR_INVALID_VALUE
