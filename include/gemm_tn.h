@@ -42,7 +42,8 @@
  *     in `stream`: their set-up may overlap its end, but they touch memory
  *     only once it has completed, so stream order holds as for any launch
  *     (GEMM_TN_PDL=0 launches them plainly).
- *   - The kernel configuration is chosen per call (gemm_tn_select_config).
+ *   - The kernel configuration is chosen per call (gemm_tn_select_config;
+ *     gemm_tn_select_splits gives the K split of the split-K ones).
  *     Problems with few output tiles split K over a thread-block cluster and
  *     add the fp32 partials in a fixed order; problems with one row of tiles
  *     start each tile's K walk at a hashed k-block. Each configuration gives
