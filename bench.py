@@ -52,9 +52,24 @@ NCU_TRAFFIC_BYTES = {
     ("fp16_3001x5003x4097", "2cta_n256_mc"): 82_883_328 + 14_531_328,
     ("bf16_8x4096x4096", "1cta_decode_splitk"): 33_638_144 + 0,
 }
+# the same for the fused kernels, keyed by (workload, configuration, epilogue)
+NCU_TRAFFIC_FUSED_BYTES: dict[tuple[str, str, str], int] = {
+    ("bf16_8192x8192x8192", "2cta_n256", "e4m3"): 1_053_888_512 + 63_751_680,
+}
+
 # the same for the attention kernel, keyed by workload
 NCU_TRAFFIC_ATTN_BYTES: dict[str, int] = {
     "attn_bf16_b2_s8192_h32_d128_causal": 453_134_336 + 116_694_016,
+}
+
+
+# fused epilogues the benchmark can time: (alpha, bias?, activation, output dtype name or None for A's)
+EPILOGUES = {
+    "none": None,
+    "bias": (1.0, True, "none", None),
+    "bias_gelu": (1.0, True, "gelu", None),
+    "fp32": (1.0, False, "none", "float32"),
+    "e4m3": (1.0 / 16, False, "none", "float8_e4m3fn"),   # alpha as the quantisation scale
 }
 
 
@@ -69,6 +84,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--config", default=None, help="force a kernel configuration (GEMM_TN_FORCE_CONFIG)")
+    ap.add_argument("--epilogue", default="none", choices=sorted(EPILOGUES),
+                    help="time gemm_tn_fused with this epilogue instead of the plain gemm_tn (GEMM workloads; "
+                         "no end-to-end figure: the host-buffer entry point has no fused form)")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="budget of the whole --impl reference run (oracle work)")
     ap.add_argument("--cublas-context", action="store_true",
@@ -263,9 +281,22 @@ def run_native(args, dist: Dist, peaks, peak_src):
     op_bytes = (w.m * w.k + w.n * w.k) * 2
     flush = op_bytes < 2 * L2_BYTES
     scratch = torch.empty(L2_BYTES * 2 // 4, dtype=torch.int32, device=dev) if flush else None
+    fused = EPILOGUES[args.epilogue]
+    c_elem = 2
+    if fused is None:
+        def step():
+            gt.mm_tn(a, b, out=c, status=status)
+    else:
+        alpha, with_bias, act, out_name = fused
+        out_dtype = getattr(torch, out_name) if out_name else a.dtype
+        c = torch.empty((w.m, w.n), dtype=out_dtype, device=dev)
+        c_elem = c.element_size()
+        bias = torch.linspace(-1.0, 1.0, w.n, dtype=torch.float32, device=dev) if with_bias else None
+        # the fused kernels: single-CTA 128 x 128 tiles where the plain choice is those, else pairs
+        cfg_name = cfg_name if cfg_name == "1cta_n128" else ("1cta_n128" if w.m <= 128 else "2cta_n256")
 
-    def step():
-        gt.mm_tn(a, b, out=c, status=status)
+        def step():
+            gt.mm_tn_fused(a, b, out=c, alpha=alpha, bias=bias, activation=act, out_dtype=out_dtype, status=status)
 
     for _ in range(args.warmup):
         if flush:
@@ -314,8 +345,8 @@ def run_native(args, dist: Dist, peaks, peak_src):
     # roofline of the dominant (only) kernel of the step
     tensor_peak = float(peaks["bf16_tflops"])
     hbm_peak = float(peaks["hbm_gbs"])
-    # algorithmic bytes: each operand read once, C written once (2 B per element)
-    compulsory = (w.m * w.k + w.n * w.k + w.m * w.n) * 2
+    # algorithmic bytes: each operand read once, C written once (in its own element size)
+    compulsory = (w.m * w.k + w.n * w.k) * 2 + w.m * w.n * c_elem
     hbm_bound = hbm_peak * 1e9 * (w.flops / compulsory) < tensor_peak * 1e12
     if hbm_bound:
         achieved = compulsory / (avg_launch_ms * 1e-3) / 1e9
@@ -326,25 +357,29 @@ def run_native(args, dist: Dist, peaks, peak_src):
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak, "unit": "TFLOP/s",
                     "frac": round(achieved / tensor_peak, 4),
                     "frac_of_sustained": round(achieved / float(peaks.get("bf16_tflops_sustained", tensor_peak)), 4)}
-    roofline["traffic"] = NCU_TRAFFIC_BYTES.get((w.name, cfg_name))
+    roofline["traffic"] = (NCU_TRAFFIC_BYTES.get((w.name, cfg_name)) if fused is None
+                           else NCU_TRAFFIC_FUSED_BYTES.get((w.name, cfg_name, args.epilogue)))
     roofline["algorithmic_bytes"] = compulsory
     roofline["peak_source"] = f"{peak_src} ({'hbm_gbs' if hbm_bound else 'bf16_tflops'} burst; kernel timed alone)"
     roofline["kernel"] = ("gemm_tn_decode_kernel" if cfg_name == "1cta_decode_splitk"
                           else "gemm_tn_splitk_kernel" if cfg_name.endswith("splitk")
-                          else f"gemm_tn_sm103_kernel<{cfg_name}>")
+                          else f"gemm_tn_sm103_kernel<{cfg_name}>" if fused is None
+                          else f"gemm_tn_sm103_kernel<{cfg_name}, fused>")
 
-    # end to end through the host-buffer entry point
-    pin_a, pin_b = a_cpu.pin_memory(), b_cpu.pin_memory()
-    pin_c = torch.empty((w.m, w.n), dtype=a_cpu.dtype).pin_memory()
-    gt.mm_tn_host(pin_a, pin_b, out=pin_c, device=dev)   # warm
-    dist.barrier()
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        gt.mm_tn_host(pin_a, pin_b, out=pin_c, device=dev)
-    e2e_s = dist.max((time.perf_counter() - t0) / args.e2e_steps)
-    e2e = {"value": round(dist.world * w.flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
-           "h2d_bytes_per_step": op_bytes, "d2h_bytes_per_step": w.m * w.n * 2 + 4,
-           "steps": args.e2e_steps, "entry_point": "gemm_tn_host (pinned host buffers)"}
+    # end to end through the host-buffer entry point (the plain GEMM only)
+    e2e = None
+    if fused is None:
+        pin_a, pin_b = a_cpu.pin_memory(), b_cpu.pin_memory()
+        pin_c = torch.empty((w.m, w.n), dtype=a_cpu.dtype).pin_memory()
+        gt.mm_tn_host(pin_a, pin_b, out=pin_c, device=dev)   # warm
+        dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            gt.mm_tn_host(pin_a, pin_b, out=pin_c, device=dev)
+        e2e_s = dist.max((time.perf_counter() - t0) / max(args.e2e_steps, 1))
+        e2e = {"value": round(dist.world * w.flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": op_bytes, "d2h_bytes_per_step": w.m * w.n * 2 + 4,
+               "steps": args.e2e_steps, "entry_point": "gemm_tn_host (pinned host buffers)"}
 
     line = {
         "metric": METRIC,
@@ -363,7 +398,7 @@ def run_native(args, dist: Dist, peaks, peak_src):
                    "kernel_config": cfg_name, "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU",
                    "l2": "L2 flushed between launches" if flush else
                    f"inputs larger than L2 ({op_bytes / 1e6:.0f} MB of operands vs {L2_BYTES / 1e6:.0f} MB)",
-                   "accumulate": "fp32"},
+                   "accumulate": "fp32", "epilogue": args.epilogue},
         "pct_of_peak": round(100 * w.flops / (avg_launch_ms * 1e-3) / 1e12 / tensor_peak, 2),
         "roofline": roofline,
         "e2e": e2e,
@@ -372,7 +407,7 @@ def run_native(args, dist: Dist, peaks, peak_src):
     }
     if args.cublas_context:
         # the same operands through torch.matmul (cuBLAS), timed the same way
-        ref_c = torch.empty_like(c)
+        ref_c = torch.empty((w.m, w.n), dtype=a.dtype, device=dev)
         for _ in range(args.warmup):
             if flush:
                 scratch.fill_(1)
@@ -655,6 +690,8 @@ def main():
         os.environ["GEMM_TN_FORCE_CONFIG"] = args.config
     if args.gpus < 1:
         raise SystemExit("--gpus must be >= 1")
+    if args.epilogue != "none" and (args.workload.startswith("attn_") or args.impl == "reference"):
+        raise SystemExit("--epilogue applies to the native GEMM workloads only")
     if args.oracle_table:
         oracle_table()
         return
