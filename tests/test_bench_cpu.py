@@ -97,3 +97,18 @@ def test_attention_row_sample_and_flop_count():
     assert bench.attn_rows_flops(w, rows) == w.flops
     few = bench.attn_sample_rows(w, w.flops / 10)
     assert 0 < len(few) < w.seq and few == sorted(set(few))
+
+
+def test_epilogue_option_scope():
+    """--epilogue names the fused paths the benchmark can time; it is refused
+    for attention workloads and the reference arm before any device work."""
+    sys.path.insert(0, str(ROOT))
+    import bench
+    assert set(bench.EPILOGUES) == {"none", "bias", "bias_gelu", "fp32", "e4m3"}
+    assert bench.EPILOGUES["none"] is None
+    alpha, with_bias, act, out = bench.EPILOGUES["e4m3"]
+    assert out == "float8_e4m3fn" and 0.0 < alpha < 1.0 and act == "none"
+    for extra in (["--workload", "attn_bf16_b2_s8192_h32_d128_causal"], ["--impl", "reference"]):
+        r = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--epilogue", "e4m3", *extra],
+                           capture_output=True, text=True, timeout=120)
+        assert r.returncode != 0 and "native GEMM workloads only" in r.stderr
