@@ -295,7 +295,7 @@ int parse_forced_config() {
 // cut over a cluster of S CTAs, S the largest of 8, 4, 2 whose clusters are
 // all resident at once (resident[0..2]: clusters of 2, 4, 8 CTAs; GB300: 76,
 // 36, 15) and that leaves enough k-blocks per CTA: 4 for S = 2 and 8, 2 for
-// S = 4. Measured on GB300 (CUDA graphs, us per call, no split -> split):
+// S = 4 (4 for the decode kernel's M <= 32). Measured on GB300 (CUDA graphs, us per call, no split -> split):
 // 128 x 1024 x 4096 19.8 -> 6.9 (S = 8), 64 x 2048 x 8192 38.5 -> 12.2 (S = 4;
 // 16 clusters of 8 do not fit at once and took 17.2), 1024 x 1024 x 8192 39.5
 // -> 20.9 (S = 2); 256^3 (4 k-blocks) stays whole. With 8 to 15 k-blocks S = 4
@@ -314,7 +314,9 @@ int splitk_factor(int64_t m, int64_t n, int64_t k, int sms, const int resident[3
   }
   if (tiles * 2 > sms) return 0;
   const int splits_of[3] = {2, 4, 8};
-  const int min_kb_per_cta[3] = {4, 2, 4};
+  // the 2-k-block 4-way split was measured with the 128 x 128 split-K kernel
+  // only; the decode kernel (M <= 32) keeps 4 k-blocks per CTA
+  const int min_kb_per_cta[3] = {4, m <= 32 ? 4 : 2, 4};
   for (int i = 2; i >= 0; --i)
     if (tiles <= resident[i] && kb >= min_kb_per_cta[i] * splits_of[i]) return splits_of[i];
   return 0;

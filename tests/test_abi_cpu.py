@@ -71,6 +71,8 @@ def test_config_table(lib, monkeypatch):
     assert splits(256, 256, 960) == 4
     assert splits(256, 256, 1024) == 4                    # 16 k-blocks: 8 splits would leave 2 per CTA
     assert splits(8, 4096, 4096) == 4                     # the decode kernel's split
+    assert splits(8, 2048, 512) == 2                      # decode kernel: 4 k-blocks per CTA kept
+    assert splits(64, 2048, 512) == 4                     # 128 x 128 split-K kernel: 2 per CTA
     assert splits(256, 256, 256) == 0 and splits(8192, 8192, 8192) == 0 and splits(0, 5, 5) == 0
     assert sel(1024, 2048, 4096) == "1cta_n128"           # 128 tiles: one round of single-CTA tiles
     assert sel(1280, 2048, 4096) == "1cta_n256"           # 160 tiles of 128 x 128, 80 of 128 x 256: one round
@@ -143,7 +145,6 @@ def test_split_choice_invariants(lib, monkeypatch):
     monkeypatch.delenv("GEMM_TN_FORCE_CONFIG", raising=False)
     monkeypatch.delenv("GEMM_TN_SPLITK", raising=False)
     resident = {2: 76, 4: 36, 8: 15}
-    min_kb = {2: 4, 4: 2, 8: 4}
     split_cfgs = {"1cta_n128_splitk", "1cta_decode_splitk"}
     seen = set()
     for m in (1, 8, 32, 33, 128, 200, 256, 512, 1024, 2048):
@@ -158,6 +159,7 @@ def test_split_choice_invariants(lib, monkeypatch):
                 kb = -(-k // 64)
                 assert s in resident, (m, n, k, s)
                 assert tiles <= resident[s] and 2 * tiles <= 152, (m, n, k, s, tiles)
+                min_kb = {2: 4, 4: 4 if m <= 32 else 2, 8: 4}
                 assert kb >= min_kb[s] * s, (m, n, k, s, kb)
                 seen.add(s)
     assert seen == {2, 4, 8}
