@@ -34,7 +34,9 @@ from ._native import (  # noqa: F401
     GEMM_TN_NOALLOC_SCRATCH_BYTES,
     gemm_tn_host,
     gemm_tn_last_cuda_error,
+    gemm_tn_last_config,
     gemm_tn_last_error_message,
+    gemm_tn_multicast_allowed,
     gemm_tn_num_configs,
     gemm_tn_select_config,
     gemm_tn_select_splits,

@@ -55,6 +55,8 @@ _SIGNATURES = {
     "gemm_tn_host": (_int, [_int, _i64, _i64, _i64, _ptr, _ptr, _ptr, _ptr]),
     "gemm_tn_select_config": (_int, [_int, _i64, _i64, _i64]),
     "gemm_tn_select_splits": (_int, [_int, _i64, _i64, _i64]),
+    "gemm_tn_last_config": (_int, []),
+    "gemm_tn_multicast_allowed": (_int, [_ptr, _ptr]),
     "gemm_tn_num_configs": (_int, []),
     "gemm_tn_config_name": (ctypes.c_char_p, [_int]),
     "gemm_tn_status_string": (ctypes.c_char_p, [_int]),
@@ -143,6 +145,17 @@ def gemm_tn_select_config(dtype, m, n, k) -> int:
 
 def gemm_tn_select_splits(dtype, m, n, k) -> int:
     return library().gemm_tn_select_splits(dtype, m, n, k)
+
+
+def gemm_tn_last_config() -> int:
+    """Configuration the calling thread's last GEMM call launched (-1: none)."""
+    return library().gemm_tn_last_config()
+
+
+def gemm_tn_multicast_allowed(a, b) -> int:
+    """1 when both pointers are device memory of the current device (the
+    multicast configuration may read them), else 0."""
+    return library().gemm_tn_multicast_allowed(a, b)
 
 
 def gemm_tn_num_configs() -> int:

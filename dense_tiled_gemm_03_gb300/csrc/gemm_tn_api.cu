@@ -84,6 +84,9 @@ int fail_cuda(cudaError_t e, const char* what) {
   return GEMM_TN_ERR_CUDA;
 }
 
+// Configuration the calling thread's last GEMM call launched (-1: none).
+thread_local int t_last_config = -1;
+
 // ---------------------------------------------------------------- device facts
 
 struct DeviceFacts {
@@ -263,6 +266,30 @@ int validate(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
 // TMA wants a 16-byte-aligned base and a row pitch that is a multiple of 16 bytes.
 bool tma_compatible(const void* p, int64_t ld) {
   return reinterpret_cast<uintptr_t>(p) % 16 == 0 && ld % 8 == 0;
+}
+
+// Whether `p` is device memory that lives on device `dev` (not host memory,
+// managed memory or another GPU's memory reached through peer access).
+bool memory_of_device(const void* p, int dev) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
+// The multicast configuration (2cta_n256_mc) has one CTA load a half-tile of A
+// for two CTA pairs with a cluster-multicast TMA load. It may read only this
+// GPU's own memory: both operands must be device memory of the current device.
+// Any other pointer (peer, host-mapped, managed) runs the plain pair kernel.
+bool multicast_source_ok(const void* a, const void* b) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return memory_of_device(a, dev) && memory_of_device(b, dev);
 }
 
 int64_t round_up(int64_t x, int64_t q) { return (x + q - 1) / q * q; }
@@ -519,6 +546,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
              const gemm_tn_epilogue* fused = nullptr) {
   t_last_cuda_error = 0;
   t_last_message[0] = '\0';
+  t_last_config = -1;
   int st = validate(dtype, m, n, k, a, lda, b, ldb, c, ldc, b_mn, c_elem_bytes(fused));
   if (st != GEMM_TN_OK) return st;
   if (m == 0 || n == 0) return GEMM_TN_OK;
@@ -544,6 +572,8 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   splitk_resident(dev, bf16, sk_resident);
   int cfg_id = choose_config(m, n, k, resident_clusters(dev, kCfg2CtaN256, bf16),
                              resident_clusters(dev, kCfg2CtaN256Mc, bf16), sk_resident);
+  // multicast loads only from this GPU's own memory (also when forced)
+  if (cfg_id == kCfg2CtaN256Mc && !multicast_source_ok(a, b)) cfg_id = kCfg2CtaN256;
   // the fused epilogue is built for the pair 256 x 256 and single-CTA 128 x 128 tiles
   if (fused != nullptr && cfg_id != kCfg1CtaN128) cfg_id = m <= 128 ? kCfg1CtaN128 : kCfg2CtaN256;
   // split-K: K cut over a cluster of `splits` CTAs per 128 x 128 tile (plain
@@ -722,6 +752,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
     if (e == cudaSuccess) e = e2;
   }
   if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+  t_last_config = cfg_id;
   return GEMM_TN_OK;
 }
 
@@ -734,8 +765,37 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
 // device (with that device current) and cached.
 __device__ __align__(256) uint8_t g_noalloc_scratch[GEMM_TN_NOALLOC_SCRATCH_BYTES];
 
+// The address is cached per device together with the context it was looked
+// up in: a different current context on that device (a context the caller
+// created, or the primary context after cudaDeviceReset) holds its own copy of
+// the array, so the lookup is repeated when the context changes.
+struct ScratchAddr {
+  CUcontext ctx = nullptr;
+  void* addr = nullptr;
+};
 std::mutex g_scratch_mutex;
-void* g_scratch_addr[64] = {};
+ScratchAddr g_scratch_addr[64];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+std::once_flag g_ctx_once;
+
+// The current driver context (nullptr when it cannot be read).
+CUcontext current_context() {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    } else {
+      cudaGetLastError();
+    }
+  });
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current == nullptr || g_ctx_get_current(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
+}
 
 int noalloc_scratch(void** out) {
   int dev = -1;
@@ -744,14 +804,19 @@ int noalloc_scratch(void** out) {
     cudaGetLastError();
     return fail(GEMM_TN_ERR_UNSUPPORTED_DEVICE, "no current CUDA device");
   }
+  // cudaGetDevice does not create the primary context; the lookup below does,
+  // so a call with no context yet takes the lookup path and caches the new one
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchAddr& slot = g_scratch_addr[dev];
+  if (slot.addr == nullptr || ctx == nullptr || slot.ctx != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) return fail_cuda(e, "cudaGetSymbolAddress (no-alloc scratch)");
-    g_scratch_addr[dev] = p;
+    slot.addr = p;
+    slot.ctx = current_context();
   }
-  *out = g_scratch_addr[dev];
+  *out = slot.addr;
   return GEMM_TN_OK;
 }
 
@@ -1072,6 +1137,10 @@ int gemm_tn_select_splits(int dtype, int64_t m, int64_t n, int64_t k) {
   if (cfg != kCfg1CtaSplitK && cfg != kCfgDecodeSplitK) return 0;
   return resolve_splits(m, n, k, false, sms, sk);
 }
+
+int gemm_tn_last_config(void) { return t_last_config; }
+
+int gemm_tn_multicast_allowed(const void* a, const void* b) { return multicast_source_ok(a, b) ? 1 : 0; }
 
 int gemm_tn_num_configs(void) { return kNumConfigs; }
 

@@ -165,8 +165,10 @@ GEMM_TN_API int gemm_nn(int dtype, int64_t m, int64_t n, int64_t k, const void* 
  * every GPU loading this library holds until the process exits.
  *
  * - The first call on a device looks up that array's device address (with
- *   the device current) and caches it; make that first call before any
- *   stream capture on the device.
+ *   the device current) and caches it with the current context; make that
+ *   first call before any stream capture on the device. A call under another
+ *   context of the device (one the caller created, or the primary context
+ *   again after cudaDeviceReset) repeats the lookup for that context.
  * - A problem whose repacked operands need more than
  *   GEMM_TN_NOALLOC_SCRATCH_BYTES is rejected with GEMM_TN_ERR_INVALID_VALUE
  *   and nothing is enqueued. Operands that need no repack use no scratch.
@@ -206,6 +208,27 @@ GEMM_TN_API int gemm_tn_select_config(int dtype, int64_t m, int64_t n, int64_t k
  * no-op / invalid size. GEMM_TN_FORCE_CONFIG and GEMM_TN_SPLITK apply as in
  * gemm_tn_ex. Host-only: launches nothing. */
 GEMM_TN_API int gemm_tn_select_splits(int dtype, int64_t m, int64_t n, int64_t k);
+
+/* Kernel configuration (an index into the table below) that the calling
+ * thread's last gemm_tn / gemm_tn_ex / gemm_tn_fused / gemm_nn /
+ * gemm_tn_ex_noalloc call launched, or -1 if that call launched no GEMM kernel
+ * (an error, an empty problem or K == 0). gemm_tn_host reports the
+ * configuration of its last row chunk. Diagnostics; never fails. */
+GEMM_TN_API int gemm_tn_last_config(void);
+
+/*
+ * Whether the multicast configuration ("2cta_n256_mc") may read A and B: 1
+ * when both are device memory of the current device, else 0 (host or managed
+ * memory, another GPU's memory reached through peer access, an unknown
+ * pointer, or no usable device). In that configuration one CTA loads a
+ * half-tile of A for two CTA pairs with a cluster-multicast TMA load ("Tiling a
+ * matmul", section "The levels of tiling": a cluster shares a tile between its
+ * CTAs); such loads are issued only on this GPU's own memory. Every GEMM entry
+ * point applies this check whenever the selection (or GEMM_TN_FORCE_CONFIG)
+ * picks that configuration, and runs the plain CTA-pair configuration
+ * ("2cta_n256") when it fails. Host-only: launches nothing.
+ */
+GEMM_TN_API int gemm_tn_multicast_allowed(const void* a, const void* b);
 
 /* Number of kernel configurations, and the name of one ("1cta_n256", ...,
  * "1cta_n128_splitk": K split over a cluster of 2, 4 or 8 CTAs per 128 x 128

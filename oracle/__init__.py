@@ -178,14 +178,20 @@ def _activation(x: np.ndarray, act: int) -> np.ndarray:
     raise ValueError(f"unknown activation {act}")
 
 
-def fused_reference(a, b, alpha=1.0, beta=0.0, c_in=None, bias=None, activation=ACT_NONE, b_kn=False):
+def fused_reference(a, b, alpha=1.0, beta=0.0, c_in=None, bias=None, activation=ACT_NONE, b_kn=False,
+                    product=None):
     """D = act(alpha * (A x B^T) + beta * C_in + bias[j]) in fp64, with the
     magnitude bound of the pre-activation value:
         pre_bound[i][j] = |alpha| * sum_k |a_ik b_jk| + |beta * c_ij| + |bias_j|.
     The GEMM part is gemm_tn_reference (gemm_nn_reference with b_kn); the
     epilogue is the product's definition written out element by element
-    (scale, add, add, activate). Returns (d, pre_bound)."""
-    ref, bound = gemm_nn_reference(a, b) if b_kn else gemm_tn_reference(a, b)
+    (scale, add, add, activate). ``product``: the (ref, bound) pair that
+    gemm_tn_reference returned for these a and b, when the caller has it
+    already (a and b are then not read). Returns (d, pre_bound)."""
+    if product is not None:
+        ref, bound = product
+    else:
+        ref, bound = gemm_nn_reference(a, b) if b_kn else gemm_tn_reference(a, b)
     pre = float(alpha) * ref
     pre_bound = abs(float(alpha)) * bound
     if beta != 0.0 and c_in is not None:

@@ -238,3 +238,27 @@ def test_flash_attn_empty_sizes_are_noops_and_adjacent_o_is_legal(lib):
     assert rc in (gt.GEMM_TN_OK, gt.GEMM_TN_ERR_UNSUPPORTED_DEVICE, gt.GEMM_TN_ERR_CUDA)
     if rc != gt.GEMM_TN_OK:
         assert "overlaps" not in gt.gemm_tn_last_error_message()
+
+
+def test_multicast_guard_refuses_memory_that_is_not_this_gpus(lib):
+    """The multicast configuration may read only device memory of the current
+    device: host memory, NULL and unknown addresses are refused (on a machine
+    without a GPU every pointer is, since there is no current device)."""
+    import numpy as np
+    host_a = np.zeros(1 << 16, dtype=np.uint16)
+    host_b = np.zeros(1 << 16, dtype=np.uint16)
+    assert gt.gemm_tn_multicast_allowed(host_a.ctypes.data, host_b.ctypes.data) == 0
+    assert gt.gemm_tn_multicast_allowed(None, None) == 0
+    assert gt.gemm_tn_multicast_allowed(A, B) == 0
+
+
+def test_last_config_after_calls_that_launch_nothing(lib):
+    """gemm_tn_last_config reports -1 after a call that launched no GEMM
+    kernel: a validation error, an empty problem, or no usable device."""
+    assert gt.gemm_tn_ex(5, 4, 4, 4, A, 4, B, 4, C, 4, None, None) == gt.GEMM_TN_ERR_UNSUPPORTED_DTYPE
+    assert gt.gemm_tn_last_config() == -1
+    assert gt.gemm_tn_ex(0, 0, 4, 4, None, 4, None, 4, None, 4, None, None) == gt.GEMM_TN_OK
+    assert gt.gemm_tn_last_config() == -1
+    rc = gt.gemm_tn_ex(0, 4, 4, 4, A, 4, B, 4, C, 4, None, None)
+    if rc != gt.GEMM_TN_OK:
+        assert gt.gemm_tn_last_config() == -1

@@ -1,6 +1,7 @@
-"""Host-side logic of bench.py on CPU: rank aggregation over world size 2
-(gloo), the reference arm under torchrun (rank 0 alone prints), and the JSON
-line's contract keys."""
+"""Host-side logic of bench.py on CPU: the native arm's refusal of several
+GPUs, the reference arm under torchrun (rank 0 alone prints), the JSON line's
+contract keys, the tile-traffic model and the provenance of stored ncu
+figures."""
 from __future__ import annotations
 
 import json
@@ -11,7 +12,6 @@ import sys
 from pathlib import Path
 
 import pytest
-import torch.multiprocessing as mp
 
 ROOT = Path(__file__).resolve().parents[1]
 
@@ -22,23 +22,62 @@ def _free_port() -> int:
         return s.getsockname()[1]
 
 
-def _dist_worker(rank: int, world: int, port: int, out_dir: str):
-    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
-                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
-    sys.path.insert(0, str(ROOT))
+def test_native_arm_refuses_several_gpus_without_loading_the_library():
+    """The product runs on one GPU: launched for 2 GPUs (by flag, or as a rank
+    of a 2-process job) the native arm prints one line saying so and exits 0
+    without loading the CUDA library, so its cluster-multicast kernel never
+    runs in a multi-GPU process."""
+    probe = ("import json, sys; sys.path.insert(0, {root!r}); import bench; bench.main({argv!r}); "
+             "maps = open('/proc/self/maps').read(); "
+             "print(json.dumps({{'loaded': 'libgemm_tn' in maps, "
+             "'binding': 'dense_tiled_gemm_03_gb300._native' in sys.modules}}))")
+    for argv, env in ((["--gpus", "2"], {}), ([], {"WORLD_SIZE": "2", "RANK": "0"}),
+                      (["--gpus", "2"], {"WORLD_SIZE": "2", "RANK": "1"})):
+        res = subprocess.run([sys.executable, "-c", probe.format(root=str(ROOT), argv=argv)],
+                             capture_output=True, text=True, timeout=300, cwd=ROOT, env={**os.environ, **env})
+        assert res.returncode == 0, res.stderr[-3000:]
+        lines = [json.loads(l) for l in res.stdout.splitlines() if l.startswith("{")]
+        probe_out = lines[-1]
+        assert probe_out == {"loaded": False, "binding": False}
+        printed = lines[:-1]
+        if env.get("RANK") == "1":
+            assert printed == []          # only rank 0 prints
+        else:
+            assert len(printed) == 1 and "unavailable" in printed[0] and printed[0]["n_gpus"] == 2
+
+
+def test_modelled_traffic_matches_the_oracle_model():
+    """The benchmark's tile-traffic model is the oracle's rectangular model
+    (written twice, independently) for the tiles of every configuration."""
     import bench
-    d = bench.Dist()
-    d.barrier()
-    got = d.max(10.0 + rank)
-    d.barrier()
-    d.close()
-    Path(out_dir, f"rank{rank}.txt").write_text(repr(got))
+    from oracle import tiling_model
+    for (m, n, k) in [(8192, 8192, 8192), (4096, 4096, 4096), (3001, 5003, 4097), (128, 16384, 16384),
+                      (256, 256, 256), (8, 4096, 4096)]:
+        for cfg in bench.TILE_OF_CONFIG:
+            tm, tn = bench.tile_of(cfg, m)
+            assert bench.modelled_traffic_bytes(m, n, k, tm, tn) == tiling_model.rect_traffic_bytes(m, n, k, tm, tn)
+    # the headline on CTA-pair tiles: A and B each read 32 times, C written once
+    assert bench.modelled_traffic_bytes(8192, 8192, 8192, 256, 256) == 2 * (2 * 8192 * 8192 * 32) + 2 * 8192 ** 2
 
 
-def test_dist_max_over_two_gloo_ranks(tmp_path):
-    port = _free_port()
-    mp.start_processes(_dist_worker, args=(2, port, str(tmp_path)), nprocs=2, start_method="spawn")
-    assert [float((tmp_path / f"rank{r}.txt").read_text()) for r in range(2)] == [11.0, 11.0]
+def test_stored_traffic_goes_stale_with_the_sources():
+    import bench
+    digest = bench.source_digest()
+    assert len(digest) == 12 and digest == bench.source_digest()
+    entry = {"bytes": 123, "kernel": "k", "when": "d", "source": digest}
+    assert bench.stored_traffic(entry, digest)[0] == 123
+    got, why = bench.stored_traffic(dict(entry, source="000000000000"), digest)
+    assert got is None and why.startswith("stale")
+    assert bench.stored_traffic(None, digest)[0] is None
+    for e in list(bench.NCU_TRAFFIC.values()) + list(bench.NCU_TRAFFIC_ATTN.values()):
+        assert set(e) >= {"bytes", "kernel", "when", "source"}
+
+
+def test_cpulist_round_trip():
+    import bench
+    assert bench.parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench.format_cpulist({0, 1, 2, 3, 8, 10, 11}) == "0-3,8,10-11"
+    assert bench.format_cpulist(set()) == ""
 
 
 def test_reference_arm_under_torchrun_prints_one_line():

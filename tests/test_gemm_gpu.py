@@ -91,18 +91,50 @@ def test_workload_parity_every_config(name, config):
     assert_parity(c, a, b, f"{name} {config}")
 
 
-def test_headline_workload_sampled_parity():
-    """bf16 8192^3 in the configuration the benchmark runs: every column of
-    sampled rows and every row of sampled columns (tile edges included)."""
+@pytest.fixture(scope="module")
+def headline_reference():
+    """The bf16 8192^3 workload's operands with the oracle's ref and bound over
+    the whole output, computed once for the module (about 25 s on 16 host
+    cores): the plain, [K, N] and fused headline checks all compare with it."""
+    import oracle
     w = WORKLOADS["bf16_8192x8192x8192"]
     a, b = workload_operands(w)
+    ref, bound = oracle.gemm_tn_reference(a, b)
+    return w, a, b, ref, bound
+
+
+def test_headline_workload_full_parity(headline_reference):
+    """bf16 8192^3 in the configuration the benchmark runs: every one of the
+    67M output elements against the oracle."""
+    import oracle
+    w, a, b, ref, bound = headline_reference
     c, status = gpu_gemm(a, b)
     assert status == 0
-    assert torch.isfinite(c.float()).all()
-    rng = np.random.Generator(np.random.PCG64(7))
-    rows = edge_indices(w.m, 256, rng, 16)
-    cols = edge_indices(w.n, 256, rng, 16)
-    assert_sampled_parity(c, a, b, rows, cols, w.name)
+    rep = oracle.parity_report(c, ref, bound)
+    assert rep.ok, f"{w.name}: {rep}"
+
+
+def test_multicast_guard_on_the_device():
+    """The multicast configuration reads only this GPU's own memory: device
+    tensors pass the check, pinned and pageable host memory do not, and a
+    shape the selection sends to the multicast kernel runs it on device
+    operands (with parity)."""
+    dev = torch.device("cuda", 0)
+    a = torch.empty(4096, dtype=torch.float16, device=dev)
+    b = torch.empty(4096, dtype=torch.float16, device=dev)
+    pinned = torch.empty(4096, dtype=torch.float16).pin_memory()
+    pageable = torch.empty(4096, dtype=torch.float16)
+    assert gt.gemm_tn_multicast_allowed(a.data_ptr(), b.data_ptr()) == 1
+    assert gt.gemm_tn_multicast_allowed(pinned.data_ptr(), b.data_ptr()) == 0
+    assert gt.gemm_tn_multicast_allowed(a.data_ptr(), pinned.data_ptr()) == 0
+    assert gt.gemm_tn_multicast_allowed(pageable.data_ptr(), b.data_ptr()) == 0
+    m, n, k = 2560, 2560, 1024
+    assert gt.gemm_tn_config_name(gt.gemm_tn_select_config(gt.GEMM_TN_F16, m, n, k)) == "2cta_n256_mc"
+    a_cpu, b_cpu = make_operands(m, n, k, "fp16", "uniform", seed=17)
+    c, status = gpu_gemm(a_cpu, b_cpu)
+    assert gt.gemm_tn_config_name(gt.gemm_tn_last_config()) == "2cta_n256_mc"
+    assert status == 0
+    assert_parity(c, a_cpu, b_cpu, "multicast on device operands")
 
 
 # ------------------------------------------------------------ exact cases
@@ -310,7 +342,10 @@ def test_watchdog_reports_timeout_and_context_survives(config):
     and a normal call is correct."""
     import time
     from _parity import env_var
-    m, n, k = 512, 512, 512
+    # the decode kernel runs only for M <= 32 (a forced decode configuration
+    # with more rows runs the 128 x 128 split-K kernel instead)
+    m = 8 if config == "1cta_decode_splitk" else 512
+    n, k = 512, 512
     dev = torch.device("cuda", 0)
     a_cpu, b_cpu = make_operands(m, n, k, "bf16", "uniform", seed=4)
     a, b = a_cpu.to(dev), b_cpu.to(dev)
@@ -318,11 +353,14 @@ def test_watchdog_reports_timeout_and_context_survives(config):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     t0 = time.perf_counter()
     # k-block 1 (counted from the start of each CTA's K range) exists for every
-    # configuration: the split-K ones cut 512's 8 k-blocks 4 ways, 2 per CTA
+    # configuration: K = 512 has 8 k-blocks, and the split-K kernels keep at
+    # least 2 per CTA (the decode kernel 4: a 2-way split for 8 x 512 x 512)
     with forced_config(config), env_var("GEMM_TN_WATCHDOG_MS", "200"), env_var("GEMM_TN_TEST_DROP_LOAD", "1"):
         gt.mm_tn(a, b, out=out, status=status)
+        ran = gt.gemm_tn_config_name(gt.gemm_tn_last_config())
         torch.cuda.synchronize()
     elapsed = time.perf_counter() - t0
+    assert ran == config, f"forced {config} but {ran} ran"
     assert int(status.item()) == gt.GEMM_TN_ERR_TIMEOUT
     assert elapsed < 5.0, f"watchdog took {elapsed:.1f} s"
     status.zero_()
@@ -691,19 +729,20 @@ def test_nn_small_integers_are_exact(config):
     assert torch.equal(c.cpu().double(), (a.long() @ b.long()).double())
 
 
-def test_nn_headline_shape_sampled():
-    """bf16 8192^3 with B stored [K, N]: every column of sampled rows and
-    every row of sampled columns."""
+def test_nn_headline_full_parity(headline_reference):
+    """bf16 8192^3 with B stored [K, N] (the headline's B transposed, so the
+    product is the headline's): every output element against the oracle."""
     import oracle
-    w = WORKLOADS["bf16_8192x8192x8192"]
-    a_cpu, bt_cpu = workload_operands(w)
+    w, a_cpu, bt_cpu, ref, bound = headline_reference
     b_cpu = bt_cpu.T.contiguous()
     dev = torch.device("cuda", 0)
-    c = gt.mm_nn(a_cpu.to(dev), b_cpu.to(dev)).cpu()
-    rng = np.random.Generator(np.random.PCG64(8))
-    rows = edge_indices(w.m, 256, rng, 8)
-    cols = edge_indices(w.n, 256, rng, 8)
-    assert_sampled_parity(c, a_cpu, bt_cpu, rows, cols, "nn headline")
+    c = torch.full((w.m, w.n), float("nan"), dtype=a_cpu.dtype, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    gt.mm_nn(a_cpu.to(dev), b_cpu.to(dev), out=c, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rep = oracle.parity_report(c.cpu(), ref, bound)
+    assert rep.ok, f"nn headline: {rep}"
 
 
 
@@ -828,16 +867,14 @@ def test_fused_e4m3_exact_integers(m):
     assert np.array_equal(np.where(got == zero_sign, 0, got), np.where(want == zero_sign, 0, want))
 
 
-def test_fused_headline_shape_sampled():
-    """bf16 8192^3 with bias + GELU and fp32 output: sampled rows and columns."""
+def test_fused_headline_full_parity(headline_reference):
+    """bf16 8192^3 with bias + GELU and fp32 output: every output element
+    against the oracle's epilogue applied to the headline product."""
     import oracle
-    w = WORKLOADS["bf16_8192x8192x8192"]
-    a_cpu, b_cpu = workload_operands(w)
+    w, a_cpu, b_cpu, ref, bound = headline_reference
     dev = torch.device("cuda", 0)
     bias = torch.linspace(-1, 1, w.n, dtype=torch.float32)
     c = gt.mm_tn_fused(a_cpu.to(dev), b_cpu.to(dev), bias=bias.to(dev), activation="gelu", out_fp32=True).cpu()
-    rng = np.random.Generator(np.random.PCG64(9))
-    rows = torch.as_tensor(edge_indices(w.m, 256, rng, 8))
-    d_ref, pb = oracle.fused_reference(a_cpu.index_select(0, rows), b_cpu, bias=bias, activation=oracle.ACT_GELU)
-    rep = oracle.fused_parity_report(c.index_select(0, rows), d_ref, pb, oracle.ACT_GELU)
+    d_ref, pb = oracle.fused_reference(a_cpu, b_cpu, bias=bias, activation=oracle.ACT_GELU, product=(ref, bound))
+    rep = oracle.fused_parity_report(c, d_ref, pb, oracle.ACT_GELU)
     assert rep.ok, rep

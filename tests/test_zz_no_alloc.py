@@ -10,6 +10,8 @@ first failure has already run every other test.
 """
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -92,3 +94,70 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     torch.cuda.synchronize()
     assert (c == 7.0).all()
     assert gt.GEMM_TN_NOALLOC_SCRATCH_BYTES == 64 * 1024 * 1024
+
+
+# CUmemPool_attribute values (cuda.h): bytes of the pool in use now, and the
+# high-water mark of that since it was last reset (setting it to 0 resets it
+# to the current use)
+_POOL_USED_MEM_CURRENT = 7
+_POOL_USED_MEM_HIGH = 8
+
+
+def _current_pool(ordinal: int):
+    """The memory pool cudaMallocAsync draws from on device `ordinal` (its
+    current pool), through the driver API."""
+    cuda = ctypes.CDLL("libcuda.so.1")
+    assert cuda.cuInit(0) == 0
+    dev = ctypes.c_int()
+    assert cuda.cuDeviceGet(ctypes.byref(dev), ordinal) == 0
+    pool = ctypes.c_void_p()
+    assert cuda.cuDeviceGetMemPool(ctypes.byref(pool), dev) == 0
+    return cuda, pool
+
+
+def _pool_attr(cuda, pool, attr: int) -> int:
+    v = ctypes.c_uint64()
+    assert cuda.cuMemPoolGetAttribute(pool, attr, ctypes.byref(v)) == 0
+    return v.value
+
+
+def _reset_high(cuda, pool) -> None:
+    zero = ctypes.c_uint64(0)
+    assert cuda.cuMemPoolSetAttribute(pool, _POOL_USED_MEM_HIGH, ctypes.byref(zero)) == 0
+
+
+def test_noalloc_allocates_nothing_where_gemm_tn_ex_does():
+    """A problem whose operands both need the padded copy (K = 409: odd row
+    pitches). gemm_tn_ex takes that copy from cudaMallocAsync, so the high-water
+    mark of the device's memory pool rises by at least its size (the control);
+    gemm_tn_ex_noalloc on the same problem leaves the mark where it was, and
+    both give the same results."""
+    m, n, k = 301, 503, 409
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "fp16", "uniform", seed=99)
+    a, b = a_cpu.to(dev), b_cpu.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    c_noalloc = torch.full((m, n), float("nan"), dtype=a.dtype, device=dev)
+    c_ex = torch.full((m, n), float("nan"), dtype=a.dtype, device=dev)
+    torch.cuda.synchronize()
+    cuda, pool = _current_pool(0)
+    used0 = _pool_attr(cuda, pool, _POOL_USED_MEM_CURRENT)
+
+    _reset_high(cuda, pool)
+    assert _call(gt.gemm_tn_ex_noalloc, a, b, c_noalloc, status) == gt.GEMM_TN_OK
+    torch.cuda.synchronize()
+    assert _pool_attr(cuda, pool, _POOL_USED_MEM_HIGH) == used0, "the no-alloc call allocated from the pool"
+
+    _reset_high(cuda, pool)
+    assert _call(gt.gemm_tn_ex, a, b, c_ex, status) == gt.GEMM_TN_OK
+    torch.cuda.synchronize()
+    # the padded copies: rows of round_up(409, 8) = 416 elements, each copy
+    # rounded up to 256 bytes
+    padded = (-(-m * 416 * 2 // 256) + -(-n * 416 * 2 // 256)) * 256
+    assert _pool_attr(cuda, pool, _POOL_USED_MEM_HIGH) >= used0 + padded, "control: gemm_tn_ex did not allocate"
+    assert _pool_attr(cuda, pool, _POOL_USED_MEM_CURRENT) == used0, "gemm_tn_ex did not give its workspace back"
+    assert int(status.item()) == 0
+    ref, bound = oracle.gemm_tn_reference(a_cpu, b_cpu)
+    allowance = oracle.ALLOW_REL * bound + oracle.ALLOW_ABS
+    got, expected = c_noalloc.cpu().double().numpy(), c_ex.cpu().double().numpy()
+    assert np.isfinite(got).all() and (np.abs(got - expected) <= allowance).all()
