@@ -116,6 +116,9 @@ def parse_args(argv=None):
     ap.add_argument("--oracle-table", action="store_true",
                     help="instead of the benchmark line: time the CPU oracle on every GEMM workload, with all "
                          "host threads and with one thread (one JSON line per workload and thread count)")
+    ap.add_argument("--sustained", type=float, default=0.0,
+                    help="also run the step back to back for this many seconds (power-capped steady state) and "
+                         "report its TFLOP/s, median SM clock and TFLOP/s per GHz")
     ap.add_argument("--child-median", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -357,6 +360,36 @@ def time_calls(step, steps: int, warmup: int, stream, flush=None, sampler=None, 
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     return {"median_ms": statistics.median(times), "min_ms": min(times), "mean_ms": sum(times) / len(times),
             "region_ms": r0.elapsed_time(r1), "launches": launches, "clocks": clocks}
+
+
+def sustained_run(step, seconds: float, stream, flops: float, sampler) -> dict:
+    """The step back to back for about `seconds` (no events between calls):
+    TFLOP/s over the whole region, with the SM clock sampled meanwhile and the
+    rate per GHz of median clock, so that runs at different clocks compare."""
+    import torch
+    step()
+    torch.cuda.synchronize()
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for _ in range(3):
+        step()
+    r1.record(stream)
+    torch.cuda.synchronize()
+    per_call = r0.elapsed_time(r1) / 3 / 1e3
+    calls = max(3, int(seconds / max(per_call, 1e-6)))
+    sampler.start()
+    torch.cuda.synchronize()
+    r0.record(stream)
+    for _ in range(calls):
+        step()
+    r1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    s = r0.elapsed_time(r1) / 1e3
+    tflops = calls * flops / s / 1e12
+    mhz = clocks.get("sm_mhz")
+    return {"tflops": round(tflops, 1), "seconds": round(s, 3), "calls": calls, "clocks": clocks,
+            "tflops_per_ghz": round(tflops / (mhz / 1e3), 1) if mhz else None}
 
 
 def child_median(args) -> dict:
@@ -615,6 +648,10 @@ def run_native(args, peaks, peak_src):
                 workloads[name] = time_workload(gt, torch, dev, other, args.steps, args.warmup, peaks, peak_src,
                                                 digest)
 
+    sustained = None
+    if args.sustained > 0:
+        sustained = sustained_run(step, args.sustained, stream, w.flops, NvmlSampler(gpu_uuid(dev), 0.02))
+
     e2e = None
     if fused is None and not args.no_e2e:
         e2e = e2e_leg(gt, torch, dev, w, a_cpu, b_cpu, args.e2e_steps, t["median_ms"], placement)
@@ -672,6 +709,8 @@ def run_native(args, peaks, peak_src):
         "clocks": clocks,
         "workloads": workloads,
     }
+    if sustained is not None:
+        line["sustained"] = sustained
     if args.cublas_context:
         # the same operands through torch.matmul (cuBLAS), timed the same way
         ref_c = torch.empty((w.m, w.n), dtype=a.dtype, device=dev)

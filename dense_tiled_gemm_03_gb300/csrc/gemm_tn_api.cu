@@ -479,12 +479,14 @@ WorkPlan plan_work(int64_t tiles, int64_t k_blocks, int clusters, int stream_k) 
 // tiles into `split` sub-tiles along N (2 or 4, keeping N >= 64 per MMA) so
 // that wave has up to `split` times as many, shorter units for the same
 // workers. Returns the split factor (1: none) and the first cut tile.
-// GEMM_TN_TAIL_SPLIT=0 turns it off.
+// GEMM_TN_TAIL_SPLIT=0 turns it off; =force cuts the last wave whatever the
+// number of full waves before it (measurements).
 
 int tail_split(const ConfigInfo& cfg, int64_t tiles, int clusters, int64_t* split_begin, bool b_mn) {
   *split_begin = tiles;
   const char* env = std::getenv("GEMM_TN_TAIL_SPLIT");
   if (env != nullptr && std::strcmp(env, "0") == 0) return 1;
+  const bool forced = env != nullptr && std::strcmp(env, "force") == 0;   // any number of full waves
   const int64_t full = tiles >= clusters ? tiles - tiles % clusters : 0;
   const int64_t last = tiles - full;
   if (last == 0) return 1;
@@ -495,7 +497,7 @@ int tail_split(const ConfigInfo& cfg, int64_t tiles, int clusters, int64_t* spli
   // after the full waves, with the plain kernel for those, measured worse
   // still (fp16 3001 x 5003 x 4097: 120 against 112 us; bf16 8192^3: +2-3%):
   // the second launch waits for the whole first grid and starts cold.
-  if (full / clusters > 4) return 1;
+  if (full / clusters > 4 && !forced) return 1;
   for (int s : {4, 2}) {
     if (cfg.block_n / s >= 64 && (cfg.b_rows / s) % (b_mn ? 64 : 8) == 0 && last * s <= clusters) {
       *split_begin = full;

@@ -37,6 +37,17 @@ struct RepackArgs {
   int num_jobs;
 };
 
+// 16 source bytes, read past L1 and marked first to be evicted from L2: the
+// source is read once, so its lines should make room before the copy's
+// destination lines, which the GEMM reads right after.
+__device__ __forceinline__ uint4 ld_stream(uintptr_t p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+
 // 16 bytes starting `shift` bytes (even, 0..14) into the 32 bytes lo:hi.
 __device__ __forceinline__ uint4 extract16(const uint4& lo, const uint4& hi, uint32_t shift) {
   uint32_t x0, x1, x2, x3, x4;
@@ -57,6 +68,8 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const __grid_constant_
   // then be scheduled (it waits for this grid before reading the copies)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  uint64_t evict_first;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
   const int64_t rows_a = args.job[0].rows;
   const int64_t total_rows = rows_a + (args.num_jobs > 1 ? args.job[1].rows : 0);
   for (int64_t gr = blockIdx.x; gr < total_rows; gr += gridDim.x) {
@@ -72,8 +85,8 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const __grid_constant_
       if (want < end) {
         const uintptr_t base = want & ~static_cast<uintptr_t>(15);
         const uint32_t shift = static_cast<uint32_t>(want - base);
-        const uint4 lo = *reinterpret_cast<const uint4*>(base);
-        const uint4 hi = (shift != 0 && base + 16 < end) ? *reinterpret_cast<const uint4*>(base + 16)
+        const uint4 lo = ld_stream(base, evict_first);
+        const uint4 hi = (shift != 0 && base + 16 < end) ? ld_stream(base + 16, evict_first)
                                                           : make_uint4(0u, 0u, 0u, 0u);
         out = shift == 0 ? lo : extract16(lo, hi, shift);
         const int64_t valid = jb.cols - c * 8;   // elements of this chunk inside the row
