@@ -37,6 +37,8 @@ from ._native import (  # noqa: F401
     gemm_tn_last_config,
     gemm_tn_last_error_message,
     gemm_tn_multicast_allowed,
+    gemm_tn_trim_workspace,
+    gemm_tn_workspace_pool,
     gemm_tn_num_configs,
     gemm_tn_select_config,
     gemm_tn_select_splits,

@@ -56,6 +56,8 @@ _SIGNATURES = {
     "gemm_tn_select_config": (_int, [_int, _i64, _i64, _i64]),
     "gemm_tn_select_splits": (_int, [_int, _i64, _i64, _i64]),
     "gemm_tn_last_config": (_int, []),
+    "gemm_tn_workspace_pool": (_ptr, []),
+    "gemm_tn_trim_workspace": (_int, []),
     "gemm_tn_multicast_allowed": (_int, [_ptr, _ptr]),
     "gemm_tn_num_configs": (_int, []),
     "gemm_tn_config_name": (ctypes.c_char_p, [_int]),
@@ -150,6 +152,17 @@ def gemm_tn_select_splits(dtype, m, n, k) -> int:
 def gemm_tn_last_config() -> int:
     """Configuration the calling thread's last GEMM call launched (-1: none)."""
     return library().gemm_tn_last_config()
+
+
+def gemm_tn_workspace_pool() -> int | None:
+    """Handle (cudaMemPool_t) of the library's workspace pool on the current
+    device, or None without a usable device."""
+    return library().gemm_tn_workspace_pool()
+
+
+def gemm_tn_trim_workspace() -> int:
+    """Return the workspace pool's unused memory on the current device."""
+    return library().gemm_tn_trim_workspace()
 
 
 def gemm_tn_multicast_allowed(a, b) -> int:

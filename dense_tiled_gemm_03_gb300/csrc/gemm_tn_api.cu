@@ -420,7 +420,46 @@ uint64_t watchdog_ns() {
   return static_cast<uint64_t>(ms) * 1000000ull;
 }
 
-// fixed_scratch: nullptr = repack workspace from cudaMallocAsync (the normal
+// ---------------------------------------------------------------- workspace pool
+//
+// Stream-ordered workspaces (padded copies of misaligned operands, stream-K
+// partials and flags) come from a memory pool the library creates once per
+// device and that keeps its memory between calls: with the device's default
+// pool, whose memory goes back to the system at every synchronisation, a call
+// after a synchronisation waited for fresh memory to be mapped (bf16 8192^3
+// with a synchronisation after each call: 672 against 580 us on the device).
+// gemm_tn_trim_workspace returns the unused part.
+std::mutex g_ws_pool_mutex;
+cudaMemPool_t g_ws_pool[64] = {};
+
+// The workspace pool of device `dev`, created on first use (a failed
+// creation is retried by the next call).
+cudaError_t workspace_pool(int dev, cudaMemPool_t* out) {
+  std::lock_guard<std::mutex> lock(g_ws_pool_mutex);
+  if (g_ws_pool[dev] == nullptr) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    cudaError_t e = cudaMemPoolCreate(&pool, &props);
+    if (e == cudaSuccess) {
+      uint64_t keep = UINT64_MAX;
+      e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      if (e != cudaSuccess) cudaMemPoolDestroy(pool);
+    }
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return e;
+    }
+    g_ws_pool[dev] = pool;
+  }
+  *out = g_ws_pool[dev];
+  return cudaSuccess;
+}
+
+// fixed_scratch: nullptr = workspace from the library's pool (the normal
 // path); otherwise a caller-designated device buffer of fixed_scratch_bytes
 // that is used instead and never freed (gemm_tn_ex_noalloc).
 // How the tiles of one call are shared out over the grid's workers (CTA
@@ -435,16 +474,44 @@ struct WorkPlan {
   int workers;
   int64_t dp_tiles;
   int64_t sk_iters;
+  int sk_workers;   // workers 0 .. sk_workers - 1 share the stream-K iterations
 };
 
 constexpr int64_t kMinSkIters = 8;
 
 WorkPlan plan_work(int64_t tiles, int64_t k_blocks, int clusters, int stream_k) {
-  WorkPlan p{static_cast<int>(std::min<int64_t>(tiles, clusters)), tiles, 0};
+  WorkPlan p{static_cast<int>(std::min<int64_t>(tiles, clusters)), tiles, 0, 0};
   if (stream_k == 0) return p;
+  if (stream_k < 0) {
+    // the default: problems of at least one full wave whose last wave is
+    // partial cut that wave's tiles into equal k-ranges (mode 3), or, when
+    // they are too many for two parts each, spread them over all workers
+    // (mode 2). Measured on GB300 against whole tiles with the N cut of the
+    // last wave (tail split), us per call: bf16 8192^3 566 -> 552 (mode 3),
+    // fp16 4096^3 86.8 -> 84.6 (mode 2), fp16 3001 x 5003 x 4097 119.9 ->
+    // 113.7 (mode 3). Fewer tiles than workers keep whole tiles.
+    if (tiles < clusters || tiles % clusters == 0) return p;
+    const int64_t rem = tiles % clusters;
+    stream_k = std::min<int64_t>(clusters / rem, k_blocks / kMinSkIters) >= 2 ? 3 : 2;
+  }
   if (tiles >= clusters) {
     const int64_t rem = tiles % clusters;
     if (rem == 0) return p;
+    // mode 3: each tile of the partial wave is cut into s equal k-ranges, s =
+    // the most parts that give every worker at most one (and each part at
+    // least kMinSkIters k-blocks); worker t * s + q takes part q of cut tile
+    // t, so the parts running together read the same k-range of tiles that
+    // share rows of A or B, and one wave's worth of work is spread over all
+    // but clusters - rem * s workers
+    if (stream_k == 3) {
+      const int64_t s = std::min<int64_t>(clusters / rem, k_blocks / kMinSkIters);
+      if (s < 2) return p;
+      p.workers = clusters;
+      p.dp_tiles = tiles - rem;
+      p.sk_iters = rem * k_blocks;
+      p.sk_workers = static_cast<int>(rem * s);
+      return p;
+    }
     // mode 2: only the partial wave's tiles are split (each across about
     // clusters / rem workers), when that leaves at least kMinSkIters k-blocks
     // per worker
@@ -452,12 +519,15 @@ WorkPlan plan_work(int64_t tiles, int64_t k_blocks, int clusters, int stream_k) 
       p.workers = clusters;
       p.dp_tiles = tiles - rem;
       p.sk_iters = rem * k_blocks;
+      p.sk_workers = clusters;
       return p;
     }
+    if (stream_k != 1) return p;
     const int64_t sk_tiles = rem + clusters;
     p.workers = clusters;
     p.dp_tiles = tiles - sk_tiles;
     p.sk_iters = sk_tiles * k_blocks;
+    p.sk_workers = clusters;
     return p;
   }
   const int64_t iters = tiles * k_blocks;
@@ -466,16 +536,18 @@ WorkPlan plan_work(int64_t tiles, int64_t k_blocks, int clusters, int stream_k) 
     p.workers = static_cast<int>(w);
     p.dp_tiles = 0;
     p.sk_iters = iters;
+    p.sk_workers = p.workers;
   }
   return p;
 }
 
-// The stream-K tail is opt-in (GEMM_TN_STREAMK=1). Measured on GB300 it
-// balances the SMs perfectly but lowers every SM's tensor-pipe activity more
-// than it saves: with all 152 SMs streaming operands at once each reaches
-// ~68% tensor activity, while in the data-parallel schedule the partial last
-// wave runs with fewer SMs at up to ~84% (fp16 4096^3: 88.6 us vs 84.8 us).
-// Tail split: when the tiles leave a last, partial wave, cut each of its
+// The stream-K tail is the default for a partial last wave (plan_work). Its
+// fp32 partial rows go out and come back as 512-byte warp-wide accesses, and
+// the contributors' flags carry a per-launch value, so no clearing pass runs
+// before the GEMM; with 16-byte-per-row accesses and a memset of the flags
+// it had measured slower than whole tiles (fp16 4096^3: 105 against 88.6 us).
+// Tail split (used when the stream-K tail is not, e.g. in the fused epilogue
+// and the no-alloc entry point): when the tiles leave a last, partial wave, cut each of its
 // tiles into `split` sub-tiles along N (2 or 4, keeping N >= 64 per MMA) so
 // that wave has up to `split` times as many, shorter units for the same
 // workers. Returns the split factor (1: none) and the first cut tile.
@@ -507,13 +579,27 @@ int tail_split(const ConfigInfo& cfg, int64_t tiles, int clusters, int64_t* spli
   return 1;
 }
 
-// GEMM_TN_STREAMK=2 splits only the partial wave's tiles (experimental).
+// GEMM_TN_STREAMK selects the stream-K mode: unset, the default choice of
+// plan_work (-1); 0 whole tiles only; 1 the last partial wave and one full
+// wave spread over all workers; 2 only the partial wave's tiles, over all
+// workers; 3 each partial-wave tile cut into equal k-ranges, one per worker.
 int stream_k_mode() {
   const char* s = std::getenv("GEMM_TN_STREAMK");
-  if (s == nullptr) return 0;
+  if (s == nullptr || *s == '\0') return -1;
   if (std::strcmp(s, "1") == 0) return 1;
   if (std::strcmp(s, "2") == 0) return 2;
+  if (std::strcmp(s, "3") == 0) return 3;
   return 0;
+}
+
+// Flag value of one stream-K launch: a tag in the high word and a per-process
+// launch counter in the low word. Each launch's flags start as whatever the
+// workspace held (no clearing pass): earlier launches wrote smaller counters,
+// and a contributor stores this launch's value only once its partial rows are
+// written.
+std::atomic<uint64_t> g_flag_counter{0};
+uint64_t next_flag_epoch() {
+  return (0x5EED5EEDull << 32) | ((g_flag_counter.fetch_add(1, std::memory_order_relaxed) + 1) & 0xFFFFFFFFull);
 }
 
 // K rotation and evict-first B loads for problems with one row of tiles.
@@ -632,7 +718,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   const size_t partial_bytes =
       plan.sk_iters > 0 ? static_cast<size_t>(grid_ctas) * 128 * static_cast<size_t>(cfg.block_n) * 4 : 0;
   const size_t flag_bytes =
-      plan.sk_iters > 0 ? static_cast<size_t>(grid_ctas) * gemm_tn_dev::kNumEpilogueWarps * sizeof(int) : 0;
+      plan.sk_iters > 0 ? static_cast<size_t>(grid_ctas) * gemm_tn_dev::kNumEpilogueWarps * sizeof(uint64_t) : 0;
   const size_t ws_bytes = a_bytes + b_bytes + partial_bytes + flag_bytes;
   void* workspace = nullptr;
   void* owned_workspace = nullptr;   // what this call allocated and must free
@@ -648,8 +734,13 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
       }
       workspace = fixed_scratch;
     } else {
-      e = cudaMallocAsync(&workspace, ws_bytes, stream);
-      if (e != cudaSuccess) return fail_cuda(e, "cudaMallocAsync (workspace)");
+      int dev_id = -1;
+      cudaMemPool_t pool = nullptr;
+      e = cudaGetDevice(&dev_id);
+      if (e == cudaSuccess) e = dev_id >= 0 && dev_id < 64 ? workspace_pool(dev_id, &pool) : cudaErrorInvalidDevice;
+      if (e != cudaSuccess) return fail_cuda(e, "workspace pool");
+      e = cudaMallocFromPoolAsync(&workspace, ws_bytes, pool, stream);
+      if (e != cudaSuccess) return fail_cuda(e, "cudaMallocFromPoolAsync (workspace)");
       owned_workspace = workspace;
     }
   }
@@ -675,14 +766,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
     return fail_cuda(e, "repack launch");
   }
   float* partials = partial_bytes ? reinterpret_cast<float*>(ws + a_bytes + b_bytes) : nullptr;
-  int* flags = flag_bytes ? reinterpret_cast<int*>(ws + a_bytes + b_bytes + partial_bytes) : nullptr;
-  if (flags != nullptr) {
-    e = cudaMemsetAsync(flags, 0, flag_bytes, stream);
-    if (e != cudaSuccess) {
-      if (owned_workspace) cudaFreeAsync(owned_workspace, stream);
-      return fail_cuda(e, "cudaMemsetAsync (stream-K flags)");
-    }
-  }
+  uint64_t* flags = flag_bytes ? reinterpret_cast<uint64_t*>(ws + a_bytes + b_bytes + partial_bytes) : nullptr;
 
   alignas(64) gemm_tn_dev::GemmArgs args;
   std::memset(&args, 0, sizeof(args));
@@ -721,8 +805,10 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   args.dp_tiles = static_cast<int32_t>(plan.dp_tiles);
   args.num_workers = plan.workers;
   args.sk_iters = plan.sk_iters;
+  args.sk_workers = plan.sk_workers;
   args.partials = partials;
   args.flags = flags;
+  args.flag_epoch = flags != nullptr ? next_flag_epoch() : 0;
   args.split = split;
   args.split_log2 = split == 4 ? 2 : (split == 2 ? 1 : 0);
   args.split_begin = static_cast<int32_t>(split_begin);
@@ -1141,6 +1227,31 @@ int gemm_tn_select_splits(int dtype, int64_t m, int64_t n, int64_t k) {
 }
 
 int gemm_tn_last_config(void) { return t_last_config; }
+
+void* gemm_tn_workspace_pool(void) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  cudaMemPool_t pool = nullptr;
+  return workspace_pool(dev, &pool) == cudaSuccess ? static_cast<void*>(pool) : nullptr;
+}
+
+int gemm_tn_trim_workspace(void) {
+  t_last_cuda_error = 0;
+  t_last_message[0] = '\0';
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return fail(GEMM_TN_ERR_UNSUPPORTED_DEVICE, "no current CUDA device");
+  }
+  cudaMemPool_t pool = nullptr;
+  e = workspace_pool(dev, &pool);
+  if (e == cudaSuccess) e = cudaMemPoolTrimTo(pool, 0);
+  return e == cudaSuccess ? GEMM_TN_OK : fail_cuda(e, "cudaMemPoolTrimTo (workspace pool)");
+}
 
 int gemm_tn_multicast_allowed(const void* a, const void* b) { return multicast_source_ok(a, b) ? 1 : 0; }
 

@@ -71,12 +71,14 @@ struct GemmArgs {
   int32_t drop_load_kb;   // test hook: producer of tile 0 skips this k-block's loads (-1: never)
   // Work split over the num_workers clusters of the grid. Tiles [0, dp_tiles)
   // go whole and round-robin to the workers. The sk_iters k-block iterations
-  // of tiles [dp_tiles, num_tiles) (stream-K tail) are cut into num_workers
-  // contiguous ranges; a tile cut between workers is finished by the worker
-  // holding its first k-block, which adds the others' fp32 partials.
+  // of tiles [dp_tiles, num_tiles) (stream-K tail) are cut into sk_workers
+  // contiguous ranges, one for each of workers 0 .. sk_workers - 1; a tile cut
+  // between workers is finished by the worker holding its first k-block,
+  // which adds the others' fp32 partials.
   int32_t dp_tiles;
   int32_t num_workers;
   int64_t sk_iters;
+  int32_t sk_workers;
   // Tail split: tiles [split_begin, num_tiles) -- the last, partial wave --
   // are each cut into `split` sub-tiles of block_n / split columns, so that
   // wave holds more, shorter units of work (split 1: no cut).
@@ -91,8 +93,9 @@ struct GemmArgs {
   const float* bias;      // nullable [N]
   int32_t activation;     // 0 none, 1 relu, 2 gelu
   int32_t out_kind;
-  float* partials;        // per CTA: block_n / 32 chunks x 128 rows x 32 fp32 (stream-K only)
-  int* flags;             // per CTA and epilogue warp: 1 once its partial rows are written (zeroed by the host)
+  float* partials;        // per CTA: block_n / 32 chunks x 8 x 128 rows of float4 (stream-K only)
+  uint64_t* flags;        // per CTA and epilogue warp: flag_epoch once its partial rows are written
+  uint64_t flag_epoch;    // this launch's flag value (unique per launch; stale values never match)
   // Memory-bound problems with one row of tiles (B streamed once, A re-read
   // from L2): k_rotate != 0 starts every tile that covers all of K at its
   // own k-block (k_start) and wraps around, and b_evict_first marks the B
@@ -194,13 +197,13 @@ struct WorkItem {
 
 // First stream-K iteration of `worker`'s range.
 __device__ __forceinline__ int64_t sk_range_begin(const GemmArgs& a, int worker) {
-  return a.sk_iters * worker / a.num_workers;
+  return a.sk_iters * worker / a.sk_workers;
 }
 
 // Worker whose stream-K range holds iteration i (ranges are non-empty).
 __device__ __forceinline__ int sk_worker_of(const GemmArgs& a, int64_t i) {
-  int w = static_cast<int>(i * a.num_workers / a.sk_iters);
-  while (w + 1 < a.num_workers && sk_range_begin(a, w + 1) <= i) ++w;
+  int w = static_cast<int>(i * a.sk_workers / a.sk_iters);
+  while (w + 1 < a.sk_workers && sk_range_begin(a, w + 1) <= i) ++w;
   while (w > 0 && sk_range_begin(a, w) > i) --w;
   return w;
 }
@@ -218,7 +221,7 @@ struct WorkCursor {
 
   __device__ __forceinline__ WorkCursor(const GemmArgs& a, int worker)
       : dp_next(worker), sk_cur(0), sk_end(0) {
-    if (a.sk_iters > 0) {
+    if (a.sk_iters > 0 && worker < a.sk_workers) {
       sk_cur = sk_range_begin(a, worker);
       sk_end = sk_range_begin(a, worker + 1);
     }
@@ -283,14 +286,14 @@ __device__ __forceinline__ int rotate_kb(int kb, int start, int num_k_blocks) {
   return r >= num_k_blocks ? r - num_k_blocks : r;
 }
 
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ uint64_t ld_acquire_gpu(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release_gpu(int* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_release_gpu(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.b64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
 
 template <class Cfg>
@@ -327,13 +330,14 @@ struct Watchdog {
     }
   }
 
-  // Wait until a global flag written by another CTA reads 1; false on
-  // timeout or when another role has already given up.
-  __device__ __forceinline__ bool wait_flag(const int* flag) const {
-    if (ld_acquire_gpu(flag) == 1) return true;
+  // Wait until a global flag written by another CTA holds this launch's
+  // epoch; false on timeout or when another role has already given up.
+  __device__ __forceinline__ bool wait_flag(const uint64_t* flag) const {
+    const uint64_t want = args->flag_epoch;
+    if (ld_acquire_gpu(flag) == want) return true;
     const uint64_t deadline = globaltimer_ns() + args->timeout_ns;
     while (true) {
-      if (ld_acquire_gpu(flag) == 1) return true;
+      if (ld_acquire_gpu(flag) == want) return true;
       if (*abort_flag) return false;
       if (globaltimer_ns() > deadline) {
         fail();
@@ -664,11 +668,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       }
       // finisher: partial rows of the next chunk are loaded one chunk ahead
       const bool finisher = last_contrib >= first_contrib;
-      const int64_t part_row = row_in_cta;
+      // partial rows are stored as [cta][chunk][j][128 rows] float4s: the j-th
+      // 16 bytes of every row of a chunk lie side by side, so each warp-wide
+      // store or load of them moves 512 contiguous bytes
       auto partial_src = [&](int w, int chunk) {
         const int cta = w * Cfg::kClusterSize + static_cast<int>(cluster_rank);
-        return reinterpret_cast<const float4*>(
-            args.partials + ((static_cast<int64_t>(cta) * kChunks + chunk) * 128 + part_row) * 32);
+        return reinterpret_cast<const float4*>(args.partials) +
+               (static_cast<int64_t>(cta) * kChunks + chunk) * (8 * 128) + row_in_cta;
       };
       // this warp's last chunk (-1: none), after whose TMEM load it hands
       // the accumulator back to the MMA warp (every epilogue warp arrives once)
@@ -688,7 +694,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       float4 pre[8];
       if (finisher && half < chunks) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) pre[j] = __ldcg(partial_src(first_contrib, half) + j);
+        for (int j = 0; j < 8; ++j) pre[j] = __ldcg(partial_src(first_contrib, half) + j * 128);
       }
       for (int chunk = half; chunk < chunks; chunk += 2) {
         const int col0 = col_tile + chunk * 32;
@@ -698,11 +704,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         // the accumulator is in registers now: hand it back to the MMA warp
         if (chunk == my_last) hand_back();
         if (contributor) {
-          float4* dst = reinterpret_cast<float4*>(
-              args.partials + ((static_cast<int64_t>(blockIdx.x) * kChunks + chunk) * 128 + row_in_cta) * 32);
+          float4* dst = reinterpret_cast<float4*>(args.partials) +
+                        (static_cast<int64_t>(blockIdx.x) * kChunks + chunk) * (8 * 128) + row_in_cta;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+            dst[j * 128] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                  __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
           continue;
         }
@@ -716,11 +722,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
               for (int j = 0; j < 8; ++j) v[j] = pre[j];
               if (chunk + 2 < chunks) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) pre[j] = __ldcg(partial_src(first_contrib, chunk + 2) + j);
+                for (int j = 0; j < 8; ++j) pre[j] = __ldcg(partial_src(first_contrib, chunk + 2) + j * 128);
               }
             } else {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) v[j] = __ldcg(partial_src(w, chunk) + j);
+              for (int j = 0; j < 8; ++j) v[j] = __ldcg(partial_src(w, chunk) + j * 128);
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -963,7 +969,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         // visible at GPU scope before lane 0 raises the flag
         __threadfence();
         __syncwarp();
-        if (lane == 0) st_release_gpu(args.flags + blockIdx.x * kNumEpilogueWarps + epi_warp, 1);
+        if (lane == 0) st_release_gpu(args.flags + blockIdx.x * kNumEpilogueWarps + epi_warp, args.flag_epoch);
       }
       if (++acc == Cfg::kNumAcc) {
         acc = 0;

@@ -32,9 +32,16 @@
  *     kernel stops, leaves C unspecified and, if the caller passed `d_status`,
  *     stores GEMM_TN_ERR_TIMEOUT there (first error wins; the caller zeroes
  *     it and reads it after synchronising).
- *   - GEMM_TN_STREAMK=1 splits the last partial wave of tiles by k-block
- *     ranges over all workers (stream-K), with an fp32 workspace from
- *     cudaMallocAsync on `stream`; off by default (slower on GB300).
+ *   - Stream-K tail: when the output tiles fill at least one wave of the
+ *     persistent grid and leave a partial last wave, that wave's tiles are
+ *     cut into k-block ranges over the workers ("Tiling a matmul", section
+ *     "Where it breaks": split-K / stream-K keep all SMs busy); the fp32
+ *     partial rows go through a stream-ordered workspace (see
+ *     gemm_tn_workspace_pool) and are added in a fixed order, so repeated
+ *     calls stay bit-identical.
+ *     GEMM_TN_STREAMK=0 turns it off (the last wave's tiles are then cut
+ *     along N instead when that fits one wave); 1, 2 or 3 force a mode
+ *     (measurements and tests).
  *     The environment variable GEMM_TN_TEST_DROP_LOAD=<k-block> is a test
  *     hook of gemm_tn_ex: the kernel skips that k-block's loads of its first
  *     tiles so that a wait expires and the watchdog path runs.
@@ -97,8 +104,9 @@ GEMM_TN_API int gemm_tn(int dtype, int64_t m, int64_t n, int64_t k, const void* 
  * lda >= k, ldb >= k, ldc >= n. Any stride and any 2-byte-aligned pointer is
  * accepted. When A or B is not laid out the way the tensor-memory-access
  * engine needs (16-byte-aligned base, row pitch a multiple of 16 bytes) the
- * call first copies that operand into a stream-ordered workspace
- * (cudaMallocAsync / cudaFreeAsync on `stream`) with a padded row pitch.
+ * call first copies that operand into a stream-ordered workspace with a
+ * padded row pitch (allocated and freed on `stream` in the library's
+ * workspace pool, gemm_tn_workspace_pool).
  * d_status: nullable device int that receives GEMM_TN_ERR_TIMEOUT if the
  * device watchdog fires; never cleared by the library.
  */
@@ -157,12 +165,15 @@ GEMM_TN_API int gemm_nn(int dtype, int64_t m, int64_t n, int64_t k, const void* 
  * has reserved (nearly) all device memory for its own pool at start-up, where
  * an extra allocation fails or fragments the pool, or a code path with a hard
  * latency or memory budget, where an allocation can block or fail at the
- * worst moment. This entry point computes exactly what gemm_tn_ex computes,
- * with the same arguments and checks, and allocates nothing: the only
- * temporary memory gemm_tn_ex may need, the padded copy of an operand whose
- * base or row pitch the tensor-memory-access engine cannot address, comes
- * from a static device array of GEMM_TN_NOALLOC_SCRATCH_BYTES (64 MiB) that
- * every GPU loading this library holds until the process exits.
+ * worst moment. This entry point computes the product gemm_tn_ex computes,
+ * with the same arguments and checks, and allocates nothing: the padded copy
+ * of an operand whose base or row pitch the tensor-memory-access engine
+ * cannot address comes from a static device array of
+ * GEMM_TN_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU loading this library
+ * holds until the process exits, and the stream-K tail (which needs a
+ * workspace) is not used: a partial last wave of tiles is cut along N or run
+ * whole instead, so the low-order bits of those tiles can differ from
+ * gemm_tn_ex's (both are within the stated tolerance).
  *
  * - The first call on a device looks up that array's device address (with
  *   the device current) and caches it with the current context; make that
@@ -208,6 +219,20 @@ GEMM_TN_API int gemm_tn_select_config(int dtype, int64_t m, int64_t n, int64_t k
  * no-op / invalid size. GEMM_TN_FORCE_CONFIG and GEMM_TN_SPLITK apply as in
  * gemm_tn_ex. Host-only: launches nothing. */
 GEMM_TN_API int gemm_tn_select_splits(int dtype, int64_t m, int64_t n, int64_t k);
+
+/* The memory pool (a cudaMemPool_t, returned as void*) that the calls above
+ * take their stream-ordered workspaces from on the current device: padded
+ * copies of misaligned operands and the stream-K tail's fp32 partials. The
+ * library creates it on first use (pinned device memory of that device) and
+ * never returns its memory on its own: a workspace freed by one call is reused
+ * by the next without mapping memory again. Its attributes can be read with
+ * cudaMemPoolGetAttribute (diagnostics). NULL when there is no usable device. */
+GEMM_TN_API void* gemm_tn_workspace_pool(void);
+
+/* Return the workspace pool's unused memory on the current device to the
+ * system (cudaMemPoolTrimTo(pool, 0)); memory of workspaces still in use on
+ * some stream is kept. GEMM_TN_ERR_CUDA / _UNSUPPORTED_DEVICE on failure. */
+GEMM_TN_API int gemm_tn_trim_workspace(void);
 
 /* Kernel configuration (an index into the table below) that the calling
  * thread's last gemm_tn / gemm_tn_ex / gemm_tn_fused / gemm_nn /

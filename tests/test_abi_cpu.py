@@ -262,3 +262,13 @@ def test_last_config_after_calls_that_launch_nothing(lib):
     rc = gt.gemm_tn_ex(0, 4, 4, 4, A, 4, B, 4, C, 4, None, None)
     if rc != gt.GEMM_TN_OK:
         assert gt.gemm_tn_last_config() == -1
+
+
+def test_workspace_pool_queries_without_a_device(lib):
+    """Without a usable device there is no workspace pool, and trimming it
+    reports an error instead of failing silently."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("checks the no-device answers")
+    assert gt.gemm_tn_workspace_pool() is None
+    assert gt.gemm_tn_trim_workspace() in (gt.GEMM_TN_ERR_UNSUPPORTED_DEVICE, gt.GEMM_TN_ERR_CUDA)

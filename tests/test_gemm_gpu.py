@@ -377,12 +377,13 @@ def test_watchdog_reports_timeout_and_context_survives(config):
 def test_stream_k_cut_tiles(mnk, config):
     """Shapes whose tiles do not fill whole waves: the last tiles are cut by
     k-block ranges across workers (up to ~16 contributors per tile when there
-    are fewer tiles than workers) and finished by the worker holding their
-    first k-block. Parity with stream-K on, and with it off."""
+    are fewer tiles than workers; mode 3 cuts each partial-wave tile into equal
+    parts, one per worker) and finished by the worker holding their first
+    k-block. Parity with stream-K on in every mode, and with it off."""
     from _parity import env_var
     m, n, k = mnk
     a, b = make_operands(m, n, k, "bf16", "normal_over_sqrt_k", seed=m ^ n ^ k)
-    for sk in ("1", "2", "0"):
+    for sk in ("1", "2", "3", "0"):
         with env_var("GEMM_TN_STREAMK", sk):
             c, status = gpu_gemm(a, b, config)
         assert status == 0
@@ -878,3 +879,33 @@ def test_fused_headline_full_parity(headline_reference):
     d_ref, pb = oracle.fused_reference(a_cpu, b_cpu, bias=bias, activation=oracle.ACT_GELU, product=(ref, bound))
     rep = oracle.fused_parity_report(c, d_ref, pb, oracle.ACT_GELU)
     assert rep.ok, rep
+
+
+def test_workspace_pool_keeps_memory_between_calls():
+    """A call with a stream-K tail takes its fp32 partials from the library's
+    workspace pool. After a synchronisation the pool still holds that memory
+    (the next call reuses it without mapping memory again), trimming returns
+    it, and a call after the trim is still correct."""
+    import ctypes
+    m, n, k = 2304, 4352, 1000
+    a_cpu, b_cpu = make_operands(m, n, k, "bf16", "uniform", seed=23)
+    cuda = ctypes.CDLL("libcuda.so.1")
+    pool = ctypes.c_void_p(gt.gemm_tn_workspace_pool())
+    assert pool.value
+
+    def attr(code):   # CU_MEMPOOL_ATTR_RESERVED_MEM_CURRENT = 5, USED_MEM_HIGH = 8
+        v = ctypes.c_uint64()
+        assert cuda.cuMemPoolGetAttribute(pool, code, ctypes.byref(v)) == 0
+        return v.value
+
+    zero = ctypes.c_uint64(0)
+    assert cuda.cuMemPoolSetAttribute(pool, 8, ctypes.byref(zero)) == 0
+    c, status = gpu_gemm(a_cpu, b_cpu)
+    assert status == 0
+    assert attr(8) > 0, "the stream-K tail took no workspace"
+    assert attr(5) > 0, "the pool gave its memory back at the synchronisation"
+    assert_parity(c, a_cpu, b_cpu, "stream-K tail from the pool")
+    assert gt.gemm_tn_trim_workspace() == gt.GEMM_TN_OK
+    assert attr(5) == 0
+    c2, status = gpu_gemm(a_cpu, b_cpu)
+    assert status == 0 and torch.equal(c, c2)

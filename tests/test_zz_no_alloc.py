@@ -128,10 +128,11 @@ def _reset_high(cuda, pool) -> None:
 
 def test_noalloc_allocates_nothing_where_gemm_tn_ex_does():
     """A problem whose operands both need the padded copy (K = 409: odd row
-    pitches). gemm_tn_ex takes that copy from cudaMallocAsync, so the high-water
-    mark of the device's memory pool rises by at least its size (the control);
-    gemm_tn_ex_noalloc on the same problem leaves the mark where it was, and
-    both give the same results."""
+    pitches). gemm_tn_ex takes that copy from the library's workspace pool, so
+    the pool's high-water mark rises by at least its size (the control);
+    gemm_tn_ex_noalloc on the same problem leaves the high-water marks of that
+    pool and of the device's current pool (the one cudaMallocAsync uses) where
+    they were, and both calls give the same results."""
     m, n, k = 301, 503, 409
     dev = torch.device("cuda", 0)
     a_cpu, b_cpu = make_operands(m, n, k, "fp16", "uniform", seed=99)
@@ -140,22 +141,29 @@ def test_noalloc_allocates_nothing_where_gemm_tn_ex_does():
     c_noalloc = torch.full((m, n), float("nan"), dtype=a.dtype, device=dev)
     c_ex = torch.full((m, n), float("nan"), dtype=a.dtype, device=dev)
     torch.cuda.synchronize()
-    cuda, pool = _current_pool(0)
-    used0 = _pool_attr(cuda, pool, _POOL_USED_MEM_CURRENT)
+    cuda, device_pool = _current_pool(0)
+    lib_pool = ctypes.c_void_p(gt.gemm_tn_workspace_pool())
+    assert lib_pool.value, "no workspace pool on the device"
+    pools = {"device": device_pool, "library": lib_pool}
+    used0 = {name: _pool_attr(cuda, p, _POOL_USED_MEM_CURRENT) for name, p in pools.items()}
 
-    _reset_high(cuda, pool)
+    for p in pools.values():
+        _reset_high(cuda, p)
     assert _call(gt.gemm_tn_ex_noalloc, a, b, c_noalloc, status) == gt.GEMM_TN_OK
     torch.cuda.synchronize()
-    assert _pool_attr(cuda, pool, _POOL_USED_MEM_HIGH) == used0, "the no-alloc call allocated from the pool"
+    for name, p in pools.items():
+        assert _pool_attr(cuda, p, _POOL_USED_MEM_HIGH) == used0[name], f"the no-alloc call allocated from the {name} pool"
 
-    _reset_high(cuda, pool)
+    _reset_high(cuda, lib_pool)
     assert _call(gt.gemm_tn_ex, a, b, c_ex, status) == gt.GEMM_TN_OK
     torch.cuda.synchronize()
     # the padded copies: rows of round_up(409, 8) = 416 elements, each copy
     # rounded up to 256 bytes
     padded = (-(-m * 416 * 2 // 256) + -(-n * 416 * 2 // 256)) * 256
-    assert _pool_attr(cuda, pool, _POOL_USED_MEM_HIGH) >= used0 + padded, "control: gemm_tn_ex did not allocate"
-    assert _pool_attr(cuda, pool, _POOL_USED_MEM_CURRENT) == used0, "gemm_tn_ex did not give its workspace back"
+    assert _pool_attr(cuda, lib_pool, _POOL_USED_MEM_HIGH) >= used0["library"] + padded, \
+        "control: gemm_tn_ex did not take its workspace from the pool"
+    assert _pool_attr(cuda, lib_pool, _POOL_USED_MEM_CURRENT) == used0["library"], \
+        "gemm_tn_ex did not give its workspace back"
     assert int(status.item()) == 0
     ref, bound = oracle.gemm_tn_reference(a_cpu, b_cpu)
     allowance = oracle.ALLOW_REL * bound + oracle.ALLOW_ABS
