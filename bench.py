@@ -85,6 +85,7 @@ EPILOGUES = {
 TILE_OF_CONFIG = {
     "1cta_n256": (128, 256), "1cta_n128": (128, 128), "2cta_n256": (256, 256), "2cta_n128": (256, 128),
     "2cta_n256_mc": (256, 512), "1cta_n128_splitk": (128, 128), "1cta_decode_splitk": (None, 128),
+    "1cta_n64": (128, 64),
 }
 
 

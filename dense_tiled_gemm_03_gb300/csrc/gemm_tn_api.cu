@@ -61,6 +61,7 @@ const ConfigInfo kConfigs[kNumConfigs] = {
     {"2cta_n256_mc", 2, 256, 256, 128, 6, 2, 64},
     {"1cta_n128_splitk", 1, 128, 128, 128, 6, 1, 128},
     {"1cta_decode_splitk", 1, 128, 128, 128, 11, 1, 16},
+    {"1cta_n64", 1, 128, 64, 64, 8, 1, 128},
 };
 
 thread_local int t_last_cuda_error = 0;
@@ -368,6 +369,12 @@ int choose_config(int64_t m, int64_t n, int64_t k, int resident_pairs = 76, int 
   // rows take the MMA's M side)
   if (splitk_factor(m, n, k, 2 * resident_pairs, splitk_resident) > 1)
     return m <= 32 ? kCfgDecodeSplitK : kCfg1CtaSplitK;
+  // Tiny problems: 128 x 64 tiles while they fill at most half the SMs, so
+  // more SMs share the operand loads and each epilogue is half as long
+  // (GB300, us per call in CUDA graphs, 1cta_n64 vs 1cta_n128: 256^3 3.90
+  // vs 4.29, 384 x 384 x 256 4.01 vs 4.21; with 256 tiles of 128 x 64 at
+  // 1024 x 2048 x 1024 it took 14.2 against 7.9).
+  if (((m + 127) / 128) * ((n + 63) / 64) <= static_cast<int64_t>(resident_pairs)) return kCfg1CtaN64;
   if (m <= 128) return kCfg1CtaN128;
   // One round of single-CTA 128 x 128 tiles: every SM gets at most one tile,
   // and a 128 x 128 tile is half the work of a pair's 256 x 256 (GB300, us
@@ -664,6 +671,8 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   if (cfg_id == kCfg2CtaN256Mc && !multicast_source_ok(a, b)) cfg_id = kCfg2CtaN256;
   // the fused epilogue is built for the pair 256 x 256 and single-CTA 128 x 128 tiles
   if (fused != nullptr && cfg_id != kCfg1CtaN128) cfg_id = m <= 128 ? kCfg1CtaN128 : kCfg2CtaN256;
+  // B stored [K, N] is built for 128- and 256-column tiles
+  if (b_mn && cfg_id == kCfg1CtaN64) cfg_id = kCfg1CtaN128;
   // split-K: K cut over a cluster of `splits` CTAs per 128 x 128 tile (plain
   // K-major GEMM only; a forced split-K that cannot cut K runs whole tiles)
   int splits = 0;

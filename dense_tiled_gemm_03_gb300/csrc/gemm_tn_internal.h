@@ -40,7 +40,8 @@ enum ConfigId : int {
   kCfg2CtaN256Mc = 4, // 4-CTA cluster: two pairs on 256 x 512, A shared by TMA multicast
   kCfg1CtaSplitK = 5, // 128 x 128 tiles, K split over a cluster of 2, 4 or 8 CTAs (few tiles, long K)
   kCfgDecodeSplitK = 6, // M <= 32: B's rows on the MMA's M side, K split over a cluster (decode-like)
-  kNumConfigs = 7
+  kCfg1CtaN64 = 7,    // one CTA per 128 x 64 tile, 8-stage ring (small problems: more SMs share the loads)
+  kNumConfigs = 8
 };
 
 struct ConfigInfo {

@@ -1,5 +1,5 @@
 // sm103_gemm_1cta.cu -- instantiations of the tcgen05 GEMM kernel with one CTA
-// per output tile (cta_group::1): 128 x 256 and 128 x 128 tiles.
+// per output tile (cta_group::1): 128 x 256, 128 x 128 and 128 x 64 tiles.
 #include "gemm_tn_internal.h"
 #include "sm103_launch.cuh"
 
@@ -9,6 +9,8 @@ using Cfg256F16 = gemm_tn_dev::GemmConfig<1, 256, 4, false>;
 using Cfg256Bf16 = gemm_tn_dev::GemmConfig<1, 256, 4, true>;
 using Cfg128F16 = gemm_tn_dev::GemmConfig<1, 128, 6, false>;
 using Cfg128Bf16 = gemm_tn_dev::GemmConfig<1, 128, 6, true>;
+using Cfg64F16 = gemm_tn_dev::GemmConfig<1, 64, 8, false>;
+using Cfg64Bf16 = gemm_tn_dev::GemmConfig<1, 64, 8, true>;
 
 cudaError_t launch_gemm_1cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream) {
   switch (id) {
@@ -16,6 +18,8 @@ cudaError_t launch_gemm_1cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& arg
       return bf16 ? Launcher<Cfg256Bf16>::launch(args, grid, stream) : Launcher<Cfg256F16>::launch(args, grid, stream);
     case kCfg1CtaN128:
       return bf16 ? Launcher<Cfg128Bf16>::launch(args, grid, stream) : Launcher<Cfg128F16>::launch(args, grid, stream);
+    case kCfg1CtaN64:
+      return bf16 ? Launcher<Cfg64Bf16>::launch(args, grid, stream) : Launcher<Cfg64F16>::launch(args, grid, stream);
     default:
       return cudaErrorInvalidValue;
   }
@@ -27,13 +31,17 @@ int max_resident_1cta(int id, bool bf16) {
       return bf16 ? Launcher<Cfg256Bf16>::max_clusters() : Launcher<Cfg256F16>::max_clusters();
     case kCfg1CtaN128:
       return bf16 ? Launcher<Cfg128Bf16>::max_clusters() : Launcher<Cfg128F16>::max_clusters();
+    case kCfg1CtaN64:
+      return bf16 ? Launcher<Cfg64Bf16>::max_clusters() : Launcher<Cfg64F16>::max_clusters();
     default:
       return 0;
   }
 }
 
 int smem_bytes_1cta(int id) {
-  return id == kCfg1CtaN256 ? static_cast<int>(Cfg256F16::kSmemBytes) : static_cast<int>(Cfg128F16::kSmemBytes);
+  return id == kCfg1CtaN256  ? static_cast<int>(Cfg256F16::kSmemBytes)
+         : id == kCfg1CtaN64 ? static_cast<int>(Cfg64F16::kSmemBytes)
+                              : static_cast<int>(Cfg128F16::kSmemBytes);
 }
 
 }  // namespace gemm_tn_impl

@@ -258,7 +258,8 @@ GEMM_TN_API int gemm_tn_multicast_allowed(const void* a, const void* b);
 /* Number of kernel configurations, and the name of one ("1cta_n256", ...,
  * "1cta_n128_splitk": K split over a cluster of 2, 4 or 8 CTAs per 128 x 128
  * tile, chosen when the tiles fill less than half the SMs; "1cta_decode_splitk":
- * the same split with B's rows on the MMA's M side, for M <= 32). */
+ * the same split with B's rows on the MMA's M side, for M <= 32; "1cta_n64":
+ * 128 x 64 tiles for problems whose tiles fill at most half the SMs). */
 GEMM_TN_API int gemm_tn_num_configs(void);
 GEMM_TN_API const char* gemm_tn_config_name(int config);
 

@@ -48,7 +48,7 @@ def test_version_status_strings_and_configs(lib):
     assert gt.gemm_tn_status_string(99) == "GEMM_TN_ERR_UNKNOWN"
     names = [gt.gemm_tn_config_name(i) for i in range(gt.gemm_tn_num_configs())]
     assert names == ["1cta_n256", "1cta_n128", "2cta_n256", "2cta_n128", "2cta_n256_mc", "1cta_n128_splitk",
-                     "1cta_decode_splitk"]
+                     "1cta_decode_splitk", "1cta_n64"]
     assert gt.gemm_tn_config_name(-1) == "invalid"
 
 
@@ -62,7 +62,9 @@ def test_config_table(lib, monkeypatch):
     assert sel(64, 2048, 8192) == "1cta_n128_splitk"      # 16 tiles: 4 splits (15 clusters of 8 fit at once)
     assert sel(8, 4096, 4096) == "1cta_decode_splitk"     # <= 32 rows: B on the MMA's M side
     assert sel(33, 4096, 4096) == "1cta_n128_splitk"
-    assert sel(256, 256, 256) == "1cta_n128"              # 4 k-blocks: too short to split; one round
+    assert sel(256, 256, 256) == "1cta_n64"               # 4 k-blocks: too short to split; 8 tiles of 128 x 64
+    assert sel(384, 384, 256) == "1cta_n64"               # 18 tiles of 128 x 64: at most half the SMs
+    assert sel(1024, 1024, 256) == "1cta_n128"            # 128 tiles of 128 x 64 would be more than half
     splits = lambda m, n, k: gt.gemm_tn_select_splits(gt.GEMM_TN_F16, m, n, k)
     assert splits(128, 1024, 4096) == 8                   # 8 tiles, 64 k-blocks
     assert splits(64, 2048, 8192) == 4                    # 16 tiles: more than 15 clusters of 8

@@ -20,7 +20,7 @@ from _parity import (assert_parity, assert_sampled_parity, edge_indices, epilogu
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = ["1cta_n256", "1cta_n128", "2cta_n128", "2cta_n256", "2cta_n256_mc", "1cta_n128_splitk",
+CONFIGS = ["1cta_n256", "1cta_n128", "1cta_n64", "2cta_n128", "2cta_n256", "2cta_n256_mc", "1cta_n128_splitk",
            "1cta_decode_splitk"]
 
 
