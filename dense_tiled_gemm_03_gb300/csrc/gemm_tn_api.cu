@@ -553,8 +553,8 @@ WorkPlan plan_work(int64_t tiles, int64_t k_blocks, int clusters, int stream_k) 
 // the contributors' flags carry a per-launch value, so no clearing pass runs
 // before the GEMM; with 16-byte-per-row accesses and a memset of the flags
 // it had measured slower than whole tiles (fp16 4096^3: 105 against 88.6 us).
-// Tail split (used when the stream-K tail is not, e.g. in the fused epilogue
-// and the no-alloc entry point): when the tiles leave a last, partial wave, cut each of its
+// Tail split (used when the stream-K tail is not, e.g. in the no-alloc entry
+// point or with GEMM_TN_STREAMK=0): when the tiles leave a last, partial wave, cut each of its
 // tiles into `split` sub-tiles along N (2 or 4, keeping N >= 64 per MMA) so
 // that wave has up to `split` times as many, shorter units for the same
 // workers. Returns the split factor (1: none) and the first cut tile.
@@ -700,7 +700,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   if (clusters <= 0) return fail(GEMM_TN_ERR_CUDA, "kernel cannot be resident on this device (occupancy query)");
   // The no-alloc path keeps to whole tiles: its fixed scratch is for repacks.
   WorkPlan plan = plan_work(tiles, num_k_blocks, clusters,
-                            fixed_scratch == nullptr && fused == nullptr && splits == 0 ? stream_k_mode() : 0);
+                            fixed_scratch == nullptr && splits == 0 ? stream_k_mode() : 0);
   int64_t split_begin = tiles;
   // split-capable kernels exist for the two CTA-pair configurations of the plain GEMM
   const bool can_split = !b_mn && fused == nullptr && (cfg_id == kCfg2CtaN256 || cfg_id == kCfg2CtaN256Mc);

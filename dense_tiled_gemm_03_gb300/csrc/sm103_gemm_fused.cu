@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(256) fused_k0_kernel(void* c, int64_t ldc, int
       v += beta * prev;
     }
     if (activation == 1) v = fmaxf(v, 0.0f);
-    if (activation == 2) v = 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+    if (activation == 2) v = gelu_erf(v);
     if (out_kind == 1) {
       static_cast<float*>(c)[at] = v;
     } else if (out_kind == 2) {

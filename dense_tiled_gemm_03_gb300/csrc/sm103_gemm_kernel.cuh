@@ -842,7 +842,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j], 0.0f);
           } else if (args.activation == 2) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.5f * v[j] * (1.0f + erff(v[j] * 0.70710678118654752f));
+            for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
           }
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(v[j]);

@@ -405,6 +405,29 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 1/x by the multi-function unit's approximate reciprocal (x normal, > 0 here).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// GELU, x * Phi(x) with Phi the standard normal CDF, without branches:
+// Phi(-|x|) = (1 - erf(|x| / sqrt 2)) / 2 with the complementary error function
+// of Abramowitz and Stegun, Handbook of Mathematical Functions, formula 7.1.26:
+//   1 - erf(z) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-z^2),
+//   t = 1 / (1 + p z), z >= 0, absolute error at most 1.5e-7,
+// and Phi(|x|) = 1 - Phi(-|x|). Taking the lower tail directly keeps Phi(x)
+// for negative x accurate to that bound rather than to a difference near 1.
+__device__ __forceinline__ float gelu_erf(float x) {
+  const float z = fabsf(x) * 0.70710678118654752f;
+  const float t = rcp_approx(fmaf(0.3275911f, z, 1.0f));
+  const float poly =
+      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
+  const float lower = 0.5f * poly * ex2_approx(-(z * z) * 1.4426950408889634f);   // Phi(-|x|)
+  return x * (x >= 0.0f ? 1.0f - lower : lower);
+}
+
 // ------------------------------------------------------------------ descriptors
 
 // Shared-memory matrix descriptor for a K-major operand tile stored the way a

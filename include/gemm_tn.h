@@ -138,8 +138,9 @@ typedef struct gemm_tn_epilogue {
  * beta != 0 C's previous e4m3 contents are read back exactly. ("TileLang: a
  * tile language one level below Triton", exercise 4: a quantisation to FP8
  * is bandwidth-bound, so it belongs fused with the operator that produces
- * its input.) K == 0 gives act(beta * C + bias). Same errors, watchdog and
- * workspace behaviour as gemm_tn_ex; the stream-K tail is not used.
+ * its input.) K == 0 gives act(beta * C + bias). Same errors, watchdog,
+ * workspace and stream-K behaviour as gemm_tn_ex (with a stream-K tail the
+ * fp32 partial sums are added before the epilogue's one pass over C).
  */
 GEMM_TN_API int gemm_tn_fused(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t lda, const void* b,
                               int64_t ldb, void* c, int64_t ldc, const gemm_tn_epilogue* epilogue, int* d_status,

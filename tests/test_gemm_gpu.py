@@ -909,3 +909,28 @@ def test_workspace_pool_keeps_memory_between_calls():
     assert attr(5) == 0
     c2, status = gpu_gemm(a_cpu, b_cpu)
     assert status == 0 and torch.equal(c, c2)
+
+
+def test_fused_gelu_accuracy_on_a_grid():
+    """The epilogue's GELU, x * Phi(x) with erf from Abramowitz and Stegun
+    7.1.26 (absolute error <= 1.5e-7), evaluated through the K = 0 fused call
+    (D = act(beta * C)) on a grid of x in [-12, 12] and the fp32 extremes of
+    its range, against the oracle's fp64 GELU: |d - gelu(x)| <= 1e-6 * |x|
+    (erf's bound plus the fp32 reciprocal and exponential)."""
+    import oracle
+    dev = torch.device("cuda", 0)
+    grid = np.concatenate([np.linspace(-12.0, 12.0, 48001), [0.0, -0.0, 1e-30, -1e-30, 1e-5, -1e-5, 40.0, -40.0]])
+    x = torch.tensor(grid, dtype=torch.float32).reshape(1, -1)
+    n = x.shape[1]
+    c = x.to(dev).clone()
+    empty = torch.empty((1, 0), dtype=torch.bfloat16, device=dev)
+    b = torch.empty((n, 0), dtype=torch.bfloat16, device=dev)
+    gt.mm_tn_fused(empty, b, out=c, alpha=1.0, beta=1.0, activation="gelu", out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    want, _ = oracle.fused_reference(np.zeros((1, 0)), np.zeros((n, 0)), beta=1.0, c_in=x.double().numpy(),
+                                     activation=oracle.ACT_GELU)
+    got = c.cpu().double().numpy()
+    xd = x.double().numpy()
+    err = np.abs(got - want)
+    assert np.isfinite(got).all()
+    assert (err <= 1e-6 * np.abs(xd)).all(), f"max err/|x| {np.max(err / np.maximum(np.abs(xd), 1e-300)):.3e}"
