@@ -66,9 +66,35 @@ CSRC = ROOT / "dense_tiled_gemm_03_gb300" / "csrc"
 # CUDA sources at capture time: the figure is reported only while the sources
 # are unchanged (a changed kernel makes it stale). Keyed by (workload, kernel
 # configuration) or, for the fused kernels, (workload, configuration, epilogue).
-NCU_TRAFFIC: dict[tuple, dict] = {}
+NCU_TRAFFIC: dict[tuple, dict] = {
+    ("bf16_8192x8192x8192", "2cta_n256"): {  # 567.1 us
+        "bytes": 1209692928 + 136768000, "when": "2026-12-02", "source": "6992d8496f20",
+        "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 0, 0>>"},
+    ("fp16_4096x4096x4096", "2cta_n256_mc"): {  # 81.9 us
+        "bytes": 104357632 + 33707008, "when": "2026-12-02", "source": "6992d8496f20",
+        "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0>>"},
+    ("fp16_3001x5003x4097", "2cta_n256_mc"): {  # 90.6 us
+        "bytes": 95369472 + 24315392, "when": "2026-12-02", "source": "6992d8496f20",
+        "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0>>"},
+    ("bf16_128x16384x16384", "1cta_n128"): {  # 93.2 us
+        "bytes": 542154240 + 3247872, "when": "2026-12-02", "source": "6992d8496f20",
+        "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 128, 6, 1, 1, 0, 0, 0>>"},
+    ("fp16_256x256x256", "1cta_n64"): {  # 6.9 us
+        "bytes": 304128 + 0, "when": "2026-12-02", "source": "6992d8496f20",
+        "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 64, 8, 0, 1, 0, 0, 0>>"},
+    ("bf16_8x4096x4096", "1cta_decode_splitk"): {  # 12.8 us
+        "bytes": 33638656 + 0, "when": "2026-12-02", "source": "6992d8496f20",
+        "kernel": "gemm_tn_decode_kernel<4, 16, 1>"},
+    ("bf16_8192x8192x8192", "2cta_n256", "bias_gelu"): {  # 585.2 us
+        "bytes": 1269319936 + 136698368, "when": "2026-12-02", "source": "6992d8496f20",
+        "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 1, 0>>"},
+}
 # the same for the attention kernel, keyed by workload
-NCU_TRAFFIC_ATTN: dict[str, dict] = {}
+NCU_TRAFFIC_ATTN: dict[str, dict] = {
+    "attn_bf16_b2_s8192_h32_d128_causal": {  # 752.9 us
+        "bytes": 453243136 + 116762624, "when": "2026-12-02", "source": "01b296033520",
+        "kernel": "flash_attn_fwd_kernel<Cfg<128, 1>>"},
+}
 
 # fused epilogues the benchmark can time: (alpha, bias?, activation, output dtype name or None for A's)
 EPILOGUES = {
@@ -132,21 +158,23 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-# CUDA sources each kernel family is built from (the attention kernel's own
-# translation unit, the PTX helpers and the host side that encodes its maps)
+# CUDA sources each kernel family is built from: the attention kernel's own
+# translation unit, the PTX helpers and the host side that encodes its maps;
+# the GEMM kernels are built from every other file but the repack kernel's
 ATTN_SOURCES = ("sm103_flash_attn.cu", "sm103_ptx.cuh", "gemm_tn_internal.h", "gemm_tn_api.cu")
+NOT_GEMM_SOURCES = ("sm103_flash_attn.cu", "repack.cu")
 
 
 def source_digest(kind: str = "gemm") -> str:
     """Digest of the CUDA sources of one kernel family, in name order: "gemm"
-    every file under csrc/ but the attention kernel's, "attn" ATTN_SOURCES."""
+    every file under csrc/ but NOT_GEMM_SOURCES, "attn" ATTN_SOURCES."""
     h = hashlib.sha256()
     for p in sorted(CSRC.iterdir()):
         if not (p.is_file() and p.suffix in (".cu", ".cuh", ".h")):
             continue
         if kind == "attn" and p.name not in ATTN_SOURCES:
             continue
-        if kind == "gemm" and p.name == ATTN_SOURCES[0]:
+        if kind == "gemm" and p.name in NOT_GEMM_SOURCES:
             continue
         h.update(p.name.encode())
         h.update(p.read_bytes())
