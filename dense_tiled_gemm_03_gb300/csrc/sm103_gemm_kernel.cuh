@@ -952,14 +952,23 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
           for (int j = 0; j < 16; ++j) stg[lane * Cfg::kStageRowWords + j] = packed[j];
           __syncwarp();
           // transpose through shared memory: each store instruction writes 32
-          // consecutive columns of one row
+          // consecutive columns of one row. All 32 values are read back
+          // before the first store, and the row pointer steps by ldc, so the
+          // stores issue back to back (with a load-store pair per row and a
+          // 64-bit row offset each time, the last tile's epilogue of the
+          // ragged workload took 7.7 us; this way 3.3 us)
           const int col = col0 + static_cast<int>(lane);
-          const bool col_ok = col < args.n;
-#pragma unroll 4
-          for (int rr = 0; rr < 32; ++rr) {
-            const int row = row0 + rr;
-            const uint16_t v = reinterpret_cast<const uint16_t*>(stg + rr * Cfg::kStageRowWords)[lane];
-            if (col_ok && row < args.m) cptr[static_cast<int64_t>(row) * args.ldc + col] = v;
+          uint16_t vals[32];
+#pragma unroll
+          for (int rr = 0; rr < 32; ++rr) vals[rr] = reinterpret_cast<const uint16_t*>(stg + rr * Cfg::kStageRowWords)[lane];
+          if (col < args.n) {
+            const int rows_here = min(32, args.m - row0);
+            uint16_t* p = cptr + static_cast<int64_t>(row0) * args.ldc + col;
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) {
+              if (rr < rows_here) *p = vals[rr];
+              p += args.ldc;
+            }
           }
           __syncwarp();
         }
