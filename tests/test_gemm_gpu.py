@@ -584,14 +584,17 @@ def test_cuda_graph_capture_and_replay():
     assert_parity(out.cpu(), a.cpu(), b_cpu, "graph replay after operand update")
 
 
-@pytest.mark.parametrize("mnk", [(128, 4096, 4096), (8, 4096, 4096), (256, 256, 256), (2048, 2048, 2048)],
-                         ids=["splitk", "decode", "one_round_128", "one_round_128x256"])
+@pytest.mark.parametrize("mnk", [(128, 4096, 4096), (8, 4096, 4096), (256, 256, 256), (2048, 2048, 2048),
+                                 (2304, 4352, 1000), (1000, 1003, 1001)],
+                         ids=["splitk", "decode", "one_round_128", "one_round_128x256", "stream_k", "repack"])
 def test_cuda_graph_chain_of_each_kernel_kind(mnk):
     """Three dependent calls of one kernel kind (cluster split-K, decode,
-    single-CTA tiles) captured into a CUDA graph, where their programmatic
-    dependent launches become graph edges: C1 = A B^T, C2 = C1' ..., replayed
-    twice with the intermediate pre-filled with NaN; the results equal the
-    ones computed call by call with synchronisations."""
+    single-CTA tiles, a stream-K tail, misaligned operands that are copied
+    first) captured into a CUDA graph, where their programmatic dependent
+    launches become graph edges and their workspaces (stream-K partials,
+    padded copies) allocations of the graph: C1 = A B^T, C2 = C1' ...,
+    replayed twice with the intermediate pre-filled with NaN; the results
+    equal the ones computed call by call with synchronisations."""
     m, n, k = mnk
     dev = torch.device("cuda", 0)
     a_cpu, b_cpu = make_operands(m, n, k, "bf16", "normal_over_sqrt_k", seed=m + n)
