@@ -67,32 +67,32 @@ CSRC = ROOT / "dense_tiled_gemm_03_gb300" / "csrc"
 # are unchanged (a changed kernel makes it stale). Keyed by (workload, kernel
 # configuration) or, for the fused kernels, (workload, configuration, epilogue).
 NCU_TRAFFIC: dict[tuple, dict] = {
-    ("bf16_8192x8192x8192", "2cta_n256"): {  # 567.1 us
-        "bytes": 1209692928 + 136768000, "when": "2026-12-02", "source": "6992d8496f20",
+    ("bf16_8192x8192x8192", "2cta_n256"): {  # 558.1 us
+        "bytes": 1074360576 + 136466176, "when": "2026-12-02", "source": "b58ca1fc6b1f",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 0, 0>>"},
-    ("fp16_4096x4096x4096", "2cta_n256_mc"): {  # 81.9 us
-        "bytes": 104357632 + 33707008, "when": "2026-12-02", "source": "6992d8496f20",
+    ("fp16_4096x4096x4096", "2cta_n256_mc"): {  # 83.0 us
+        "bytes": 105923840 + 34510336, "when": "2026-12-02", "source": "b58ca1fc6b1f",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0>>"},
-    ("fp16_3001x5003x4097", "2cta_n256_mc"): {  # 90.6 us
-        "bytes": 95369472 + 24315392, "when": "2026-12-02", "source": "6992d8496f20",
+    ("fp16_3001x5003x4097", "2cta_n256_mc"): {  # 84.3 us
+        "bytes": 97894912 + 27675904, "when": "2026-12-02", "source": "b58ca1fc6b1f",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0>>"},
-    ("bf16_128x16384x16384", "1cta_n128"): {  # 93.2 us
-        "bytes": 542154240 + 3247872, "when": "2026-12-02", "source": "6992d8496f20",
+    ("bf16_128x16384x16384", "1cta_n128"): {  # 92.8 us
+        "bytes": 542148352 + 3367168, "when": "2026-12-02", "source": "b58ca1fc6b1f",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 128, 6, 1, 1, 0, 0, 0>>"},
-    ("fp16_256x256x256", "1cta_n64"): {  # 6.9 us
-        "bytes": 304128 + 0, "when": "2026-12-02", "source": "6992d8496f20",
+    ("fp16_256x256x256", "1cta_n64"): {  # 7.2 us
+        "bytes": 306432 + 0, "when": "2026-12-02", "source": "b58ca1fc6b1f",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 64, 8, 0, 1, 0, 0, 0>>"},
-    ("bf16_8x4096x4096", "1cta_decode_splitk"): {  # 12.8 us
-        "bytes": 33638656 + 0, "when": "2026-12-02", "source": "6992d8496f20",
+    ("bf16_8x4096x4096", "1cta_decode_splitk"): {  # 13.1 us
+        "bytes": 33638656 + 0, "when": "2026-12-02", "source": "b58ca1fc6b1f",
         "kernel": "gemm_tn_decode_kernel<4, 16, 1>"},
-    ("bf16_8192x8192x8192", "2cta_n256", "bias_gelu"): {  # 585.2 us
-        "bytes": 1269319936 + 136698368, "when": "2026-12-02", "source": "6992d8496f20",
+    ("bf16_8192x8192x8192", "2cta_n256", "bias_gelu"): {  # 579.8 us
+        "bytes": 1090167040 + 136193536, "when": "2026-12-02", "source": "b58ca1fc6b1f",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 1, 0>>"},
 }
 # the same for the attention kernel, keyed by workload
 NCU_TRAFFIC_ATTN: dict[str, dict] = {
-    "attn_bf16_b2_s8192_h32_d128_causal": {  # 752.9 us
-        "bytes": 453243136 + 116762624, "when": "2026-12-02", "source": "01b296033520",
+    "attn_bf16_b2_s8192_h32_d128_causal": {  # 756.6 us
+        "bytes": 453869568 + 116987392, "when": "2026-12-02", "source": "01b296033520",
         "kernel": "flash_attn_fwd_kernel<Cfg<128, 1>>"},
 }
 
