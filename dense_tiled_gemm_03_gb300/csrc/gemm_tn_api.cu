@@ -22,8 +22,8 @@
 #include <atomic>
 #include <mutex>
 
-#include "../../include/flash_attn.h"
-#include "../../include/gemm_tn.h"
+#include "flash_attn.h"
+#include "gemm_tn.h"
 #include "gemm_tn_internal.h"
 #include "sm103_gemm_kernel.cuh"
 

@@ -115,10 +115,10 @@ struct Watch {
   // Wait for the phase of `bar` with parity `parity`; false on timeout or when
   // another role has given up.
   __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
-    if (mbar_try_wait<false>(bar, parity)) return true;
+    if (mbar_try_wait<false, false>(bar, parity)) return true;
     const uint64_t deadline = globaltimer_ns() + args->timeout_ns;
     while (true) {
-      if (mbar_try_wait<false>(bar, parity)) return true;
+      if (mbar_try_wait<false, false>(bar, parity)) return true;
       if (*abort_flag) return false;
       if (globaltimer_ns() > deadline) {
         if (args->status != nullptr) atomicCAS(args->status, 0, kStatusTimeout);
@@ -131,7 +131,7 @@ struct Watch {
   // Bounded wait while draining after a failure; never raises the flag.
   __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
     const uint64_t deadline = globaltimer_ns() + args->timeout_ns;
-    while (!mbar_try_wait<false>(bar, parity)) {
+    while (!mbar_try_wait<false, false>(bar, parity)) {
       if (globaltimer_ns() > deadline) return false;
     }
     return true;

@@ -161,6 +161,7 @@ struct GemmConfig {
 
   static_assert(kBlockN % 32 == 0 && kBlockN >= 32 && kBlockN <= 256, "MMA N");
   static_assert(kCtaGroup == 1 || kCtaGroup == 2, "cta group");
+  static_assert(kStages >= 1 && kStages <= 32, "issued phases fit a 32-bit mask");
   static_assert(kClusterPairs == 1 || (kClusterPairs == 2 && kCtaGroup == 2), "A multicast pairs CTA pairs");
   static_assert(kBRows % 8 == 0 && kBRows <= 256, "TMA box rows");
   static_assert(!kBMnMajor || kBRows % 64 == 0, "MN-major B is loaded in 64-wide boxes");
@@ -296,6 +297,21 @@ __device__ __forceinline__ void st_release_gpu(uint64_t* p, uint64_t v) {
   asm volatile("st.release.gpu.global.b64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
 
+// The last phase the producer issued into each stage of its ring (up to 32
+// stages), held in two registers. A dynamically indexed array would sit in
+// local memory, and the thread's later memory operations, its first tensor
+// copy among them, would wait behind those local stores.
+struct IssuedPhases {
+  uint32_t issued = 0u;   // bit s: some phase was issued into stage s
+  uint32_t parity = 0u;   // bit s: the parity of that phase
+  __device__ __forceinline__ void record(int s, uint32_t phase) {
+    issued |= 1u << s;
+    parity = (parity & ~(1u << s)) | ((phase & 1u) << s);
+  }
+  __device__ __forceinline__ bool any(int s) const { return ((issued >> s) & 1u) != 0u; }
+  __device__ __forceinline__ uint32_t phase(int s) const { return (parity >> s) & 1u; }
+};
+
 template <class Cfg>
 __device__ __forceinline__ void store_pair_bits(uint32_t& out, uint32_t lo, uint32_t hi) {
   const float flo = __uint_as_float(lo), fhi = __uint_as_float(hi);
@@ -425,11 +441,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
   const uint32_t tmem_base = *tmem_slot;
   // The set-up above (barriers, TMEM, descriptor prefetch) may overlap the
   // end of the previous kernel in the stream; global memory is touched only
-  // once that kernel has completed. The next kernel may then be scheduled: it
-  // takes an SM only when a CTA of this grid leaves it, and this grid is
-  // resident as a whole, so nothing here waits on it.
-  griddep_wait();
-  griddep_launch_dependents();
+  // once that kernel has completed. Every thread but the producer waits for
+  // it here. The producer first works out its first unit of work, which
+  // depends on the launch's parameters alone, and waits just before its
+  // first copy, so that this arithmetic overlaps the previous kernel too.
+  // The next kernel may then be scheduled: it takes an SM only when a CTA of
+  // this grid leaves it, and this grid is resident as a whole, so nothing
+  // here waits on it.
+  const bool producer_thread = warp == kProducerWarp && lane == 0;
+  if (!producer_thread) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
 
   const Watchdog<Cfg> wd{&args, abort_flag, smem_addr(const_cast<uint32_t*>(abort_flag))};
   const int worker = static_cast<int>(blockIdx.x) / Cfg::kClusterSize;
@@ -440,9 +463,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       const uint64_t pol_b = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
-      int issued_phase_of[Cfg::kStages];
-      for (int s = 0; s < Cfg::kStages; ++s) issued_phase_of[s] = -1;
+      IssuedPhases issued;
       bool ok = true;
+      bool dep_waited = false;   // griddep_wait() has returned
       int item_index = 0;
       WorkCursor<Cfg::kTailSplit> cursor(args, worker);
       WorkItem item;
@@ -484,6 +507,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             ok = false;
             break;
           }
+          if (!dep_waited) {
+            griddep_wait();
+            griddep_launch_dependents();
+            dep_waited = true;
+          }
           const int kb = rotate_kb(kb_i, kstart, args.num_k_blocks);
           const uint32_t fb = full_bar(stage);
           const bool drop = item_index == 0 && kb_i == args.drop_load_kb;
@@ -501,7 +529,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
                                          a_row + static_cast<int>(pair) * (Cfg::kBlockM / 2), mask);
               load_b(stage, map_to_cta(fb, pair_leader), kb);
             }
-            issued_phase_of[stage] = static_cast<int>(phase);
+            issued.record(stage, phase);
             if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
@@ -520,7 +548,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
               load_b(stage, fb, kb);
             }
           }
-          issued_phase_of[stage] = static_cast<int>(phase);
+          issued.record(stage, phase);
           if (++stage == Cfg::kStages) {
             stage = 0;
             phase ^= 1u;
@@ -528,13 +556,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         }
         ++item_index;
       }
+      if (!dep_waited) {
+        griddep_wait();
+        griddep_launch_dependents();
+      }
       // Loads may still be landing if another role gave up: wait (bounded)
       // for the last phase issued into every stage before the CTA may exit.
       // On the normal path these phases have completed already. The
       // leader's full barriers count the peer's bytes (and, with multicast,
       // the other pair's halves) too.
       for (int s = 0; s < Cfg::kStages; ++s) {
-        if (issued_phase_of[s] >= 0 && leader) wd.drain(full_bar(s), static_cast<uint32_t>(issued_phase_of[s]));
+        if (issued.any(s) && leader) wd.drain(full_bar(s), issued.phase(s));
       }
     }
   } else if (warp == kMmaWarp) {

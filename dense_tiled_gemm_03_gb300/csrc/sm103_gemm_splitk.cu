@@ -41,6 +41,7 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 constexpr int kBlockK = 64;             // one 128-byte swizzle row of 16-bit data
 constexpr int kStages = 6;
+static_assert(kStages <= 32, "issued phases fit a 32-bit mask");
 constexpr uint32_t kTileBytes = 128 * 64 * 2;                       // A or B box of one k-block
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kTileBytes;
@@ -135,9 +136,12 @@ __global__ void __launch_bounds__(splitk::kThreads, 1) gemm_tn_splitk_kernel(con
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  // set-up may overlap the previous kernel in the stream; memory waits for it
-  griddep_wait();
-  griddep_launch_dependents();
+  // set-up may overlap the previous kernel in the stream; memory waits for
+  // it: the producer just before its first copy, every other thread here
+  if (warp != 0 || lane != 0) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
   const Watchdog<ClusterOf<S>> wd{&args, abort_flag, smem_addr(const_cast<uint32_t*>(abort_flag))};
 
   if (warp == 0) {
@@ -145,25 +149,34 @@ __global__ void __launch_bounds__(splitk::kThreads, 1) gemm_tn_splitk_kernel(con
       // ------------------------------------------------------------ TMA producer
       int stage = 0;
       uint32_t phase = 0;
-      int issued_phase_of[kStages];
-      for (int s = 0; s < kStages; ++s) issued_phase_of[s] = -1;
+      IssuedPhases issued;
+      bool dep_waited = false;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!wd.wait(empty_bar(stage), phase ^ 1u)) break;
+        if (!dep_waited) {
+          griddep_wait();
+          griddep_launch_dependents();
+          dep_waited = true;
+        }
         const uint32_t fb = full_bar(stage);
         mbar_arrive_expect_tx(fb, 2 * kTileBytes);
         if (kb - kb0 != args.drop_load_kb) {
           tma_load_2d(&args.tmap_a, a_tile(stage), fb, kb * kBlockK, tm * kBlockM);
           tma_load_2d(&args.tmap_b, b_tile(stage), fb, kb * kBlockK, tn * kBlockN);
         }
-        issued_phase_of[stage] = static_cast<int>(phase);
+        issued.record(stage, phase);
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
+      if (!dep_waited) {
+        griddep_wait();
+        griddep_launch_dependents();
+      }
       // loads still landing after another role gave up finish before exit
       for (int s = 0; s < kStages; ++s)
-        if (issued_phase_of[s] >= 0) wd.drain(full_bar(s), static_cast<uint32_t>(issued_phase_of[s]));
+        if (issued.any(s)) wd.drain(full_bar(s), issued.phase(s));
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -280,6 +293,7 @@ template <int kN>
 struct Layout {
   static constexpr uint32_t kATileBytes = kN * 64 * 2;
   static constexpr int kStages = static_cast<int>(kRingBudget / (kBTileBytes + kATileBytes));
+  static_assert(kStages >= 1 && kStages <= 32, "issued phases fit a 32-bit mask");
   static constexpr uint32_t kOffB = 0;
   static constexpr uint32_t kOffA = kOffB + kStages * kBTileBytes;
   static constexpr uint32_t kRingEnd = kOffA + kStages * kATileBytes;
@@ -346,9 +360,12 @@ __global__ void __launch_bounds__(decode::kThreads, 1) gemm_tn_decode_kernel(con
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  // set-up may overlap the previous kernel in the stream; memory waits for it
-  griddep_wait();
-  griddep_launch_dependents();
+  // set-up may overlap the previous kernel in the stream; memory waits for
+  // it: the producer just before its first copy, every other thread here
+  if (warp != 0 || lane != 0) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
   const Watchdog<splitk::ClusterOf<S>> wd{&args, abort_flag, smem_addr(const_cast<uint32_t*>(abort_flag))};
 
   if (warp == 0) {
@@ -356,24 +373,33 @@ __global__ void __launch_bounds__(decode::kThreads, 1) gemm_tn_decode_kernel(con
       // ------------------------------------------------------------ TMA producer
       int stage = 0;
       uint32_t phase = 0;
-      int issued_phase_of[L::kStages];
-      for (int s = 0; s < L::kStages; ++s) issued_phase_of[s] = -1;
+      IssuedPhases issued;
+      bool dep_waited = false;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!wd.wait(empty_bar(stage), phase ^ 1u)) break;
+        if (!dep_waited) {
+          griddep_wait();
+          griddep_launch_dependents();
+          dep_waited = true;
+        }
         const uint32_t fb = full_bar(stage);
         mbar_arrive_expect_tx(fb, decode::kBTileBytes + L::kATileBytes);
         if (kb - kb0 != args.drop_load_kb) {
           tma_load_2d(&args.tmap_b, b_tile(stage), fb, kb * 64, tn * 128);
           tma_load_2d(&args.tmap_a, a_tile(stage), fb, kb * 64, 0);   // rows past M read as zero
         }
-        issued_phase_of[stage] = static_cast<int>(phase);
+        issued.record(stage, phase);
         if (++stage == L::kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
+      if (!dep_waited) {
+        griddep_wait();
+        griddep_launch_dependents();
+      }
       for (int s = 0; s < L::kStages; ++s)
-        if (issued_phase_of[s] >= 0) wd.drain(full_bar(s), static_cast<uint32_t>(issued_phase_of[s]));
+        if (issued.any(s)) wd.drain(full_bar(s), issued.phase(s));
     }
   } else if (warp == 1) {
     if (lane == 0) {
