@@ -67,32 +67,32 @@ CSRC = ROOT / "dense_tiled_gemm_03_gb300" / "csrc"
 # are unchanged (a changed kernel makes it stale). Keyed by (workload, kernel
 # configuration) or, for the fused kernels, (workload, configuration, epilogue).
 NCU_TRAFFIC: dict[tuple, dict] = {
-    ("bf16_8192x8192x8192", "2cta_n256"): {  # 558.1 us
-        "bytes": 1074360576 + 136466176, "when": "2026-12-02", "source": "b58ca1fc6b1f",
+    ("bf16_8192x8192x8192", "2cta_n256"): {  # 551.9 us
+        "bytes": 1097201920 + 136544000, "when": "2026-12-02", "source": "c0e2e31ecd24",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 0, 0>>"},
-    ("fp16_4096x4096x4096", "2cta_n256_mc"): {  # 83.0 us
-        "bytes": 105923840 + 34510336, "when": "2026-12-02", "source": "b58ca1fc6b1f",
+    ("fp16_4096x4096x4096", "2cta_n256_mc"): {  # 79.1 us
+        "bytes": 106600704 + 33580800, "when": "2026-12-02", "source": "c0e2e31ecd24",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0>>"},
-    ("fp16_3001x5003x4097", "2cta_n256_mc"): {  # 84.3 us
-        "bytes": 97894912 + 27675904, "when": "2026-12-02", "source": "b58ca1fc6b1f",
+    ("fp16_3001x5003x4097", "2cta_n256_mc"): {  # 82.6 us
+        "bytes": 98435840 + 27375872, "when": "2026-12-02", "source": "c0e2e31ecd24",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0>>"},
-    ("bf16_128x16384x16384", "1cta_n128"): {  # 92.8 us
-        "bytes": 542148352 + 3367168, "when": "2026-12-02", "source": "b58ca1fc6b1f",
+    ("bf16_128x16384x16384", "1cta_n128"): {  # 91.9 us
+        "bytes": 542143232 + 3301632, "when": "2026-12-02", "source": "c0e2e31ecd24",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 128, 6, 1, 1, 0, 0, 0>>"},
-    ("fp16_256x256x256", "1cta_n64"): {  # 7.2 us
-        "bytes": 306432 + 0, "when": "2026-12-02", "source": "b58ca1fc6b1f",
+    ("fp16_256x256x256", "1cta_n64"): {  # 7.1 us
+        "bytes": 307200 + 0, "when": "2026-12-02", "source": "c0e2e31ecd24",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 64, 8, 0, 1, 0, 0, 0>>"},
-    ("bf16_8x4096x4096", "1cta_decode_splitk"): {  # 13.1 us
-        "bytes": 33638656 + 0, "when": "2026-12-02", "source": "b58ca1fc6b1f",
+    ("bf16_8x4096x4096", "1cta_decode_splitk"): {  # 12.8 us
+        "bytes": 33638912 + 0, "when": "2026-12-02", "source": "c0e2e31ecd24",
         "kernel": "gemm_tn_decode_kernel<4, 16, 1>"},
-    ("bf16_8192x8192x8192", "2cta_n256", "bias_gelu"): {  # 579.8 us
-        "bytes": 1090167040 + 136193536, "when": "2026-12-02", "source": "b58ca1fc6b1f",
+    ("bf16_8192x8192x8192", "2cta_n256", "bias_gelu"): {  # 562.5 us
+        "bytes": 1081618688 + 136291840, "when": "2026-12-02", "source": "c0e2e31ecd24",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 1, 0>>"},
 }
 # the same for the attention kernel, keyed by workload
 NCU_TRAFFIC_ATTN: dict[str, dict] = {
-    "attn_bf16_b2_s8192_h32_d128_causal": {  # 756.6 us
-        "bytes": 453869568 + 116987392, "when": "2026-12-02", "source": "01b296033520",
+    "attn_bf16_b2_s8192_h32_d128_causal": {  # 753.0 us
+        "bytes": 454881792 + 117135360, "when": "2026-12-02", "source": "edb08f805c1c",
         "kernel": "flash_attn_fwd_kernel<Cfg<128, 1>>"},
 }
 
