@@ -623,6 +623,15 @@ bool k_rotation_on(int64_t num_m_tiles) {
   return num_m_tiles == 1;
 }
 
+// Multiply-and-shift constants for dividing by d (1 <= d < 2^31); see FastDiv.
+gemm_tn_dev::FastDiv make_fast_div(int64_t d) {
+  uint32_t l = 0;
+  while ((int64_t{1} << l) < d) ++l;
+  const uint64_t mul = ((uint64_t{1} << 32) * ((uint64_t{1} << l) - static_cast<uint64_t>(d))) /
+                           static_cast<uint64_t>(d) + 1;
+  return gemm_tn_dev::FastDiv{static_cast<uint32_t>(mul), l};
+}
+
 // Tile rows per rasterization group: tiles in flight together then share
 // about 2048 rows of A and the matching columns of B in L2.
 // GEMM_TN_GROUP_M overrides it (tuning experiments).
@@ -808,6 +817,14 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   args.num_k_blocks = static_cast<int32_t>(num_k_blocks);
   args.num_tiles = static_cast<int32_t>(tiles);
   args.group_m = static_cast<int32_t>(std::min<int64_t>(group_rows(cfg), num_m_tiles));
+  {
+    // group_m <= num_m_tiles, so a group spans at most num_tiles (< 2^31) tiles
+    const int64_t last_first_row = (num_m_tiles - 1) / args.group_m * args.group_m;
+    args.div_group = make_fast_div(static_cast<int64_t>(args.group_m) * num_n_tiles);
+    args.div_rows = make_fast_div(args.group_m);
+    args.div_last_rows = make_fast_div(num_m_tiles - last_first_row);
+    args.div_m_tiles = make_fast_div(num_m_tiles);
+  }
   args.status = d_status;
   args.timeout_ns = watchdog_ns();
   args.drop_load_kb = drop_load_kb;

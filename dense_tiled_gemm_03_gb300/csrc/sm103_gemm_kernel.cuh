@@ -55,6 +55,25 @@ constexpr int kNumEpilogueWarps = 8;
 constexpr int kStatusTimeout = 6;      // == GEMM_TN_ERR_TIMEOUT
 
 // Kernel arguments. Tensor maps first: they must be 64-byte aligned.
+// Division by an invariant divisor d (1 <= d < 2^31) as a multiply-high, an
+// add and a shift, exact for every dividend n < 2^31: Granlund and
+// Montgomery, "Division by invariant integers using multiplication" (1994),
+// the round-up method. With l = ceil(log2 d) and
+// mul = floor(2^32 (2^l - d) / d) + 1 (below 2^32), floor(n / d) =
+// (umulhi(n, mul) + n) >> l; the sum stays below 2^32 since umulhi(n, mul) < n.
+// A runtime 32-bit division is a dependent chain of ~20 instructions through
+// the reciprocal unit, on the producer's path to its first copy.
+struct FastDiv {
+  uint32_t mul;
+  uint32_t shift;
+#ifdef __CUDACC__
+  __device__ __forceinline__ int div(int n) const {
+    const uint32_t u = static_cast<uint32_t>(n);
+    return static_cast<int>((__umulhi(u, mul) + u) >> shift);
+  }
+#endif
+};
+
 struct GemmArgs {
   CUtensorMap tmap_a;     // A: dims {K, M}, box {64, 128}, 128B swizzle
   CUtensorMap tmap_b;     // B: dims {K, N}, box {64, BN / cta_group}, 128B swizzle
@@ -66,6 +85,10 @@ struct GemmArgs {
   int32_t m, n, k;
   int32_t num_m_tiles, num_n_tiles, num_k_blocks, num_tiles;
   int32_t group_m;        // tile rows per rasterization group
+  FastDiv div_group;      // by group_m * num_n_tiles (tiles per group)
+  FastDiv div_rows;       // by group_m
+  FastDiv div_last_rows;  // by the tile rows of the last group (num_m_tiles - its first row)
+  FastDiv div_m_tiles;    // by num_m_tiles (the split-K and decode kernels' column-major tile order)
   int* status;            // nullable device int: first error code wins
   uint64_t timeout_ns;    // per-wait watchdog budget
   int32_t drop_load_kb;   // test hook: producer of tile 0 skips this k-block's loads (-1: never)
@@ -173,16 +196,17 @@ struct GemmConfig {
 };
 
 // Tile index -> (tile row, tile column), grouped so that consecutive indices
-// sweep `group_m` tile rows before moving to the next column.
-__device__ __forceinline__ void tile_coords(int tile, int num_m_tiles, int num_n_tiles, int group_m, int& tm,
-                                            int& tn) {
-  const int per_group = group_m * num_n_tiles;
-  const int g = tile / per_group;
-  const int first_m = g * group_m;
-  const int rows = min(num_m_tiles - first_m, group_m);
-  const int in_group = tile - g * per_group;
-  tm = first_m + in_group % rows;
-  tn = in_group / rows;
+// sweep `group_m` tile rows before moving to the next column; the last group
+// may hold fewer rows.
+__device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& tm, int& tn) {
+  const int g = a.div_group.div(tile);
+  const int first_m = g * a.group_m;
+  const int in_group = tile - g * a.group_m * a.num_n_tiles;
+  const bool full = first_m + a.group_m <= a.num_m_tiles;
+  const int rows = full ? a.group_m : a.num_m_tiles - first_m;
+  const int col = (full ? a.div_rows : a.div_last_rows).div(in_group);
+  tm = first_m + (in_group - col * rows);
+  tn = col;
 }
 
 // ---------------------------------------------------------------- work split
@@ -471,7 +495,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
       WorkItem item;
       while (ok && cursor.next(args, item)) {
         int tm, tj;
-        tile_coords(item.tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tj);
+        tile_coords(args, item.tile, tm, tj);
         const int tn = tj * Cfg::kClusterPairs + static_cast<int>(pair);
         const int a_row = tm * Cfg::kTileM + static_cast<int>(cta_rank) * Cfg::kBlockM;
         const int sub_n = Cfg::kBlockN >> item.nsub_log2;   // columns of this unit of work
@@ -662,7 +686,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
     WorkItem item;
     while (ok && cursor.next(args, item)) {
       int tm, tj;
-      tile_coords(item.tile, args.num_m_tiles, args.num_n_tiles, args.group_m, tm, tj);
+      tile_coords(args, item.tile, tm, tj);
       const int tn = tj * Cfg::kClusterPairs + static_cast<int>(pair);
       // warp-uniform outcome: the tcgen05 loads below are warp-collective
       if (!__all_sync(0xffffffffu, wd.wait(acc_full_bar(acc), acc_phase))) break;

@@ -100,8 +100,8 @@ __global__ void __launch_bounds__(splitk::kThreads, 1) gemm_tn_splitk_kernel(con
   const uint32_t lane = lane_id();
   const uint32_t rank = cluster_ctarank();          // this CTA's slice of K
   const int tile = static_cast<int>(blockIdx.x) / S;
-  const int tm = tile % args.num_m_tiles;
-  const int tn = tile / args.num_m_tiles;
+  const int tn = args.div_m_tiles.div(tile);
+  const int tm = tile - tn * args.num_m_tiles;
   const int kb0 = static_cast<int>(static_cast<int64_t>(rank) * args.num_k_blocks / S);
   const int kb1 = static_cast<int>(static_cast<int64_t>(rank + 1) * args.num_k_blocks / S);
 
