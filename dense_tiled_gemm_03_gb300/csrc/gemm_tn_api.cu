@@ -39,7 +39,7 @@ cudaError_t launch_gemm_nn(int id, bool bf16, const gemm_tn_dev::GemmArgs& args,
 cudaError_t launch_gemm_fused(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_splitk(int splits, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid,
                                cudaStream_t stream);
-cudaError_t launch_gemm_decode(int splits, int rows, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid,
+cudaError_t launch_gemm_decode(int splits, int rows, bool bf16, bool k_pairs, const gemm_tn_dev::GemmArgs& args, int grid,
                                cudaStream_t stream);
 int decode_rows(int64_t m);
 int max_resident_splitk(int splits, bool bf16, int num_sms);
@@ -192,6 +192,30 @@ int encode_matrix_map(CUtensorMap* map, bool bf16, const void* ptr, int64_t rows
   const CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                             const_cast<void*>(ptr), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return fail(GEMM_TN_ERR_CUDA, buf);
+  }
+  return GEMM_TN_OK;
+}
+
+// A K-major [rows, cols] 16-bit matrix (cols a multiple of 64) as a 3-D map
+// {64, rows, cols / 64}, moved in boxes of {64, box_rows, 2}: one copy brings
+// two 64-column k-blocks, each a 128-byte-swizzled [box_rows x 64] tile, one
+// after the other. A box's second k-block past the last reads as zeros.
+int encode_kpair_map(CUtensorMap* map, bool bf16, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                     int box_rows) {
+  auto encode = encode_fn();
+  if (encode == nullptr) return fail(GEMM_TN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 2};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  const CUresult r = encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                            const_cast<void*>(ptr), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     char buf[96];
     std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
@@ -788,9 +812,19 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
 
   alignas(64) gemm_tn_dev::GemmArgs args;
   std::memset(&args, 0, sizeof(args));
-  st = encode_matrix_map(&args.tmap_a, bf16, a_use, m, k, lda_use, kBlockK, decode > 0 ? decode : cfg.a_box_rows,
-                         CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st == GEMM_TN_OK && b_mn)   // [K, N]: 64 N x 64 K boxes
+  // the decode kernel moves two k-blocks per copy when K is a multiple of 64
+  // and every CTA of its cluster still gets at least one pair
+  const bool k_pairs = decode > 0 && k % 64 == 0 && (k / 64 + 1) / 2 >= splits;
+  if (k_pairs) {
+    st = encode_kpair_map(&args.tmap_a, bf16, a_use, m, k, lda_use, decode);
+    if (st == GEMM_TN_OK) st = encode_kpair_map(&args.tmap_b, bf16, b_use, n, k, ldb_use, 128);
+  } else {
+    st = encode_matrix_map(&args.tmap_a, bf16, a_use, m, k, lda_use, kBlockK, decode > 0 ? decode : cfg.a_box_rows,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (k_pairs) {
+    // B's map is set above
+  } else if (st == GEMM_TN_OK && b_mn)   // [K, N]: 64 N x 64 K boxes
     st = encode_matrix_map(&args.tmap_b, bf16, b_use, k, n, ldb_use, 64, kBlockK, CU_TENSOR_MAP_SWIZZLE_128B);
   else if (st == GEMM_TN_OK)
     st = encode_matrix_map(&args.tmap_b, bf16, b_use, n, k, ldb_use, kBlockK, cfg.b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -851,7 +885,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   }
 
   if (decode > 0)
-    e = counted(launch_gemm_decode(splits, decode, bf16, args, grid_ctas, stream));
+    e = counted(launch_gemm_decode(splits, decode, bf16, k_pairs, args, grid_ctas, stream));
   else if (splits > 0)
     e = counted(launch_gemm_splitk(splits, bf16, args, grid_ctas, stream));
   else if (fused != nullptr)

@@ -352,9 +352,10 @@ def test_watchdog_reports_timeout_and_context_survives(config):
     out = torch.zeros((m, n), dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     t0 = time.perf_counter()
-    # k-block 1 (counted from the start of each CTA's K range) exists for every
+    # load 1 (counted from the start of each CTA's K range) exists for every
     # configuration: K = 512 has 8 k-blocks, and the split-K kernels keep at
-    # least 2 per CTA (the decode kernel 4: a 2-way split for 8 x 512 x 512)
+    # least 2 per CTA (the decode kernel 4 in copies of two: a 2-way split for
+    # 8 x 512 x 512 gives each CTA two such copies)
     with forced_config(config), env_var("GEMM_TN_WATCHDOG_MS", "200"), env_var("GEMM_TN_TEST_DROP_LOAD", "1"):
         gt.mm_tn(a, b, out=out, status=status)
         ran = gt.gemm_tn_config_name(gt.gemm_tn_last_config())
@@ -478,13 +479,17 @@ def test_split_k_over_a_cluster(mnk, splits):
 
 @pytest.mark.parametrize("splits", ["2", "4", "8"])
 @pytest.mark.parametrize("mnk", [(1, 4096, 4096), (8, 1000, 2048), (16, 300, 1000), (17, 640, 4097), (32, 129, 512),
-                                 (33, 4000, 8192), (64, 2048, 1024)], ids=lambda s: "x".join(map(str, s)))
+                                 (33, 4000, 8192), (64, 2048, 1024), (8, 512, 4160), (24, 384, 1472), (5, 700, 576)],
+                         ids=lambda s: "x".join(map(str, s)))
 def test_decode_split_k(mnk, splits):
     """At most 32 rows of A: B's rows on the MMA's M side and A's rows
     (zero-filled to 16 or 32) on its N side (a forced decode configuration
     with more rows runs the 128 x 128 split-K kernel), K split over a cluster, C
     stored column by column: parity, nothing written past N into C's padded
-    pitch, and bit-identical results on repeated launches."""
+    pitch, and bit-identical results on repeated launches. With K a multiple
+    of 64 each copy moves two k-blocks (an odd count leaves the last copy's
+    second k-block past K: 4160 = 65 x 64, 1472 = 23 x 64, 576 = 9 x 64; with
+    fewer pairs than CTAs, 576 at S = 8, one k-block per copy instead)."""
     from _parity import env_var
     m, n, k = mnk
     dev = torch.device("cuda", 0)
