@@ -37,7 +37,7 @@ int max_resident_2cta(int id, bool bf16);
 int smem_bytes_2cta(int id);
 cudaError_t launch_gemm_nn(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_fused(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
-cudaError_t launch_gemm_splitk(int splits, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid,
+cudaError_t launch_gemm_splitk(int splits, bool bf16, bool k_pairs, const gemm_tn_dev::GemmArgs& args, int grid,
                                cudaStream_t stream);
 cudaError_t launch_gemm_decode(int splits, int rows, bool bf16, bool k_pairs, const gemm_tn_dev::GemmArgs& args, int grid,
                                cudaStream_t stream);
@@ -812,11 +812,11 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
 
   alignas(64) gemm_tn_dev::GemmArgs args;
   std::memset(&args, 0, sizeof(args));
-  // the decode kernel moves two k-blocks per copy when K is a multiple of 64
-  // and every CTA of its cluster still gets at least one pair
-  const bool k_pairs = decode > 0 && k % 64 == 0 && (k / 64 + 1) / 2 >= splits;
+  // the split-K and decode kernels move two k-blocks per copy when K is a
+  // multiple of 64 and every CTA of their clusters still gets at least one pair
+  const bool k_pairs = splits > 0 && !b_mn && k % 64 == 0 && (k / 64 + 1) / 2 >= splits;
   if (k_pairs) {
-    st = encode_kpair_map(&args.tmap_a, bf16, a_use, m, k, lda_use, decode);
+    st = encode_kpair_map(&args.tmap_a, bf16, a_use, m, k, lda_use, decode > 0 ? decode : 128);
     if (st == GEMM_TN_OK) st = encode_kpair_map(&args.tmap_b, bf16, b_use, n, k, ldb_use, 128);
   } else {
     st = encode_matrix_map(&args.tmap_a, bf16, a_use, m, k, lda_use, kBlockK, decode > 0 ? decode : cfg.a_box_rows,
@@ -887,7 +887,7 @@ int run_gemm(int dtype, int64_t m, int64_t n, int64_t k, const void* a, int64_t 
   if (decode > 0)
     e = counted(launch_gemm_decode(splits, decode, bf16, k_pairs, args, grid_ctas, stream));
   else if (splits > 0)
-    e = counted(launch_gemm_splitk(splits, bf16, args, grid_ctas, stream));
+    e = counted(launch_gemm_splitk(splits, bf16, k_pairs, args, grid_ctas, stream));
   else if (fused != nullptr)
     e = counted(launch_gemm_fused(cfg_id, bf16, args, grid_ctas, stream));
   else if (b_mn)

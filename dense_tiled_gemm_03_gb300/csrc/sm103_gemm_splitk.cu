@@ -40,8 +40,8 @@ constexpr int kThreads = 192;           // warp 0 TMA, warp 1 MMA, warps 2-5 TME
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 constexpr int kBlockK = 64;             // one 128-byte swizzle row of 16-bit data
-constexpr int kStages = 6;
-static_assert(kStages <= 32, "issued phases fit a 32-bit mask");
+constexpr int kStages = 6;              // k-blocks the ring holds; kStages / kKb stages of kKb k-blocks
+static_assert(kStages <= 32 && kStages % 2 == 0, "issued phases fit a 32-bit mask; stages of two k-blocks");
 constexpr uint32_t kTileBytes = 128 * 64 * 2;                       // A or B box of one k-block
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kTileBytes;
@@ -87,10 +87,16 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 }  // namespace splitk
 
-template <int S, bool kBf16>
+// kKb k-blocks per stage: with K a multiple of 64, one 3-D tensor copy moves
+// two k-blocks of A or B ({64, 128, 2} boxes over {64, rows, K / 64} maps; the
+// decode kernel below explains why), and the ring holds half as many stages
+// of twice the size.
+template <int S, bool kBf16, int kKb>
 __global__ void __launch_bounds__(splitk::kThreads, 1) gemm_tn_splitk_kernel(const __grid_constant__ GemmArgs args) {
   using namespace splitk;
   static_assert(S == 2 || S == 4 || S == 8, "cluster of 2, 4 or 8 CTAs");
+  static_assert(kKb == 1 || kKb == 2, "one or two k-blocks per stage");
+  constexpr int kRing = kStages / kKb;          // stages in use
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -102,11 +108,13 @@ __global__ void __launch_bounds__(splitk::kThreads, 1) gemm_tn_splitk_kernel(con
   const int tile = static_cast<int>(blockIdx.x) / S;
   const int tn = args.div_m_tiles.div(tile);
   const int tm = tile - tn * args.num_m_tiles;
-  const int kb0 = static_cast<int>(static_cast<int64_t>(rank) * args.num_k_blocks / S);
-  const int kb1 = static_cast<int>(static_cast<int64_t>(rank + 1) * args.num_k_blocks / S);
+  // this CTA's stages: [kb0, kb1) in units of kKb k-blocks
+  const int units = (args.num_k_blocks + kKb - 1) / kKb;
+  const int kb0 = static_cast<int>(static_cast<int64_t>(rank) * units / S);
+  const int kb1 = static_cast<int>(static_cast<int64_t>(rank + 1) * units / S);
 
-  auto a_tile = [&](int s) { return base + kOffA + s * kTileBytes; };
-  auto b_tile = [&](int s) { return base + kOffB + s * kTileBytes; };
+  auto a_tile = [&](int s) { return base + kOffA + s * kKb * kTileBytes; };
+  auto b_tile = [&](int s) { return base + kOffB + s * kKb * kTileBytes; };
   auto full_bar = [&](int s) { return base + kOffBar + 8u * s; };
   auto empty_bar = [&](int s) { return base + kOffBar + 8u * (kStages + s); };
   const uint32_t acc_full_bar = base + kOffBar + 8u * (2 * kStages);
@@ -159,13 +167,18 @@ __global__ void __launch_bounds__(splitk::kThreads, 1) gemm_tn_splitk_kernel(con
           dep_waited = true;
         }
         const uint32_t fb = full_bar(stage);
-        mbar_arrive_expect_tx(fb, 2 * kTileBytes);
+        mbar_arrive_expect_tx(fb, 2 * kKb * kTileBytes);
         if (kb - kb0 != args.drop_load_kb) {
-          tma_load_2d(&args.tmap_a, a_tile(stage), fb, kb * kBlockK, tm * kBlockM);
-          tma_load_2d(&args.tmap_b, b_tile(stage), fb, kb * kBlockK, tn * kBlockN);
+          if constexpr (kKb == 2) {
+            tma_load_3d(&args.tmap_a, a_tile(stage), fb, 0, tm * kBlockM, 2 * kb);
+            tma_load_3d(&args.tmap_b, b_tile(stage), fb, 0, tn * kBlockN, 2 * kb);
+          } else {
+            tma_load_2d(&args.tmap_a, a_tile(stage), fb, kb * kBlockK, tm * kBlockM);
+            tma_load_2d(&args.tmap_b, b_tile(stage), fb, kb * kBlockK, tn * kBlockN);
+          }
         }
         issued.record(stage, phase);
-        if (++stage == kStages) {
+        if (++stage == kRing) {
           stage = 0;
           phase ^= 1u;
         }
@@ -175,7 +188,7 @@ __global__ void __launch_bounds__(splitk::kThreads, 1) gemm_tn_splitk_kernel(con
         griddep_launch_dependents();
       }
       // loads still landing after another role gave up finish before exit
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < kRing; ++s)
         if (issued.any(s)) wd.drain(full_bar(s), issued.phase(s));
     }
   } else if (warp == 1) {
@@ -191,13 +204,16 @@ __global__ void __launch_bounds__(splitk::kThreads, 1) gemm_tn_splitk_kernel(con
           break;
         }
         tc_fence_after_sync();
-        const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage));
-        const uint64_t b_desc = sw128_kmajor_desc(b_tile(stage));
 #pragma unroll
-        for (int kk = 0; kk < kBlockK / 16; ++kk)
-          mma_f16<1>(tmem_base, a_desc + 2u * kk, b_desc + 2u * kk, kIdesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kKb * (kBlockK / 16); ++kk) {
+          // k-block kk / 4 of the stage, 16-element step kk % 4 within it
+          const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage) + (kk >> 2) * kTileBytes);
+          const uint64_t b_desc = sw128_kmajor_desc(b_tile(stage) + (kk >> 2) * kTileBytes);
+          mma_f16<1>(tmem_base, a_desc + 2u * (kk & 3), b_desc + 2u * (kk & 3), kIdesc,
+                     (kb > kb0 || kk > 0) ? 1u : 0u);
+        }
         mma_commit(empty_bar(stage));
-        if (++stage == kStages) {
+        if (++stage == kRing) {
           stage = 0;
           phase ^= 1u;
         }
@@ -545,7 +561,7 @@ __global__ void __launch_bounds__(decode::kThreads, 1) gemm_tn_decode_kernel(con
 namespace gemm_tn_impl {
 namespace {
 
-template <int S, bool kBf16>
+template <int S, bool kBf16, int kKb>
 struct SplitKLauncher {
   static cudaError_t ensure_smem_attr() {
     static std::atomic<uint64_t> done_mask{0};
@@ -554,7 +570,7 @@ struct SplitKLauncher {
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (done_mask.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    e = cudaFuncSetAttribute(gemm_tn_dev::gemm_tn_splitk_kernel<S, kBf16>,
+    e = cudaFuncSetAttribute(gemm_tn_dev::gemm_tn_splitk_kernel<S, kBf16, kKb>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(gemm_tn_dev::splitk::kSmemBytes));
     if (e == cudaSuccess) done_mask.fetch_or(bit, std::memory_order_acq_rel);
@@ -586,7 +602,7 @@ struct SplitKLauncher {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     fill(cfg, attr, grid, stream, dependent_launch_enabled());
-    return cudaLaunchKernelEx(&cfg, gemm_tn_dev::gemm_tn_splitk_kernel<S, kBf16>, args);
+    return cudaLaunchKernelEx(&cfg, gemm_tn_dev::gemm_tn_splitk_kernel<S, kBf16, kKb>, args);
   }
 
   static int max_clusters(int num_sms) {
@@ -595,7 +611,7 @@ struct SplitKLauncher {
     cudaLaunchAttribute attr[2];
     fill(cfg, attr, num_sms - num_sms % S, nullptr, false);
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_dev::gemm_tn_splitk_kernel<S, kBf16>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_dev::gemm_tn_splitk_kernel<S, kBf16, kKb>, &cfg) !=
         cudaSuccess) {
       cudaGetLastError();
       return 0;
@@ -675,24 +691,30 @@ cudaError_t launch_gemm_decode(int splits, int rows, bool bf16, bool k_pairs, co
   }
 }
 
-cudaError_t launch_gemm_splitk(int splits, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid,
-                               cudaStream_t stream) {
+template <bool kBf16, int kKb>
+cudaError_t launch_splitk_kb(int splits, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream) {
   switch (splits) {
-    case 2: return bf16 ? SplitKLauncher<2, true>::launch(args, grid, stream)
-                        : SplitKLauncher<2, false>::launch(args, grid, stream);
-    case 4: return bf16 ? SplitKLauncher<4, true>::launch(args, grid, stream)
-                        : SplitKLauncher<4, false>::launch(args, grid, stream);
-    case 8: return bf16 ? SplitKLauncher<8, true>::launch(args, grid, stream)
-                        : SplitKLauncher<8, false>::launch(args, grid, stream);
+    case 2: return SplitKLauncher<2, kBf16, kKb>::launch(args, grid, stream);
+    case 4: return SplitKLauncher<4, kBf16, kKb>::launch(args, grid, stream);
+    case 8: return SplitKLauncher<8, kBf16, kKb>::launch(args, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
+cudaError_t launch_gemm_splitk(int splits, bool bf16, bool k_pairs, const gemm_tn_dev::GemmArgs& args, int grid,
+                               cudaStream_t stream) {
+  if (bf16) return k_pairs ? launch_splitk_kb<true, 2>(splits, args, grid, stream)
+                           : launch_splitk_kb<true, 1>(splits, args, grid, stream);
+  return k_pairs ? launch_splitk_kb<false, 2>(splits, args, grid, stream)
+                 : launch_splitk_kb<false, 1>(splits, args, grid, stream);
+}
+
+// (both forms of a stage take the same shared memory and threads)
 int max_resident_splitk(int splits, bool bf16, int num_sms) {
   switch (splits) {
-    case 2: return bf16 ? SplitKLauncher<2, true>::max_clusters(num_sms) : SplitKLauncher<2, false>::max_clusters(num_sms);
-    case 4: return bf16 ? SplitKLauncher<4, true>::max_clusters(num_sms) : SplitKLauncher<4, false>::max_clusters(num_sms);
-    case 8: return bf16 ? SplitKLauncher<8, true>::max_clusters(num_sms) : SplitKLauncher<8, false>::max_clusters(num_sms);
+    case 2: return bf16 ? SplitKLauncher<2, true, 1>::max_clusters(num_sms) : SplitKLauncher<2, false, 1>::max_clusters(num_sms);
+    case 4: return bf16 ? SplitKLauncher<4, true, 1>::max_clusters(num_sms) : SplitKLauncher<4, false, 1>::max_clusters(num_sms);
+    case 8: return bf16 ? SplitKLauncher<8, true, 1>::max_clusters(num_sms) : SplitKLauncher<8, false, 1>::max_clusters(num_sms);
     default: return 0;
   }
 }

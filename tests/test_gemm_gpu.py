@@ -345,7 +345,7 @@ def test_watchdog_reports_timeout_and_context_survives(config):
     # the decode kernel runs only for M <= 32 (a forced decode configuration
     # with more rows runs the 128 x 128 split-K kernel instead)
     m = 8 if config == "1cta_decode_splitk" else 512
-    n, k = 512, 512
+    n, k = 512, 1024
     dev = torch.device("cuda", 0)
     a_cpu, b_cpu = make_operands(m, n, k, "bf16", "uniform", seed=4)
     a, b = a_cpu.to(dev), b_cpu.to(dev)
@@ -353,9 +353,9 @@ def test_watchdog_reports_timeout_and_context_survives(config):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     t0 = time.perf_counter()
     # load 1 (counted from the start of each CTA's K range) exists for every
-    # configuration: K = 512 has 8 k-blocks, and the split-K kernels keep at
-    # least 2 per CTA (the decode kernel 4 in copies of two: a 2-way split for
-    # 8 x 512 x 512 gives each CTA two such copies)
+    # configuration: K = 1024 has 16 k-blocks, and the split-K kernels keep
+    # at least 4 per CTA here (512 x 512 x 1024 at S = 4; 8 x 512 x 1024 at
+    # S = 2 or 4), which they move in copies of two
     with forced_config(config), env_var("GEMM_TN_WATCHDOG_MS", "200"), env_var("GEMM_TN_TEST_DROP_LOAD", "1"):
         gt.mm_tn(a, b, out=out, status=status)
         ran = gt.gemm_tn_config_name(gt.gemm_tn_last_config())
@@ -450,12 +450,16 @@ def test_dependent_launch_chain(pad):
 
 @pytest.mark.parametrize("splits", ["2", "4", "8"])
 @pytest.mark.parametrize("mnk", [(128, 1024, 4096), (16, 4096, 2048), (300, 700, 1000), (129, 257, 513),
-                                 (1, 1, 1024), (200, 390, 4097)], ids=lambda s: "x".join(map(str, s)))
+                                 (1, 1, 1024), (200, 390, 4097), (256, 384, 1216), (64, 300, 320)],
+                         ids=lambda s: "x".join(map(str, s)))
 def test_split_k_over_a_cluster(mnk, splits):
     """K cut over a cluster of 2, 4 or 8 CTAs per 128 x 128 tile, the fp32
     partials added through distributed shared memory in CTA order: parity for
     ragged M, N, K (K = 4097 also repacks A and B), an odd C pitch written
-    only inside N, and bit-identical results on repeated launches."""
+    only inside N, and bit-identical results on repeated launches. With K a
+    multiple of 64 each copy moves two k-blocks (1216 = 19 x 64 leaves the
+    last copy's second k-block past K; 320 = 5 x 64 has fewer pairs than CTAs
+    at S = 4 and keeps one k-block per copy)."""
     from _parity import env_var
     m, n, k = mnk
     dev = torch.device("cuda", 0)
