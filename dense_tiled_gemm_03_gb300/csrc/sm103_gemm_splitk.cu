@@ -20,7 +20,7 @@
 // and no global workspace, flag or atomic is involved.
 //
 // Every mbarrier wait is bounded (GEMM_TN_ERR_TIMEOUT through the status
-// word); the roles never leave early, so both cluster barriers are always
+// word); the roles never leave early, so every cluster barrier is always
 // reached by every thread.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -140,8 +140,14 @@ __global__ void __launch_bounds__(splitk::kThreads, 1) gemm_tn_splitk_kernel(con
     tmem_alloc<1>(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish<1>();
   }
+  // The pipeline uses only this CTA's barriers and TMEM, so set-up ends at a
+  // CTA barrier. Its peers' shared memory is touched only in the reduction
+  // (and by a role that gives up, after the watchdog's budget): the cluster
+  // barrier that guarantees every peer has started is arrived at here and
+  // waited for there, off the path to the first copy.
   tc_fence_before_sync();
-  cluster_sync_all();
+  __syncthreads();
+  cluster_arrive_relaxed();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   // set-up may overlap the previous kernel in the stream; memory waits for
@@ -245,7 +251,9 @@ __global__ void __launch_bounds__(splitk::kThreads, 1) gemm_tn_splitk_kernel(con
   __syncwarp();
 
   // ---------------------------------------------------------------- cluster reduction
-  // every CTA's partial is in its shared memory: make them visible cluster-wide
+  // every peer has started (the set-up's arrival); then every CTA's partial
+  // is in its shared memory: make them visible cluster-wide
+  cluster_wait();
   tc_fence_before_sync();
   cluster_sync_all();
   {
@@ -406,8 +414,14 @@ __global__ void __launch_bounds__(decode::kThreads, 1) gemm_tn_decode_kernel(con
     tmem_alloc<1>(smem_addr(tmem_slot), L::kTmemCols);
     tmem_relinquish<1>();
   }
+  // The pipeline uses only this CTA's barriers and TMEM, so set-up ends at a
+  // CTA barrier. Its peers' shared memory is touched only in the reduction
+  // (and by a role that gives up, after the watchdog's budget): the cluster
+  // barrier that guarantees every peer has started is arrived at here and
+  // waited for there, off the path to the first copy.
   tc_fence_before_sync();
-  cluster_sync_all();
+  __syncthreads();
+  cluster_arrive_relaxed();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   // set-up may overlap the previous kernel in the stream; memory waits for
@@ -518,6 +532,7 @@ __global__ void __launch_bounds__(decode::kThreads, 1) gemm_tn_decode_kernel(con
   __syncwarp();
 
   // ---------------------------------------------------------------- cluster reduction
+  cluster_wait();   // every peer has started (the set-up's arrival)
   tc_fence_before_sync();
   cluster_sync_all();
   {
