@@ -39,8 +39,8 @@ cudaError_t launch_gemm_nn(int id, bool bf16, const gemm_tn_dev::GemmArgs& args,
 cudaError_t launch_gemm_fused(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_splitk(int splits, bool bf16, bool k_pairs, const gemm_tn_dev::GemmArgs& args, int grid,
                                cudaStream_t stream);
-cudaError_t launch_gemm_decode(int splits, int rows, bool bf16, bool k_pairs, const gemm_tn_dev::GemmArgs& args, int grid,
-                               cudaStream_t stream);
+cudaError_t launch_gemm_decode(int splits, int rows, bool bf16, bool k_pairs, const gemm_tn_dev::GemmArgs& args,
+                               int grid, cudaStream_t stream);
 int decode_rows(int64_t m);
 int max_resident_splitk(int splits, bool bf16, int num_sms);
 constexpr int kGb300SplitKResidentDefault[3] = {76, 36, 15};

@@ -54,7 +54,6 @@ constexpr int kFirstEpilogueWarp = 2;
 constexpr int kNumEpilogueWarps = 8;
 constexpr int kStatusTimeout = 6;      // == GEMM_TN_ERR_TIMEOUT
 
-// Kernel arguments. Tensor maps first: they must be 64-byte aligned.
 // Division by an invariant divisor d (1 <= d < 2^31) as a multiply-high, an
 // add and a shift, exact for every dividend n < 2^31: Granlund and
 // Montgomery, "Division by invariant integers using multiplication" (1994),
@@ -74,6 +73,7 @@ struct FastDiv {
 #endif
 };
 
+// Kernel arguments. Tensor maps first: they must be 64-byte aligned.
 struct GemmArgs {
   CUtensorMap tmap_a;     // A: dims {K, M}, box {64, 128}, 128B swizzle
   CUtensorMap tmap_b;     // B: dims {K, N}, box {64, BN / cta_group}, 128B swizzle
@@ -91,7 +91,8 @@ struct GemmArgs {
   FastDiv div_m_tiles;    // by num_m_tiles (the split-K and decode kernels' column-major tile order)
   int* status;            // nullable device int: first error code wins
   uint64_t timeout_ns;    // per-wait watchdog budget
-  int32_t drop_load_kb;   // test hook: producer of tile 0 skips this k-block's loads, the decode kernel this copy's (-1: never)
+  int32_t drop_load_kb;   // test hook: the producer skips this k-block's loads, or this copy's where one
+                          // copy moves two k-blocks (split-K and decode kernels); -1: never
   // Work split over the num_workers clusters of the grid. Tiles [0, dp_tiles)
   // go whole and round-robin to the workers. The sk_iters k-block iterations
   // of tiles [dp_tiles, num_tiles) (stream-K tail) are cut into sk_workers
@@ -322,9 +323,8 @@ __device__ __forceinline__ void st_release_gpu(uint64_t* p, uint64_t v) {
 }
 
 // The last phase the producer issued into each stage of its ring (up to 32
-// stages), held in two registers. A dynamically indexed array would sit in
-// local memory, and the thread's later memory operations, its first tensor
-// copy among them, would wait behind those local stores.
+// stages), held in two registers: a dynamically indexed array would live in
+// local memory, and with this none of the kernels needs a stack frame.
 struct IssuedPhases {
   uint32_t issued = 0u;   // bit s: some phase was issued into stage s
   uint32_t parity = 0u;   // bit s: the parity of that phase
@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
   // once that kernel has completed. Every thread but the producer waits for
   // it here. The producer first works out its first unit of work, which
   // depends on the launch's parameters alone, and waits just before its
-  // first copy, so that this arithmetic overlaps the previous kernel too.
+  // first copy, so that this arithmetic may overlap the previous kernel too.
   // The next kernel may then be scheduled: it takes an SM only when a CTA of
   // this grid leaves it, and this grid is resident as a whole, so nothing
   // here waits on it.

@@ -727,9 +727,12 @@ cudaError_t launch_gemm_splitk(int splits, bool bf16, bool k_pairs, const gemm_t
 // (both forms of a stage take the same shared memory and threads)
 int max_resident_splitk(int splits, bool bf16, int num_sms) {
   switch (splits) {
-    case 2: return bf16 ? SplitKLauncher<2, true, 1>::max_clusters(num_sms) : SplitKLauncher<2, false, 1>::max_clusters(num_sms);
-    case 4: return bf16 ? SplitKLauncher<4, true, 1>::max_clusters(num_sms) : SplitKLauncher<4, false, 1>::max_clusters(num_sms);
-    case 8: return bf16 ? SplitKLauncher<8, true, 1>::max_clusters(num_sms) : SplitKLauncher<8, false, 1>::max_clusters(num_sms);
+    case 2: return bf16 ? SplitKLauncher<2, true, 1>::max_clusters(num_sms)
+                        : SplitKLauncher<2, false, 1>::max_clusters(num_sms);
+    case 4: return bf16 ? SplitKLauncher<4, true, 1>::max_clusters(num_sms)
+                        : SplitKLauncher<4, false, 1>::max_clusters(num_sms);
+    case 8: return bf16 ? SplitKLauncher<8, true, 1>::max_clusters(num_sms)
+                        : SplitKLauncher<8, false, 1>::max_clusters(num_sms);
     default: return 0;
   }
 }
