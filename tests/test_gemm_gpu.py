@@ -515,6 +515,28 @@ def test_decode_split_k(mnk, splits):
     assert torch.equal(outs[0], outs[1]), "decode launches differ"
 
 
+@pytest.mark.parametrize("mnk", [(8, 4096, 4096), (32, 2048, 4160), (3, 1000, 2048)], ids=lambda s: "x".join(map(str, s)))
+def test_decode_bf16_default_choice(mnk):
+    """bf16 decode-like shapes through the default selection (the decode
+    kernel with two k-blocks per copy, K a multiple of 64, odd k-block count
+    included): parity, and bit-identical repeated launches."""
+    m, n, k = mnk
+    dev = torch.device("cuda", 0)
+    a_cpu, b_cpu = make_operands(m, n, k, "bf16", "normal_over_sqrt_k", seed=m + n + k)
+    a, b = a_cpu.to(dev), b_cpu.to(dev)
+    outs = []
+    for _ in range(2):
+        c = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        gt.mm_tn(a, b, out=c, status=status)
+        assert gt.gemm_tn_config_name(gt.gemm_tn_last_config()) == "1cta_decode_splitk"
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        outs.append(c.cpu())
+    assert_parity(outs[0], a_cpu, b_cpu, f"{mnk} bf16 decode")
+    assert torch.equal(outs[0], outs[1]), "decode launches differ"
+
+
 def test_split_k_is_chosen_for_few_tiles_and_matches_whole_tiles():
     """The default choice for 128 x 4096 x 4096 is the split-K cluster; its
     result is within the criterion of the whole-K single-CTA tiles'."""
