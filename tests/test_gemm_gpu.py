@@ -699,6 +699,21 @@ def test_host_entry_point_chunked_with_ragged_pitches():
     assert_sampled_parity(c_pinned, a_cpu, b_cpu, rows, cols, "host path")
 
 
+def test_host_entry_point_large_ragged():
+    """gemm_tn_host on a larger bf16 problem that it copies in two row chunks
+    of A and C (the last one ragged), with a padded K (2049) and B of 37 MB;
+    pinned and pageable buffers."""
+    m, n, k = 9000, 9000, 2049
+    a_cpu, b_cpu = make_operands(m, n, k, "bf16", "normal_over_sqrt_k", seed=78)
+    c_pinned = gt.mm_tn_host(a_cpu.pin_memory(), b_cpu.pin_memory())
+    c_pageable = gt.mm_tn_host(a_cpu, b_cpu)
+    assert torch.equal(c_pinned, c_pageable)
+    rng = np.random.Generator(np.random.PCG64(6))
+    rows = edge_indices(m, 4608, rng, 24)
+    cols = edge_indices(n, 4608, rng, 24)
+    assert_sampled_parity(c_pinned, a_cpu, b_cpu, rows, cols, "host path, large ragged")
+
+
 @pytest.mark.parametrize("config", CONFIGS)
 @pytest.mark.parametrize("mnk", [(1000, 1000, 640), (2304, 4352, 1000), (3001, 5003, 577), (4096, 4096, 512),
                                  (300, 2000, 700)], ids=lambda s: "x".join(map(str, s)))
