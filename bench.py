@@ -67,32 +67,32 @@ CSRC = ROOT / "dense_tiled_gemm_03_gb300" / "csrc"
 # are unchanged (a changed kernel makes it stale). Keyed by (workload, kernel
 # configuration) or, for the fused kernels, (workload, configuration, epilogue).
 NCU_TRAFFIC: dict[tuple, dict] = {
-    ("bf16_8192x8192x8192", "2cta_n256"): {  # 566.7 us
-        "bytes": 1074249984 + 136621568, "when": "2026-12-02", "source": "0d5ae9318df4",
-        "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 0, 0>>"},
-    ("fp16_4096x4096x4096", "2cta_n256_mc"): {  # 83.4 us
-        "bytes": 106280960 + 34165760, "when": "2026-12-02", "source": "0d5ae9318df4",
-        "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0>>"},
-    ("fp16_3001x5003x4097", "2cta_n256_mc"): {  # 83.7 us
-        "bytes": 98276096 + 27108352, "when": "2026-12-02", "source": "0d5ae9318df4",
-        "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0>>"},
-    ("bf16_128x16384x16384", "1cta_n128"): {  # 90.3 us
-        "bytes": 542196992 + 3294976, "when": "2026-12-02", "source": "0d5ae9318df4",
-        "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 128, 6, 1, 1, 0, 0, 0>>"},
-    ("fp16_256x256x256", "1cta_n64"): {  # 7.2 us
-        "bytes": 306432 + 0, "when": "2026-12-02", "source": "0d5ae9318df4",
-        "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 64, 8, 0, 1, 0, 0, 0>>"},
-    ("bf16_8x4096x4096", "1cta_decode_splitk"): {  # 11.6 us
-        "bytes": 33637376 + 0, "when": "2026-12-02", "source": "0d5ae9318df4",
+    ("bf16_8192x8192x8192", "2cta_n256"): {  # 562.4 us
+        "bytes": 1098981120 + 136559616, "when": "2026-12-02", "source": "e108a58f720e",
+        "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 0, 0, 0>>"},
+    ("fp16_4096x4096x4096", "2cta_n256_mc"): {  # 84.1 us
+        "bytes": 105147648 + 33478144, "when": "2026-12-02", "source": "e108a58f720e",
+        "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0, 0>>"},
+    ("fp16_3001x5003x4097", "2cta_n256_mc"): {  # 86.8 us
+        "bytes": 94949888 + 25451008, "when": "2026-12-02", "source": "e108a58f720e",
+        "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0, 0>>"},
+    ("bf16_128x16384x16384", "1cta_n128"): {  # 92.0 us
+        "bytes": 542155264 + 3268608, "when": "2026-12-02", "source": "e108a58f720e",
+        "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 128, 6, 1, 1, 0, 0, 0, 0>>"},
+    ("fp16_256x256x256", "1cta_n64"): {  # 6.9 us
+        "bytes": 305664 + 0, "when": "2026-12-02", "source": "e108a58f720e",
+        "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 64, 4, 0, 1, 0, 0, 0, 1>>"},
+    ("bf16_8x4096x4096", "1cta_decode_splitk"): {  # 11.9 us
+        "bytes": 33637632 + 0, "when": "2026-12-02", "source": "e108a58f720e",
         "kernel": "gemm_tn_decode_kernel<4, 16, 1, 2>"},
-    ("bf16_8192x8192x8192", "2cta_n256", "bias_gelu"): {  # 574.2 us
-        "bytes": 1067604480 + 135800576, "when": "2026-12-02", "source": "0d5ae9318df4",
-        "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 1, 0>>"},
+    ("bf16_8192x8192x8192", "2cta_n256", "bias_gelu"): {  # 576.7 us
+        "bytes": 1088462336 + 135944704, "when": "2026-12-02", "source": "e108a58f720e",
+        "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 1, 0, 0>>"},
 }
 # the same for the attention kernel, keyed by workload
 NCU_TRAFFIC_ATTN: dict[str, dict] = {
-    "attn_bf16_b2_s8192_h32_d128_causal": {  # 755.8 us
-        "bytes": 453478912 + 117583872, "when": "2026-12-02", "source": "bc55908143dc",
+    "attn_bf16_b2_s8192_h32_d128_causal": {  # 757.5 us
+        "bytes": 453220608 + 117460480, "when": "2026-12-02", "source": "3e9b1fb9e274",
         "kernel": "flash_attn_fwd_kernel<Cfg<128, 1>>"},
 }
 

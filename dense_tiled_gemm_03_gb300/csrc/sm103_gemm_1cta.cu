@@ -1,5 +1,6 @@
 // sm103_gemm_1cta.cu -- instantiations of the tcgen05 GEMM kernel with one CTA
-// per output tile (cta_group::1): 128 x 256, 128 x 128 and 128 x 64 tiles.
+// per output tile (cta_group::1): 128 x 256, 128 x 128 and 128 x 64 tiles, the
+// last two also with two k-blocks per stage.
 #include "gemm_tn_internal.h"
 #include "sm103_launch.cuh"
 
@@ -11,8 +12,26 @@ using Cfg128F16 = gemm_tn_dev::GemmConfig<1, 128, 6, false>;
 using Cfg128Bf16 = gemm_tn_dev::GemmConfig<1, 128, 6, true>;
 using Cfg64F16 = gemm_tn_dev::GemmConfig<1, 64, 8, false>;
 using Cfg64Bf16 = gemm_tn_dev::GemmConfig<1, 64, 8, true>;
+// two k-blocks per stage: half the stages in the same shared memory (128 x
+// 128 and 128 x 64 tiles; 128 x 256 tiles would keep only two stages, and
+// ran 18% slower so at 2048^3)
+template <int kBlockN, int kStages, bool kBf16>
+using CfgPairs = gemm_tn_dev::GemmConfig<1, kBlockN, kStages, kBf16, 1, false, false, false, true>;
 
-cudaError_t launch_gemm_1cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& args, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm_1cta(int id, bool bf16, bool k_pairs, const gemm_tn_dev::GemmArgs& args, int grid,
+                             cudaStream_t stream) {
+  if (k_pairs) {
+    switch (id) {
+      case kCfg1CtaN128:
+        return bf16 ? Launcher<CfgPairs<128, 3, true>>::launch(args, grid, stream)
+                    : Launcher<CfgPairs<128, 3, false>>::launch(args, grid, stream);
+      case kCfg1CtaN64:
+        return bf16 ? Launcher<CfgPairs<64, 4, true>>::launch(args, grid, stream)
+                    : Launcher<CfgPairs<64, 4, false>>::launch(args, grid, stream);
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
   switch (id) {
     case kCfg1CtaN256:
       return bf16 ? Launcher<Cfg256Bf16>::launch(args, grid, stream) : Launcher<Cfg256F16>::launch(args, grid, stream);
@@ -24,6 +43,10 @@ cudaError_t launch_gemm_1cta(int id, bool bf16, const gemm_tn_dev::GemmArgs& arg
       return cudaErrorInvalidValue;
   }
 }
+
+static_assert(CfgPairs<128, 3, false>::kSmemBytes <= Cfg128F16::kSmemBytes &&
+                  CfgPairs<64, 4, false>::kSmemBytes <= Cfg64F16::kSmemBytes,
+              "the paired stages take no more shared memory (occupancy queries use the single form)");
 
 int max_resident_1cta(int id, bool bf16) {
   switch (id) {

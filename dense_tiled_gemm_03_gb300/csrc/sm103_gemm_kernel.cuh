@@ -129,9 +129,16 @@ struct GemmArgs {
 };
 
 template <int kCtaGroup_, int kBlockN_, int kStages_, bool kBf16_, int kClusterPairs_ = 1, bool kBMnMajor_ = false,
-          bool kFused_ = false, bool kTailSplit_ = false>
+          bool kFused_ = false, bool kTailSplit_ = false, bool kKPairs_ = false>
 struct GemmConfig {
   static constexpr int kCtaGroup = kCtaGroup_;
+  // kKPairs: a stage holds two k-blocks, moved by one 3-D tensor copy per
+  // operand ({64, rows, 2} boxes over {64, rows, K / 64} maps; a k-block past
+  // K reads as zeros), for single-CTA tiles whose units of work each cover all
+  // of K in order (no stream-K range, rotated K walk or cut tail tile). The
+  // producer then issues half the copies and barrier operations per byte.
+  static constexpr bool kKPairs = kKPairs_;
+  static constexpr int kKb = kKPairs ? 2 : 1;   // k-blocks per stage
   static constexpr bool kFused = kFused_;
   // kTailSplit: the instantiation that can run the cut sub-tiles of the last
   // wave; the others keep every unit a whole tile (the split arithmetic
@@ -156,9 +163,10 @@ struct GemmConfig {
   static constexpr int kMmaK = 16;
   static constexpr int kStages = kStages_;
   static constexpr bool kBf16 = kBf16_;
-  static constexpr uint32_t kATileBytes = kBlockM * kBlockK * 2;
-  static constexpr uint32_t kBTileBytes = kBRows * kBlockK * 2;
-  static constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr uint32_t kATileBytes = kBlockM * kBlockK * 2;   // A of one k-block
+  static constexpr uint32_t kBTileBytes = kBRows * kBlockK * 2;     // B of one k-block
+  static constexpr uint32_t kStageA = kKb * kATileBytes;            // A of one stage
+  static constexpr uint32_t kStageB = kKb * kBTileBytes;            // B of one stage
   static constexpr int kAccCols = kBlockN;               // fp32 columns per accumulator
   static constexpr int kNumAcc = 2;
   static constexpr uint32_t kTmemCols = kAccCols * kNumAcc;
@@ -171,8 +179,8 @@ struct GemmConfig {
   static_assert(32 * kStageRowWords * 4 <= kEpiWarpBytes, "transpose staging fits the warp's slot");
   // layout (offsets from the 1024-aligned base)
   static constexpr uint32_t kOffA = 0;
-  static constexpr uint32_t kOffB = kOffA + kStages * kATileBytes;
-  static constexpr uint32_t kOffEpi = kOffB + kStages * kBTileBytes;
+  static constexpr uint32_t kOffB = kOffA + kStages * kStageA;
+  static constexpr uint32_t kOffEpi = kOffB + kStages * kStageB;
   static constexpr uint32_t kOffBar = (kOffEpi + kEpiBytes + 7u) & ~7u;
   // full, empty, acc_full, acc_empty, drain
   static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 1;
@@ -186,6 +194,8 @@ struct GemmConfig {
   static_assert(kBlockN % 32 == 0 && kBlockN >= 32 && kBlockN <= 256, "MMA N");
   static_assert(kCtaGroup == 1 || kCtaGroup == 2, "cta group");
   static_assert(kStages >= 1 && kStages <= 32, "issued phases fit a 32-bit mask");
+  static_assert(!kKPairs || (kCtaGroup == 1 && !kMulticastA && !kBMnMajor && !kTailSplit),
+                "two k-blocks per stage: single-CTA K-major tiles, whole units of work");
   static_assert(kClusterPairs == 1 || (kClusterPairs == 2 && kCtaGroup == 2), "A multicast pairs CTA pairs");
   static_assert(kBRows % 8 == 0 && kBRows <= 256, "TMA box rows");
   static_assert(!kBMnMajor || kBRows % 64 == 0, "MN-major B is loaded in 64-wide boxes");
@@ -422,8 +432,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
   const uint32_t pair_leader = cluster_rank & ~1u;
   const bool leader = cta_rank == 0;
 
-  auto a_tile = [&](int s) { return base + Cfg::kOffA + s * Cfg::kATileBytes; };
-  auto b_tile = [&](int s) { return base + Cfg::kOffB + s * Cfg::kBTileBytes; };
+  auto a_tile = [&](int s) { return base + Cfg::kOffA + s * Cfg::kStageA; };
+  auto b_tile = [&](int s) { return base + Cfg::kOffB + s * Cfg::kStageB; };
   auto full_bar = [&](int s) { return base + Cfg::kOffBar + 8u * s; };
   auto empty_bar = [&](int s) { return base + Cfg::kOffBar + 8u * (Cfg::kStages + s); };
   auto acc_full_bar = [&](int a) { return base + Cfg::kOffBar + 8u * (2 * Cfg::kStages + a); };
@@ -519,6 +529,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             }
           } else if constexpr (Cfg::kCtaGroup == 2) {
             tma_load_2d_pair(tmap_b, b_tile(stage_), bar, kb_ * Cfg::kBlockK, b_row);
+          } else if constexpr (Cfg::kKPairs) {
+            tma_load_3d(tmap_b, b_tile(stage_), bar, 0, b_row, 2 * kb_);   // k-blocks 2 kb_, 2 kb_ + 1
           } else if (args.b_evict_first) {
             tma_load_2d_hint(tmap_b, b_tile(stage_), bar, kb_ * Cfg::kBlockK, b_row, pol_b);
           } else {
@@ -526,7 +538,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
           }
         };
         const int kstart = k_start(args, item, tj);
-        for (int kb_i = item.kb_begin; kb_i < item.kb_end; ++kb_i) {
+        // stages of this unit of work (kKb k-blocks each; with two, every
+        // unit covers all of K from k-block 0)
+        const int st_begin = item.kb_begin / Cfg::kKb;
+        const int st_end = (item.kb_end + Cfg::kKb - 1) / Cfg::kKb;
+        for (int kb_i = st_begin; kb_i < st_end; ++kb_i) {
           if (!wd.wait(empty_bar(stage), phase ^ 1u)) {
             ok = false;
             break;
@@ -560,13 +576,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
             }
             continue;
           }
-          if (leader) mbar_arrive_expect_tx(fb, Cfg::kCtaGroup * (Cfg::kATileBytes + b_bytes));
+          if (leader) mbar_arrive_expect_tx(fb, Cfg::kCtaGroup * Cfg::kKb * (Cfg::kATileBytes + b_bytes));
           if (!drop) {
             const int x = kb * Cfg::kBlockK;
             if constexpr (Cfg::kCtaGroup == 2) {
               const uint32_t fb_leader = map_to_cta(fb, pair_leader);
               tma_load_2d_pair(&args.tmap_a, a_tile(stage), fb_leader, x, a_row);
               load_b(stage, fb_leader, kb);
+            } else if constexpr (Cfg::kKPairs) {
+              tma_load_3d(&args.tmap_a, a_tile(stage), fb, 0, a_row, 2 * kb);   // k-blocks 2 kb, 2 kb + 1
+              load_b(stage, fb, kb);
             } else {
               tma_load_2d(&args.tmap_a, a_tile(stage), fb, x, a_row);
               load_b(stage, fb, kb);
@@ -614,23 +633,30 @@ __global__ void __launch_bounds__(kNumThreads, 1) gemm_tn_sm103_kernel(const __g
         const uint32_t idesc =
             item.nsub == 1 ? Cfg::kIdesc
                            : mma_idesc_f16(Cfg::kBf16, Cfg::kTileM, Cfg::kBlockN >> item.nsub_log2, Cfg::kBMnMajor);
-        for (int kb = item.kb_begin; kb < item.kb_end; ++kb) {
+        const int st_begin = item.kb_begin / Cfg::kKb;
+        const int st_end = (item.kb_end + Cfg::kKb - 1) / Cfg::kKb;
+        for (int kb = st_begin; kb < st_end; ++kb) {
           if (!wd.wait(full_bar(stage), phase)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage));
-          const uint64_t b_desc = Cfg::kBMnMajor ? sw128_mnmajor_desc(b_tile(stage), Cfg::kBMnBoxBytes)
-                                                 : sw128_kmajor_desc(b_tile(stage));
           // one K=16 step: 32 bytes along a K-major row, or two 1024-byte
           // 8-row K groups of an MN-major tile
           constexpr uint32_t kBStep = Cfg::kBMnMajor ? (2048u >> 4) : 2u;
+          constexpr int kSteps = Cfg::kBlockK / Cfg::kMmaK;   // per k-block
 #pragma unroll
-          for (int kk = 0; kk < Cfg::kBlockK / Cfg::kMmaK; ++kk) {
-            // advancing 16 elements along K = 32 bytes = 2 descriptor units
-            mma_f16<Cfg::kCtaGroup>(d_tmem, a_desc + 2u * kk, b_desc + kBStep * kk, idesc,
-                                    (kb > item.kb_begin || kk > 0) ? 1u : 0u);
+          for (int kb2 = 0; kb2 < Cfg::kKb; ++kb2) {   // k-blocks of the stage
+            const uint64_t a_desc = sw128_kmajor_desc(a_tile(stage) + kb2 * Cfg::kATileBytes);
+            const uint64_t b_desc = Cfg::kBMnMajor
+                                        ? sw128_mnmajor_desc(b_tile(stage), Cfg::kBMnBoxBytes)
+                                        : sw128_kmajor_desc(b_tile(stage) + kb2 * Cfg::kBTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kSteps; ++kk) {
+              // advancing 16 elements along K = 32 bytes = 2 descriptor units
+              mma_f16<Cfg::kCtaGroup>(d_tmem, a_desc + 2u * kk, b_desc + kBStep * kk, idesc,
+                                      (kb > st_begin || kb2 > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           if constexpr (Cfg::kMulticastA) {
             mma_commit_pair(empty_bar(stage), 0xF);   // both pairs' buffers hold halves of this A

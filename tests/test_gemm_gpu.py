@@ -515,6 +515,27 @@ def test_decode_split_k(mnk, splits):
     assert torch.equal(outs[0], outs[1]), "decode launches differ"
 
 
+@pytest.mark.parametrize("config", ["1cta_n64", "1cta_n128"])
+@pytest.mark.parametrize("mnk", [(256, 256, 192), (300, 520, 1216), (1000, 700, 64), (129, 1000, 4032)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_single_cta_two_k_blocks_per_copy(mnk, config):
+    """128 x 64 and 128 x 128 tiles with K a multiple of 64 move two k-blocks
+    per copy: an odd k-block count (3, 19, 63) leaves the last copy's second
+    k-block past K, and K = 64 has only that one; ragged M and N. Parity in
+    both dtypes and bit-identical repeated launches."""
+    m, n, k = mnk
+    for dtype in ("fp16", "bf16"):
+        a_cpu, b_cpu = make_operands(m, n, k, dtype, "normal_over_sqrt_k", seed=m + 3 * n + k)
+        outs = []
+        for _ in range(2):
+            c, st = gpu_gemm(a_cpu, b_cpu, config)
+            assert st == 0
+            assert gt.gemm_tn_config_name(gt.gemm_tn_last_config()) == config
+            outs.append(c)
+        assert_parity(outs[0], a_cpu, b_cpu, f"{mnk} {config} {dtype}")
+        assert torch.equal(outs[0], outs[1]), "launches differ"
+
+
 @pytest.mark.parametrize("mnk", [(8, 4096, 4096), (32, 2048, 4160), (3, 1000, 2048)], ids=lambda s: "x".join(map(str, s)))
 def test_decode_bf16_default_choice(mnk):
     """bf16 decode-like shapes through the default selection (the decode
