@@ -67,32 +67,32 @@ CSRC = ROOT / "dense_tiled_gemm_03_gb300" / "csrc"
 # are unchanged (a changed kernel makes it stale). Keyed by (workload, kernel
 # configuration) or, for the fused kernels, (workload, configuration, epilogue).
 NCU_TRAFFIC: dict[tuple, dict] = {
-    ("bf16_8192x8192x8192", "2cta_n256"): {  # 562.4 us
-        "bytes": 1098981120 + 136559616, "when": "2026-12-02", "source": "e108a58f720e",
+    ("bf16_8192x8192x8192", "2cta_n256"): {  # 563.6 us
+        "bytes": 1106656512 + 136681216, "when": "2026-12-02", "source": "cfd20c33239a",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 0, 0, 0>>"},
-    ("fp16_4096x4096x4096", "2cta_n256_mc"): {  # 84.1 us
-        "bytes": 105147648 + 33478144, "when": "2026-12-02", "source": "e108a58f720e",
+    ("fp16_4096x4096x4096", "2cta_n256_mc"): {  # 83.2 us
+        "bytes": 106215168 + 33601280, "when": "2026-12-02", "source": "cfd20c33239a",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0, 0>>"},
-    ("fp16_3001x5003x4097", "2cta_n256_mc"): {  # 86.8 us
-        "bytes": 94949888 + 25451008, "when": "2026-12-02", "source": "e108a58f720e",
+    ("fp16_3001x5003x4097", "2cta_n256_mc"): {  # 84.2 us
+        "bytes": 98493184 + 27248896, "when": "2026-12-02", "source": "cfd20c33239a",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0, 0>>"},
-    ("bf16_128x16384x16384", "1cta_n128"): {  # 92.0 us
-        "bytes": 542155264 + 3268608, "when": "2026-12-02", "source": "e108a58f720e",
+    ("bf16_128x16384x16384", "1cta_n128"): {  # 92.7 us
+        "bytes": 542157056 + 3254272, "when": "2026-12-02", "source": "cfd20c33239a",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 128, 6, 1, 1, 0, 0, 0, 0>>"},
-    ("fp16_256x256x256", "1cta_n64"): {  # 6.9 us
-        "bytes": 305664 + 0, "when": "2026-12-02", "source": "e108a58f720e",
+    ("fp16_256x256x256", "1cta_n64"): {  # 7.3 us
+        "bytes": 305920 + 0, "when": "2026-12-02", "source": "cfd20c33239a",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 64, 4, 0, 1, 0, 0, 0, 1>>"},
-    ("bf16_8x4096x4096", "1cta_decode_splitk"): {  # 11.9 us
-        "bytes": 33637632 + 0, "when": "2026-12-02", "source": "e108a58f720e",
+    ("bf16_8x4096x4096", "1cta_decode_splitk"): {  # 11.6 us
+        "bytes": 33637632 + 0, "when": "2026-12-02", "source": "cfd20c33239a",
         "kernel": "gemm_tn_decode_kernel<4, 16, 1, 2>"},
-    ("bf16_8192x8192x8192", "2cta_n256", "bias_gelu"): {  # 576.7 us
-        "bytes": 1088462336 + 135944704, "when": "2026-12-02", "source": "e108a58f720e",
+    ("bf16_8192x8192x8192", "2cta_n256", "bias_gelu"): {  # 574.9 us
+        "bytes": 1082396672 + 136055808, "when": "2026-12-02", "source": "cfd20c33239a",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 1, 0, 0>>"},
 }
 # the same for the attention kernel, keyed by workload
 NCU_TRAFFIC_ATTN: dict[str, dict] = {
-    "attn_bf16_b2_s8192_h32_d128_causal": {  # 757.5 us
-        "bytes": 453220608 + 117460480, "when": "2026-12-02", "source": "3e9b1fb9e274",
+    "attn_bf16_b2_s8192_h32_d128_causal": {  # 757.0 us
+        "bytes": 454098944 + 117187840, "when": "2026-12-02", "source": "3e9b1fb9e274",
         "kernel": "flash_attn_fwd_kernel<Cfg<128, 1>>"},
 }
 

@@ -91,8 +91,9 @@ struct GemmArgs {
   FastDiv div_m_tiles;    // by num_m_tiles (the split-K and decode kernels' column-major tile order)
   int* status;            // nullable device int: first error code wins
   uint64_t timeout_ns;    // per-wait watchdog budget
-  int32_t drop_load_kb;   // test hook: the producer skips this k-block's loads, or this copy's where one
-                          // copy moves two k-blocks (split-K and decode kernels); -1: never
+  int32_t drop_load_kb;   // test hook: the producer skips the loads of this stage of its first unit of
+                          // work (a stage holds one k-block, or two with kKPairs and in the split-K and
+                          // decode kernels); -1: never
   // Work split over the num_workers clusters of the grid. Tiles [0, dp_tiles)
   // go whole and round-robin to the workers. The sk_iters k-block iterations
   // of tiles [dp_tiles, num_tiles) (stream-K tail) are cut into sk_workers

@@ -333,9 +333,9 @@ namespace decode {
 // 128 x 128 split-K kernel are in flight per SM.
 //
 // kKb k-blocks per stage: with K a multiple of 64, one 3-D tensor copy moves
-// two k-blocks of B (and one of A) at once ({64, rows, 2} boxes over the maps
-// {64, rows, K / 64}; a k-block past K, when their count is odd, reads as
-// zeros). The producer thread issues half the copies and barrier operations
+// two k-blocks of B, and another two of A, at once ({64, rows, 2} boxes over
+// the maps {64, rows, K / 64}; a k-block past K, when their count is odd,
+// reads as zeros). The producer thread issues half the copies and barrier operations
 // per byte: at 16 k-blocks per CTA its issue rate, ~550 clocks per k-block,
 // had paced the stream (8 x 4096 x 4096: 6.26 -> 5.73 us per call replayed).
 constexpr int kThreads = 192;
