@@ -67,32 +67,32 @@ CSRC = ROOT / "dense_tiled_gemm_03_gb300" / "csrc"
 # are unchanged (a changed kernel makes it stale). Keyed by (workload, kernel
 # configuration) or, for the fused kernels, (workload, configuration, epilogue).
 NCU_TRAFFIC: dict[tuple, dict] = {
-    ("bf16_8192x8192x8192", "2cta_n256"): {  # 563.6 us
-        "bytes": 1106656512 + 136681216, "when": "2026-12-02", "source": "cfd20c33239a",
+    ("bf16_8192x8192x8192", "2cta_n256"): {  # 546.8 us
+        "bytes": 1082566400 + 136527872, "when": "2026-12-02", "source": "c6c6d69fc4ea",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 0, 0, 0>>"},
-    ("fp16_4096x4096x4096", "2cta_n256_mc"): {  # 83.2 us
-        "bytes": 106215168 + 33601280, "when": "2026-12-02", "source": "cfd20c33239a",
+    ("fp16_4096x4096x4096", "2cta_n256_mc"): {  # 81.9 us
+        "bytes": 106305536 + 33761792, "when": "2026-12-02", "source": "c6c6d69fc4ea",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0, 0>>"},
-    ("fp16_3001x5003x4097", "2cta_n256_mc"): {  # 84.2 us
-        "bytes": 98493184 + 27248896, "when": "2026-12-02", "source": "cfd20c33239a",
+    ("fp16_3001x5003x4097", "2cta_n256_mc"): {  # 83.9 us
+        "bytes": 96957440 + 27212800, "when": "2026-12-02", "source": "c6c6d69fc4ea",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 0, 2, 0, 0, 0, 0>>"},
-    ("bf16_128x16384x16384", "1cta_n128"): {  # 92.7 us
-        "bytes": 542157056 + 3254272, "when": "2026-12-02", "source": "cfd20c33239a",
+    ("bf16_128x16384x16384", "1cta_n128"): {  # 92.0 us
+        "bytes": 542159872 + 3272960, "when": "2026-12-02", "source": "c6c6d69fc4ea",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 128, 6, 1, 1, 0, 0, 0, 0>>"},
-    ("fp16_256x256x256", "1cta_n64"): {  # 7.3 us
-        "bytes": 305920 + 0, "when": "2026-12-02", "source": "cfd20c33239a",
+    ("fp16_256x256x256", "1cta_n64"): {  # 6.8 us
+        "bytes": 305920 + 0, "when": "2026-12-02", "source": "c6c6d69fc4ea",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<1, 64, 4, 0, 1, 0, 0, 0, 1>>"},
-    ("bf16_8x4096x4096", "1cta_decode_splitk"): {  # 11.6 us
-        "bytes": 33637632 + 0, "when": "2026-12-02", "source": "cfd20c33239a",
+    ("bf16_8x4096x4096", "1cta_decode_splitk"): {  # 11.9 us
+        "bytes": 33637632 + 0, "when": "2026-12-02", "source": "c6c6d69fc4ea",
         "kernel": "gemm_tn_decode_kernel<4, 16, 1, 2>"},
-    ("bf16_8192x8192x8192", "2cta_n256", "bias_gelu"): {  # 574.9 us
-        "bytes": 1082396672 + 136055808, "when": "2026-12-02", "source": "cfd20c33239a",
+    ("bf16_8192x8192x8192", "2cta_n256", "bias_gelu"): {  # 555.5 us
+        "bytes": 1072375040 + 135900416, "when": "2026-12-02", "source": "c6c6d69fc4ea",
         "kernel": "gemm_tn_sm103_kernel<GemmConfig<2, 256, 6, 1, 1, 0, 1, 0, 0>>"},
 }
 # the same for the attention kernel, keyed by workload
 NCU_TRAFFIC_ATTN: dict[str, dict] = {
-    "attn_bf16_b2_s8192_h32_d128_causal": {  # 757.0 us
-        "bytes": 454098944 + 117187840, "when": "2026-12-02", "source": "3e9b1fb9e274",
+    "attn_bf16_b2_s8192_h32_d128_causal": {  # 754.8 us
+        "bytes": 454553088 + 117239552, "when": "2026-12-02", "source": "b1f83bdde46d",
         "kernel": "flash_attn_fwd_kernel<Cfg<128, 1>>"},
 }
 

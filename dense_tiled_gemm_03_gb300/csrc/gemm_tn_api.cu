@@ -391,9 +391,21 @@ int choose_config(int64_t m, int64_t n, int64_t k, int resident_pairs = 76, int 
   const int forced = parse_forced_config();
   if (forced >= 0) return forced;
   // few output tiles: split K over a cluster (with at most 32 rows of A, B's
-  // rows take the MMA's M side)
-  if (splitk_factor(m, n, k, 2 * resident_pairs, splitk_resident) > 1)
-    return m <= 32 ? kCfgDecodeSplitK : kCfg1CtaSplitK;
+  // rows take the MMA's M side) -- unless K is short and 128 x 64 tiles,
+  // which move two k-blocks per copy when K is a multiple of 64, fit in one
+  // round of the SMs: then the split's partial-sum exchange costs more than
+  // it saves (GB300, us per call in CUDA graphs, 1cta_n64 vs the K split:
+  // 256 x 256 x 512 4.21 vs 4.62 at S = 4, 512^3 4.41 vs 4.93 at S = 4, 1024^3
+  // 5.92 vs 6.37 at S = 2). Longer K, or a wider split, keeps the split.
+  const int splits = splitk_factor(m, n, k, 2 * resident_pairs, splitk_resident);
+  if (splits > 1) {
+    const int64_t kb = (k + 63) / 64;
+    const int64_t n64_tiles = ((m + 127) / 128) * ((n + 63) / 64);
+    const bool short_k = m > 128 && k % 64 == 0 && n64_tiles <= 2 * static_cast<int64_t>(resident_pairs) &&
+                         (kb <= 8 || (kb <= 16 && splits == 2));
+    if (!short_k) return m <= 32 ? kCfgDecodeSplitK : kCfg1CtaSplitK;
+    return kCfg1CtaN64;
+  }
   // Tiny problems: 128 x 64 tiles while they fill at most half the SMs, so
   // more SMs share the operand loads and each epilogue is half as long
   // (GB300, us per call in CUDA graphs, 1cta_n64 vs 1cta_n128: 256^3 3.90

@@ -69,7 +69,13 @@ def test_config_table(lib, monkeypatch):
     assert splits(128, 1024, 4096) == 8                   # 8 tiles, 64 k-blocks
     assert splits(64, 2048, 8192) == 4                    # 16 tiles: more than 15 clusters of 8
     assert splits(1024, 1024, 8192) == 2                  # 64 tiles: more than 36 clusters of 4
-    assert splits(512, 512, 512) == 4                     # 8 k-blocks: 2 per CTA of a 4-CTA cluster
+    assert splits(512, 512, 512) == 0                     # 8 k-blocks: 32 tiles of 128 x 64 in one round
+    assert sel(512, 512, 512) == "1cta_n64"
+    assert sel(1024, 1024, 1024) == "1cta_n64"            # 16 k-blocks, a 2-way split: 128 tiles of 128 x 64
+    assert sel(200, 512, 512) == "1cta_n64"               # 8 k-blocks, 16 tiles of 128 x 64
+    assert sel(512, 512, 576) == "1cta_n128_splitk"       # 9 k-blocks at a 4-way split: the split stays
+    assert sel(512, 512, 500) == "1cta_n128_splitk"       # K not a multiple of 64: one k-block per copy
+    assert sel(128, 1024, 512) == "1cta_n128_splitk"      # one row of tiles (M <= 128): the split stays
     assert splits(256, 256, 960) == 4
     assert splits(256, 256, 1024) == 4                    # 16 k-blocks: 8 splits would leave 2 per CTA
     assert splits(8, 4096, 4096) == 4                     # the decode kernel's split
