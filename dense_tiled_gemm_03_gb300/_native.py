@@ -238,6 +238,19 @@ class _on_device:
         return False
 
 
+def _status_ptr(status, device):
+    """Device pointer of the optional watchdog status word: a one-element (or
+    longer) contiguous int32 tensor on the call's device, or None. The kernels
+    write an int through it, so any other tensor is refused here."""
+    import torch
+    if status is None:
+        return None
+    if not isinstance(status, torch.Tensor) or status.device != device or status.dtype != torch.int32 or \
+            status.numel() < 1 or not status.is_contiguous():
+        raise ValueError(f"status must be a contiguous int32 tensor of at least one element on {device}")
+    return status.data_ptr()
+
+
 def _row_pitch(t, cols: int) -> int:
     if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
         raise ValueError("operands must be 2-D with unit stride along the last dimension")
@@ -264,7 +277,7 @@ def mm_tn(a, b, out=None, status=None):
     elif out.shape != (m, n) or out.dtype != a.dtype or out.device != a.device:
         raise ValueError("out must be [M, N] with the dtype and device of a")
     lda, ldb, ldc = _row_pitch(a, k), _row_pitch(b, k), _row_pitch(out, n)
-    d_status = status.data_ptr() if status is not None else None
+    d_status = _status_ptr(status, a.device)
     with _on_device(a.device) as stream:
         rc = library().gemm_tn_ex(_dtype_code(a), m, n, k, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(),
                                   ldc, d_status, stream)
@@ -303,12 +316,13 @@ def mm_tn_fused(a, b, out=None, alpha=1.0, beta=0.0, bias=None, activation="none
         out = torch.zeros((m, n), dtype=out_dtype, device=a.device)
     elif out.shape != (m, n) or out.dtype != out_dtype or out.device != a.device:
         raise ValueError(f"out must be [M, N] of {out_dtype} on a's device")
-    if bias is not None and (bias.dtype != torch.float32 or bias.shape != (n,) or bias.device != a.device):
-        raise ValueError("bias must be a CUDA fp32 [N] tensor")
+    if bias is not None and (bias.dtype != torch.float32 or bias.shape != (n,) or bias.device != a.device or
+                             not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous CUDA fp32 [N] tensor on a's device")
     ep = GemmTnEpilogue(float(alpha), float(beta), bias.data_ptr() if bias is not None else None,
                         _ACTIVATIONS[activation], codes[out_dtype])
     lda, ldb, ldc = _row_pitch(a, k), _row_pitch(b, k), _row_pitch(out, n)
-    d_status = status.data_ptr() if status is not None else None
+    d_status = _status_ptr(status, a.device)
     with _on_device(a.device) as stream:
         rc = gemm_tn_fused(_dtype_code(a), m, n, k, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(), ldc, ep,
                            d_status, stream)
@@ -334,7 +348,7 @@ def mm_nn(a, b, out=None, status=None):
     elif out.shape != (m, n) or out.dtype != a.dtype or out.device != a.device:
         raise ValueError("out must be [M, N] with the dtype and device of a")
     lda, ldb, ldc = _row_pitch(a, k), _row_pitch(b, n), _row_pitch(out, n)
-    d_status = status.data_ptr() if status is not None else None
+    d_status = _status_ptr(status, a.device)
     with _on_device(a.device) as stream:
         rc = gemm_nn(_dtype_code(a), m, n, k, a.data_ptr(), lda, b.data_ptr(), ldb, out.data_ptr(), ldc,
                      d_status, stream)
@@ -350,16 +364,25 @@ def mm_tn_host(a, b, out=None, device=None):
     import torch
     if a.device.type != "cpu" or b.device.type != "cpu":
         raise ValueError("mm_tn_host takes CPU tensors")
+    if a.dim() != 2 or b.dim() != 2:
+        raise ValueError("a and b must be 2-D")
+    if a.dtype != b.dtype:
+        raise TypeError("a and b must have the same dtype")
+    dtype = _dtype_code(a)
     a = a.contiguous()
     b = b.contiguous()
     m, k = a.shape
-    n = b.shape[0]
+    n, kb = b.shape
+    if kb != k:
+        raise ValueError(f"inner dimensions differ: {tuple(a.shape)} x {tuple(b.shape)}^T")
     if out is None:
         out = torch.empty((m, n), dtype=a.dtype)
+    elif out.device.type != "cpu" or out.shape != (m, n) or out.dtype != a.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CPU [M, N] tensor with the dtype of a")
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     stream = torch.cuda.current_stream(dev).cuda_stream
     with torch.cuda.device(dev):
-        rc = gemm_tn_host(_dtype_code(a), m, n, k, a.data_ptr(), b.data_ptr(), out.data_ptr(), stream)
+        rc = gemm_tn_host(dtype, m, n, k, a.data_ptr(), b.data_ptr(), out.data_ptr(), stream)
     if rc != GEMM_TN_OK:
         raise GemmTnError(rc, "gemm_tn_host")
     return out
@@ -386,7 +409,7 @@ def flash_attn(q, k, v, causal=True, scale=None, out=None, status=None):
     elif out.shape != q.shape or out.dtype != q.dtype or out.device != q.device or not out.is_contiguous():
         raise ValueError("out must be a contiguous tensor with q's shape, dtype and device")
     b, s, h, d = q.shape
-    d_status = status.data_ptr() if status is not None else None
+    d_status = _status_ptr(status, q.device)
     with _on_device(q.device) as stream:
         rc = flash_attn_fwd(_dtype_code(q), b, s, h, d, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                             0.0 if scale is None else float(scale), causal, d_status, stream)

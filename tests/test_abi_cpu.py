@@ -280,3 +280,44 @@ def test_workspace_pool_queries_without_a_device(lib):
         pytest.skip("checks the no-device answers")
     assert gt.gemm_tn_workspace_pool() is None
     assert gt.gemm_tn_trim_workspace() in (gt.GEMM_TN_ERR_UNSUPPORTED_DEVICE, gt.GEMM_TN_ERR_CUDA)
+
+
+def test_binding_refuses_a_status_word_it_cannot_hand_to_a_kernel():
+    """The kernels write an int through the status pointer: only a contiguous
+    int32 tensor on the call's device is passed down."""
+    import torch
+
+    from dense_tiled_gemm_03_gb300._native import _status_ptr
+
+    cpu = torch.device("cpu")
+    assert _status_ptr(None, cpu) is None
+    word = torch.zeros(1, dtype=torch.int32)
+    assert _status_ptr(word, cpu) == word.data_ptr()
+    with pytest.raises(ValueError):
+        _status_ptr(word, torch.device("cuda", 0))                     # host memory for a device call
+    with pytest.raises(ValueError):
+        _status_ptr(torch.zeros(1, dtype=torch.int64), cpu)             # wrong width
+    with pytest.raises(ValueError):
+        _status_ptr(torch.zeros(0, dtype=torch.int32), cpu)             # no element
+    with pytest.raises(ValueError):
+        _status_ptr(torch.zeros(4, dtype=torch.int32)[::2], cpu)        # not contiguous
+
+
+def test_host_entry_binding_checks_shapes_before_any_device_call():
+    """mm_tn_host writes M x N elements into `out`: shapes and dtypes are
+    checked before the library (or a device) is touched."""
+    import torch
+
+    a = torch.zeros(4, 8, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        gt.mm_tn_host(a, torch.zeros(5, 7, dtype=torch.float16))        # K differs
+    with pytest.raises(TypeError):
+        gt.mm_tn_host(a, torch.zeros(5, 8, dtype=torch.bfloat16))       # dtypes differ
+    with pytest.raises(ValueError):
+        gt.mm_tn_host(a, torch.zeros(5, 8, dtype=torch.float16), out=torch.empty(4, 4, dtype=torch.float16))
+    with pytest.raises(ValueError):
+        gt.mm_tn_host(a, torch.zeros(5, 8, dtype=torch.float16), out=torch.empty(4, 5, dtype=torch.float32))
+    with pytest.raises(ValueError):
+        gt.mm_tn_host(a, torch.zeros(5, 8, dtype=torch.float16), out=torch.empty(5, 4, dtype=torch.float16).t())
+    with pytest.raises(ValueError):
+        gt.mm_tn_host(a[0], torch.zeros(5, 8, dtype=torch.float16))     # not 2-D
